@@ -1,0 +1,140 @@
+"""ORACLE: test infrastructure, not part of the library.
+
+Python access to the fp64 C oracle in ``oracle.c`` (a plain m/n/k loop over
+bf16 inputs decoded exactly, from "How I made Muse's GPU projections 1.32×
+faster in the Open Kernel Challenge", section "The full equation, now with the
+letters explained").  Only the tests, the smoke check and the benchmark's
+CPU-baseline leg may import this package.  It never imports the CUDA library
+and the CUDA library never imports it.
+
+All array arguments are numpy uint16 bf16 bit patterns; results are float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import subprocess
+import tempfile
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = None
+
+W_NK, W_KN = 0, 1
+
+
+def lib_path() -> str:
+    # ORACLE_LIB lets the mutation test load a deliberately broken build.
+    return os.environ.get("ORACLE_LIB") or os.path.join(
+        _HERE, f"_oracle.{platform.machine()}.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (-O2, OpenMP, no fast-math) next to this file."""
+    out = lib_path()
+    if os.environ.get("ORACLE_LIB"):
+        return out
+    if (not force and os.path.exists(out)
+            and os.path.getmtime(out) >= os.path.getmtime(_SRC)):
+        return out
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    # -ffp-contract=off: each product and each sum is its own rounded fp64 op,
+    # exactly as the loop is written (no fused multiply-add reassociation).
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
+           "-o", tmp, _SRC]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        lib = ctypes.CDLL(build())
+        i64, vp = ctypes.c_int64, ctypes.c_void_p
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = ctypes.c_double
+        lib.oracle_project.argtypes = [i64, i64, i64, vp, vp, ctypes.c_int, vp, vp]
+        lib.oracle_project.restype = None
+        lib.oracle_project_cells.argtypes = [i64, i64, i64, vp, vp, ctypes.c_int, vp,
+                                             i64, vp, vp, vp]
+        lib.oracle_project_cells.restype = None
+        lib.oracle_max_threads.restype = ctypes.c_int
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
+        _LIB = lib
+    return _LIB
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns (uint16)")
+    return a
+
+
+def _shapes(X, W, w_layout):
+    M, K = X.shape
+    if w_layout == W_NK:
+        N, K2 = W.shape
+    elif w_layout == W_KN:
+        K2, N = W.shape
+    else:
+        raise ValueError("w_layout must be 0 ([N,K]) or 1 ([K,N])")
+    if K2 != K:
+        raise ValueError(f"K mismatch: X has {K}, W has {K2}")
+    return M, N, K
+
+
+def bf16_to_double(bits) -> np.ndarray:
+    """Decode bf16 bit patterns one by one through the oracle's own decoder."""
+    lib = _lib()
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([lib.oracle_bf16_to_double(int(b)) for b in flat],
+                    dtype=np.float64).reshape(np.shape(bits))
+
+
+def project(X, W, w_layout: int = W_NK, bias=None) -> np.ndarray:
+    """fp64 ``Y[m,n] = Σ_k X[m,k]·W(n,k) (+ bias[n])`` for the whole problem."""
+    X, W = _u16(X), _u16(W)
+    M, N, K = _shapes(X, W, w_layout)
+    b = None if bias is None else _u16(bias)
+    if b is not None and b.shape != (N,):
+        raise ValueError("bias must have shape [N]")
+    Y = np.empty((M, N), dtype=np.float64)
+    if M and N:
+        _lib().oracle_project(M, N, K, X.ctypes.data, W.ctypes.data, int(w_layout),
+                              None if b is None else b.ctypes.data, Y.ctypes.data)
+    return Y
+
+
+def project_cells(X, W, w_layout: int, bias, ms, ns) -> np.ndarray:
+    """fp64 output cells at coordinates ``(ms[i], ns[i])``."""
+    X, W = _u16(X), _u16(W)
+    M, N, K = _shapes(X, W, w_layout)
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    if ms.shape != ns.shape or ms.ndim != 1:
+        raise ValueError("ms and ns must be equal-length 1-D arrays")
+    if ms.size and (ms.min() < 0 or ms.max() >= M or ns.min() < 0 or ns.max() >= N):
+        raise IndexError("cell coordinate out of range")
+    b = None if bias is None else _u16(bias)
+    out = np.empty(ms.size, dtype=np.float64)
+    if ms.size:
+        _lib().oracle_project_cells(M, N, K, X.ctypes.data, W.ctypes.data,
+                                    int(w_layout), None if b is None else b.ctypes.data,
+                                    ms.size, ms.ctypes.data, ns.ctypes.data,
+                                    out.ctypes.data)
+    return out
+
+
+def max_threads() -> int:
+    return int(_lib().oracle_max_threads())
+
+
+def set_threads(n: int) -> None:
+    _lib().oracle_set_threads(int(n))
