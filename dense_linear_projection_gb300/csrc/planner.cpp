@@ -1,0 +1,199 @@
+// Host planner: cuts one projection problem into GPU work.  Pure host code (no
+// CUDA calls), so it is exercised on machines without a GPU.
+//
+// Design points, with the worklog sections that motivate them ("How I made
+// Muse's GPU projections 1.32× faster in the Open Kernel Challenge"):
+//  * Enough independent work ("Having lots of workers doesn't help if I give
+//    them nothing to do", "Enough active work, with enough resources"): the
+//    grid is one CTA per SM, each CTA owning a deep shared-memory pipeline;
+//    when there are fewer output tiles than SMs the K reduction is split
+//    ("My first useful win: split up the sum").
+//  * Block count arithmetic ("How splitting changes the grid"):
+//    tiles = ceil(M/BT) · ceil(N/BN).
+//  * Integer partition of K blocks ("Why the later TMA/WGMMA kernel was a new
+//    experiment": 128 tiles over 3 splits → 42/43/43): CTA c owns units
+//    [⌊c·U/G⌋, ⌊(c+1)·U/G⌋) so every unit is covered exactly once.
+//  * Tile shape: the swapped product Yᵀ = W·Xᵀ ("Prove the swapped product
+//    before worrying about its speed") puts 128 weight rows on the MMA's M
+//    side and the token rows (16..256) on its N side, so small M does not
+//    waste a 128-row MMA dimension.
+#include "proj_internal.h"
+
+#include <cstdio>
+
+namespace {
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int32_t pow2_ceil(int32_t v) {
+    int32_t p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+}  // namespace
+
+namespace projgb {
+
+int32_t token_tile_for(int64_t M) {
+    if (M >= kMaxTokenTile) return kMaxTokenTile;
+    int64_t bt = ceil_div(M < 1 ? 1 : M, 16) * 16;
+    return static_cast<int32_t>(bt < 16 ? 16 : bt);
+}
+
+int32_t stage_bytes_for(int32_t block_t) {
+    return kBlockN * kBlockK * 2 + block_t * kBlockK * 2;
+}
+
+}  // namespace projgb
+
+using namespace projgb;
+
+extern "C" proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K,
+                                           proj_wlayout_t w_layout, proj_dtype_t y_dtype,
+                                           int has_bias, const proj_device_desc_t *dev,
+                                           proj_plan_desc_t *out) {
+    if (!dev || !out) return PROJ_ERR_INVALID_ARG;
+    *out = proj_plan_desc_t{};
+    if (M < 0 || N < 0 || K < 0) return PROJ_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return PROJ_ERR_UNSUPPORTED;
+    if (w_layout != PROJ_W_NK && w_layout != PROJ_W_KN) return PROJ_ERR_INVALID_ARG;
+    if (y_dtype != PROJ_BF16 && y_dtype != PROJ_F32) return PROJ_ERR_INVALID_ARG;
+    if (has_bias != 0 && has_bias != 1) return PROJ_ERR_INVALID_ARG;
+    if (dev->sm_count < 1) return PROJ_ERR_INVALID_ARG;
+
+    out->block_n = kBlockN;
+    out->block_k = kBlockK;
+    out->threads = kThreads;
+    if (M == 0 || N == 0) {
+        out->kernel = PROJ_KERNEL_NONE;
+        return PROJ_OK;
+    }
+    if (K == 0) {
+        out->kernel = PROJ_KERNEL_FILL;
+        out->grid = static_cast<int32_t>(ceil_div(M * N, 256) < dev->sm_count * 8
+                                             ? ceil_div(M * N, 256)
+                                             : dev->sm_count * 8);
+        out->threads = 256;
+        return PROJ_OK;
+    }
+
+    const int32_t bt = token_tile_for(M);
+    const int32_t stage = stage_bytes_for(bt);
+    const int32_t budget = dev->smem_optin_bytes - kSmemReserve;
+    int32_t stages = budget / stage;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return PROJ_ERR_UNSUPPORTED;
+
+    out->kernel = PROJ_KERNEL_TC;
+    out->block_t = bt;
+    out->stages = stages;
+    out->smem_bytes = stages * stage + kSmemReserve;
+    // Two accumulator buffers (the epilogue of one tile overlaps the MMAs of
+    // the next); TMEM is allocated in powers of two, at least 32 columns.
+    out->tmem_cols = pow2_ceil(2 * bt < 32 ? 32 : 2 * bt);
+
+    out->tiles_m = ceil_div(M, bt);
+    out->tiles_n = ceil_div(N, kBlockN);
+    out->k_blocks = ceil_div(K, kBlockK);
+    const int64_t tiles = out->tiles_m * out->tiles_n;
+    const int64_t units = tiles * out->k_blocks;
+    const int64_t grid = units < dev->sm_count ? units : dev->sm_count;
+    out->grid = static_cast<int32_t>(grid);
+    out->tiles_dp = (tiles / grid) * grid;
+    out->tiles_sk = tiles - out->tiles_dp;
+    out->units_sk = out->tiles_sk * out->k_blocks;
+
+    // Scratch: one partial tile per (CTA, first|last split segment), one
+    // completion counter per (split tile, 32-row quarter), and the device
+    // status word.
+    int64_t partial_bytes = 0;
+    if (out->tiles_sk > 0) partial_bytes = 2 * grid * int64_t(bt) * kBlockN * 4;
+    const int64_t counter_bytes = ((out->tiles_sk * 4 * 4 + 255) / 256) * 256;
+    out->scratch_bytes = partial_bytes + counter_bytes + 256;
+    (void)has_bias;
+    return PROJ_OK;
+}
+
+static bool plan_is_tc(const proj_plan_desc_t *plan) {
+    return plan && plan->kernel == PROJ_KERNEL_TC && plan->grid > 0 && plan->k_blocks > 0 &&
+           plan->tiles_m > 0;
+}
+
+extern "C" proj_status_t proj_plan_segments(const proj_plan_desc_t *plan, int32_t cta,
+                                            proj_segment_t *out, int64_t cap, int64_t *count) {
+    if (!count || (cap > 0 && !out) || cap < 0) return PROJ_ERR_INVALID_ARG;
+    *count = 0;
+    if (!plan) return PROJ_ERR_INVALID_ARG;
+    if (plan->kernel != PROJ_KERNEL_TC) return PROJ_OK;
+    if (!plan_is_tc(plan) || cta < 0 || cta >= plan->grid) return PROJ_ERR_INVALID_ARG;
+    KernelParams kp{};
+    params_from_plan(*plan, kp);
+    WorkIter it;
+    it.init(kp, cta);
+    Segment s;
+    int64_t n = 0;
+    while (it.next(kp, s)) {
+        if (n < cap) {
+            proj_segment_t &o = out[n];
+            o.tile = s.tile;
+            o.tile_m = s.tile % kp.tiles_m;
+            o.tile_n = s.tile / kp.tiles_m;
+            o.k_block_begin = s.kb0;
+            o.k_block_end = s.kb1;
+            o.slot = s.slot;
+            o.split = s.split ? 1 : 0;
+            o.reserved = 0;
+        }
+        ++n;
+    }
+    *count = n;
+    return PROJ_OK;
+}
+
+extern "C" proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t split_tile,
+                                                   int32_t *ctas, int32_t *slots, int64_t cap,
+                                                   int64_t *count) {
+    if (!count || cap < 0 || (cap > 0 && (!ctas || !slots))) return PROJ_ERR_INVALID_ARG;
+    *count = 0;
+    if (!plan_is_tc(plan) || split_tile < 0 || split_tile >= plan->tiles_sk)
+        return PROJ_ERR_INVALID_ARG;
+    const int32_t ts = static_cast<int32_t>(split_tile);
+    const int32_t kt = static_cast<int32_t>(plan->k_blocks);
+    int32_t first, last;
+    split_tile_ctas(ts, kt, plan->units_sk, plan->grid, first, last);
+    int64_t n = 0;
+    for (int32_t c = first; c <= last; ++c) {
+        if (!cta_has_units(c, plan->units_sk, plan->grid)) continue;
+        if (n < cap) {
+            ctas[n] = c;
+            slots[n] = split_slot(c, ts, plan->units_sk, plan->grid, kt);
+        }
+        ++n;
+    }
+    *count = n;
+    return PROJ_OK;
+}
+
+namespace projgb {
+
+int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int w_layout,
+                 int y_dtype, int has_bias, char *buf, size_t len) {
+    static const char *kernels[] = {"none", "fill", "tc_tma_tcgen05"};
+    const char *kname = (p.kernel >= 0 && p.kernel <= 2) ? kernels[p.kernel] : "?";
+    return std::snprintf(
+        buf, len,
+        "{\"kernel\": \"%s\", \"M\": %lld, \"N\": %lld, \"K\": %lld, \"w_layout\": \"%s\", "
+        "\"y_dtype\": \"%s\", \"bias\": %s, \"block_n\": %d, \"block_t\": %d, \"block_k\": %d, "
+        "\"stages\": %d, \"grid\": %d, \"threads\": %d, \"smem_bytes\": %d, "
+        "\"tmem_cols\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
+        "\"tiles_dp\": %lld, \"tiles_sk\": %lld, \"units_sk\": %lld, \"scratch_bytes\": %lld}",
+        kname, (long long)M, (long long)N, (long long)K, w_layout == PROJ_W_NK ? "NK" : "KN",
+        y_dtype == PROJ_F32 ? "f32" : "bf16", has_bias ? "true" : "false", p.block_n,
+        p.block_t, p.block_k, p.stages, p.grid, p.threads, p.smem_bytes, p.tmem_cols,
+        (long long)p.tiles_m, (long long)p.tiles_n, (long long)p.k_blocks,
+        (long long)p.tiles_dp, (long long)p.tiles_sk, (long long)p.units_sk,
+        (long long)p.scratch_bytes);
+}
+
+}  // namespace projgb

@@ -1,0 +1,323 @@
+// C ABI of the GB300 dense projection library: handle lifecycle, argument
+// checks, TMA descriptor encoding and kernel launches.  See include/proj.h for
+// the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "proj.h"
+#include "proj_internal.h"
+#include "proj_kernel.cuh"
+
+using namespace projgb;
+
+struct proj_plan_s {
+    int device = 0;
+    int64_t M = 0, N = 0, K = 0;
+    int w_layout = PROJ_W_NK;
+    int y_dtype = PROJ_BF16;
+    int has_bias = 0;
+    proj_plan_desc_t plan{};
+    KernelParams params{};
+    void *scratch = nullptr;
+    // Tensor maps cached by base pointer (rebuilt when X or W moves).
+    const void *map_x_ptr = nullptr;
+    const void *map_w_ptr = nullptr;
+    CUtensorMap map_x;  // CUtensorMap carries its own 64-byte alignment
+    CUtensorMap map_w;
+    // Device staging for proj_run_host (allocated on first use).
+    void *stage_x = nullptr;
+    void *stage_y = nullptr;
+};
+
+namespace {
+
+constexpr int64_t kDefaultWaitLimitNs = 1000000000LL;  // 1 s
+
+cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows,
+// rows `row_bytes` apart, box [box_inner, box_outer], 128-byte swizzle,
+// out-of-range elements read as zero.
+bool encode_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint32_t make_idesc(int mma_m, int mma_n, bool a_mn_major) {
+    // tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5),
+    // bf16 A (7-9) and B (10-12), A major-ness (15), B K-major (16 = 0),
+    // N >> 3 (17-22), M >> 4 (24-28).
+    uint32_t d = 0;
+    d |= 1u << 4;
+    d |= 1u << 7;
+    d |= 1u << 10;
+    if (a_mn_major) d |= 1u << 15;
+    d |= static_cast<uint32_t>(mma_n >> 3) << 17;
+    d |= static_cast<uint32_t>(mma_m >> 4) << 24;
+    return d;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+proj_status_t check_launch() {
+    return cudaGetLastError() == cudaSuccess ? PROJ_OK : PROJ_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *proj_status_string(proj_status_t s) {
+    switch (s) {
+        case PROJ_OK: return "PROJ_OK";
+        case PROJ_ERR_INVALID_ARG: return "PROJ_ERR_INVALID_ARG";
+        case PROJ_ERR_UNSUPPORTED: return "PROJ_ERR_UNSUPPORTED";
+        case PROJ_ERR_MISALIGNED: return "PROJ_ERR_MISALIGNED";
+        case PROJ_ERR_OUT_OF_MEMORY: return "PROJ_ERR_OUT_OF_MEMORY";
+        case PROJ_ERR_CUDA: return "PROJ_ERR_CUDA";
+        case PROJ_ERR_DEVICE_TIMEOUT: return "PROJ_ERR_DEVICE_TIMEOUT";
+    }
+    return "PROJ_ERR_UNKNOWN";
+}
+
+proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
+                          proj_wlayout_t w_layout, proj_dtype_t x_dtype, proj_dtype_t w_dtype,
+                          proj_dtype_t y_dtype, int has_bias, proj_dtype_t bias_dtype, void *stream) {
+    if (!out) return PROJ_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (M < 0 || N < 0 || K < 0) return PROJ_ERR_INVALID_ARG;
+    if (w_layout != PROJ_W_NK && w_layout != PROJ_W_KN) return PROJ_ERR_INVALID_ARG;
+    if (has_bias != 0 && has_bias != 1) return PROJ_ERR_INVALID_ARG;
+    if (y_dtype != PROJ_BF16 && y_dtype != PROJ_F32) return PROJ_ERR_INVALID_ARG;
+    if (x_dtype != PROJ_BF16 || w_dtype != PROJ_BF16) return PROJ_ERR_UNSUPPORTED;
+    if (has_bias && bias_dtype != PROJ_BF16) return PROJ_ERR_UNSUPPORTED;
+    if (K % 8 != 0) return PROJ_ERR_MISALIGNED;
+    if (w_layout == PROJ_W_KN && N % 8 != 0) return PROJ_ERR_MISALIGNED;
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return PROJ_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return PROJ_ERR_CUDA;
+    if (prop.major != 10 || prop.minor != 3) return PROJ_ERR_UNSUPPORTED;  // built for sm_103a
+
+    proj_device_desc_t dd{prop.multiProcessorCount, static_cast<int32_t>(prop.sharedMemPerBlockOptin)};
+    proj_plan_desc_t plan;
+    proj_status_t st = proj_plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, &plan);
+    if (st != PROJ_OK) return st;
+
+    proj_plan_s *h = new (std::nothrow) proj_plan_s();
+    if (!h) return PROJ_ERR_OUT_OF_MEMORY;
+    h->device = device;
+    h->M = M;
+    h->N = N;
+    h->K = K;
+    h->w_layout = w_layout;
+    h->y_dtype = y_dtype;
+    h->has_bias = has_bias;
+    h->plan = plan;
+
+    if (plan.kernel == PROJ_KERNEL_TC) {
+        if (cudaMalloc(&h->scratch, static_cast<size_t>(plan.scratch_bytes)) != cudaSuccess) {
+            cudaGetLastError();
+            delete h;
+            return PROJ_ERR_OUT_OF_MEMORY;
+        }
+        const int64_t partial_bytes =
+            plan.tiles_sk > 0 ? int64_t(2) * plan.grid * plan.block_t * kBlockN * 4 : 0;
+        uint8_t *sc = static_cast<uint8_t *>(h->scratch);
+        KernelParams &kp = h->params;
+        kp.M = static_cast<int32_t>(M);
+        kp.N = static_cast<int32_t>(N);
+        kp.K = static_cast<int32_t>(K);
+        params_from_plan(plan, kp);
+        kp.idesc = make_idesc(kBlockN, plan.block_t, w_layout == PROJ_W_KN);
+        kp.w_kn = w_layout == PROJ_W_KN;
+        kp.y_f32 = y_dtype == PROJ_F32;
+        kp.wait_limit_ns = kDefaultWaitLimitNs;
+        kp.partials = reinterpret_cast<float *>(sc);
+        kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);
+        kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
+        // Counters and the status word start at zero; partials need no clearing.
+        if (cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(plan.scratch_bytes - partial_bytes),
+                            as_stream(stream)) != cudaSuccess ||
+            cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 plan.smem_bytes) != cudaSuccess ||
+            cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(h->scratch);
+            delete h;
+            return PROJ_ERR_CUDA;
+        }
+    }
+    *out = h;
+    return PROJ_OK;
+}
+
+proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void *bias, void *Y,
+                       void *stream) {
+    if (!h) return PROJ_ERR_INVALID_ARG;
+    if ((bias != nullptr) != (h->has_bias != 0)) return PROJ_ERR_INVALID_ARG;
+    const proj_plan_desc_t &plan = h->plan;
+    if (plan.kernel == PROJ_KERNEL_NONE) return PROJ_OK;
+    if (!Y) return PROJ_ERR_INVALID_ARG;
+    const size_t y_align = h->y_dtype == PROJ_F32 ? 4 : 2;
+    if (reinterpret_cast<uintptr_t>(Y) % y_align != 0) return PROJ_ERR_MISALIGNED;
+    if (bias && reinterpret_cast<uintptr_t>(bias) % 2 != 0) return PROJ_ERR_MISALIGNED;
+    cudaStream_t s = as_stream(stream);
+
+    if (plan.kernel == PROJ_KERNEL_FILL) {
+        dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(
+            h->M, h->N, static_cast<const uint16_t *>(bias), Y, h->y_dtype == PROJ_F32);
+        return check_launch();
+    }
+
+    if (!X || !W) return PROJ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W)) return PROJ_ERR_MISALIGNED;
+    if (X != h->map_x_ptr) {
+        if (!encode_2d(&h->map_x, X, h->K, h->M, h->K * 2, kBlockK, plan.block_t)) {
+            h->map_x_ptr = nullptr;
+            return PROJ_ERR_CUDA;
+        }
+        h->map_x_ptr = X;
+    }
+    if (W != h->map_w_ptr) {
+        const bool ok = h->w_layout == PROJ_W_NK
+                            ? encode_2d(&h->map_w, W, h->K, h->N, h->K * 2, kBlockK, kBlockN)
+                            : encode_2d(&h->map_w, W, h->N, h->K, h->N * 2, 64, kBlockK);
+        if (!ok) {
+            h->map_w_ptr = nullptr;
+            return PROJ_ERR_CUDA;
+        }
+        h->map_w_ptr = W;
+    }
+    KernelParams kp = h->params;
+    kp.bias = static_cast<const uint16_t *>(bias);
+    kp.Y = Y;
+    dev::proj_tc_kernel<<<plan.grid, plan.threads, plan.smem_bytes, s>>>(kp, h->map_w, h->map_x);
+    return check_launch();
+}
+
+proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W, const void *bias,
+                            void *Y_host, void *stream) {
+    if (!h) return PROJ_ERR_INVALID_ARG;
+    if (h->plan.kernel == PROJ_KERNEL_NONE) return PROJ_OK;
+    if (!Y_host || (!X_host && h->K > 0)) return PROJ_ERR_INVALID_ARG;
+    const size_t xb = static_cast<size_t>(h->M) * h->K * 2;
+    const size_t yb = static_cast<size_t>(h->M) * h->N * (h->y_dtype == PROJ_F32 ? 4 : 2);
+    if (!h->stage_y) {
+        if (xb && cudaMalloc(&h->stage_x, xb) != cudaSuccess) {
+            cudaGetLastError();
+            return PROJ_ERR_OUT_OF_MEMORY;
+        }
+        if (cudaMalloc(&h->stage_y, yb) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(h->stage_x);
+            h->stage_x = nullptr;
+            return PROJ_ERR_OUT_OF_MEMORY;
+        }
+    }
+    cudaStream_t s = as_stream(stream);
+    if (xb && cudaMemcpyAsync(h->stage_x, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return PROJ_ERR_CUDA;
+    proj_status_t st = proj_run(h, h->stage_x, W, bias, h->stage_y, stream);
+    if (st != PROJ_OK) return st;
+    if (cudaMemcpyAsync(Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PROJ_ERR_CUDA;
+    return PROJ_OK;
+}
+
+proj_status_t proj_device_status(proj_handle_t h, void *stream) {
+    if (!h) return PROJ_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return PROJ_ERR_CUDA;
+    if (h->plan.kernel != PROJ_KERNEL_TC) return PROJ_OK;
+    int word = 0;
+    if (cudaMemcpy(&word, h->params.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PROJ_ERR_CUDA;
+    if (word == 0) return PROJ_OK;
+    // Clear the word and the split-K counters (a run that gave up may have
+    // left some mid-count) so the handle is usable again.
+    const proj_plan_desc_t &plan = h->plan;
+    const int64_t partial_bytes =
+        plan.tiles_sk > 0 ? int64_t(2) * plan.grid * plan.block_t * kBlockN * 4 : 0;
+    if (cudaMemset(static_cast<uint8_t *>(h->scratch) + partial_bytes, 0,
+                   static_cast<size_t>(plan.scratch_bytes - partial_bytes)) != cudaSuccess)
+        return PROJ_ERR_CUDA;
+    return PROJ_ERR_DEVICE_TIMEOUT;
+}
+
+proj_status_t proj_get_plan(proj_handle_t h, proj_plan_desc_t *out) {
+    if (!h || !out) return PROJ_ERR_INVALID_ARG;
+    *out = h->plan;
+    return PROJ_OK;
+}
+
+proj_status_t proj_plan_info(proj_handle_t h, char *buf, size_t len) {
+    if (!h || !buf || len == 0) return PROJ_ERR_INVALID_ARG;
+    plan_to_json(h->plan, h->M, h->N, h->K, h->w_layout, h->y_dtype, h->has_bias, buf, len);
+    return PROJ_OK;
+}
+
+proj_status_t proj_destroy(proj_handle_t h) {
+    if (!h) return PROJ_OK;
+    proj_status_t st = PROJ_OK;
+    if (h->scratch && cudaFree(h->scratch) != cudaSuccess) st = PROJ_ERR_CUDA;
+    if (h->stage_x && cudaFree(h->stage_x) != cudaSuccess) st = PROJ_ERR_CUDA;
+    if (h->stage_y && cudaFree(h->stage_y) != cudaSuccess) st = PROJ_ERR_CUDA;
+    delete h;
+    return st;
+}
+
+proj_status_t proj_selftest_wait_timeout(int64_t limit_ns, void *stream) {
+    if (limit_ns < 1000 || limit_ns > 1000000000LL) return PROJ_ERR_INVALID_ARG;
+    int *word = nullptr;
+    if (cudaMalloc(&word, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return PROJ_ERR_OUT_OF_MEMORY;
+    }
+    cudaStream_t s = as_stream(stream);
+    proj_status_t st = PROJ_OK;
+    int host_word = 0;
+    if (cudaMemsetAsync(word, 0, sizeof(int), s) != cudaSuccess) st = PROJ_ERR_CUDA;
+    if (st == PROJ_OK) {
+        dev::proj_selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns, word);
+        st = check_launch();
+    }
+    if (st == PROJ_OK && (cudaMemcpyAsync(&host_word, word, sizeof(int), cudaMemcpyDeviceToHost, s) !=
+                              cudaSuccess ||
+                          cudaStreamSynchronize(s) != cudaSuccess))
+        st = PROJ_ERR_CUDA;
+    cudaFree(word);
+    if (st != PROJ_OK) return st;
+    return host_word == kErrSelfTest ? PROJ_ERR_DEVICE_TIMEOUT : PROJ_OK;
+}
+
+}  // extern "C"

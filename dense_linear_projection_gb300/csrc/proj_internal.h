@@ -1,0 +1,165 @@
+// Internal definitions shared by the planner, the C ABI and the device code.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "proj.h"
+
+#if defined(__CUDACC__)
+#define PROJ_HD __host__ __device__ __forceinline__
+#else
+#define PROJ_HD inline
+#endif
+
+namespace projgb {
+
+constexpr int32_t kBlockN = 128;       // weight rows per tile = tcgen05 MMA M
+constexpr int32_t kBlockK = 64;        // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int32_t kMmaK = 16;          // K per tcgen05.mma (kind::f16)
+constexpr int32_t kMaxTokenTile = 256; // tcgen05 MMA N limit for cta_group::1
+constexpr int32_t kMaxStages = 12;
+constexpr int32_t kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int32_t kEpilogueThreads = 128;
+constexpr int32_t kSmemReserve = 2048; // 1024-byte alignment slack + barriers
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+// Error bits in the device status word.
+constexpr int kErrWaitProducer = 1 << 0;
+constexpr int kErrWaitMma = 1 << 1;
+constexpr int kErrWaitEpilogue = 1 << 2;
+constexpr int kErrWaitDrain = 1 << 3;
+constexpr int kErrSelfTest = 1 << 4;
+
+int32_t token_tile_for(int64_t M);
+int32_t stage_bytes_for(int32_t block_t);
+int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int w_layout,
+                 int y_dtype, int has_bias, char *buf, size_t len);
+
+// Kernel parameters (passed by value; the tensor maps travel separately as
+// __grid_constant__ arguments).
+struct KernelParams {
+    int32_t M, N, K;
+    int32_t block_t;       // token rows per tile (MMA N)
+    int32_t tiles_m;       // tiles along M; tile t -> (tm = t % tiles_m, tn = t / tiles_m)
+    int32_t k_blocks;
+    int32_t tiles_dp;      // whole tiles, dealt round-robin: CTA c gets c, c+G, ...
+    int32_t grid;
+    int64_t units_sk;      // split-K units after the whole tiles
+    int32_t stages;
+    int32_t stage_bytes;
+    int32_t tmem_cols;
+    uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128, N=block_t)
+    int32_t w_kn;          // W stored [K,N] (MN-major A operand)
+    int32_t y_f32;         // store fp32 (else bf16)
+    int64_t wait_limit_ns; // bounded device waits give up after this long
+    const uint16_t *bias;  // [N] bf16 or nullptr
+    void *Y;
+    float *partials;       // [2*grid][block_t][128] fp32
+    uint32_t *counters;    // [4 * (tiles - tiles_dp)]: one per (split tile, row quarter)
+    int *status;           // device status word
+};
+
+// ----------------------------------------------------------------------------
+// Work decomposition, shared verbatim by the kernel (every role walks the same
+// sequence) and by the host introspection entry points (so the CPU tests check
+// the exact code the GPU runs).
+// ----------------------------------------------------------------------------
+struct Segment {
+    int32_t tile;   // tile index; tm = tile % tiles_m, tn = tile / tiles_m
+    int32_t kb0;    // first k-block
+    int32_t kb1;    // one past the last k-block
+    int32_t slot;   // partial-sum slot (split segments), else -1
+    bool split;     // the tile's K range is shared with other CTAs
+};
+
+// First split-K unit of CTA c: ⌊c·U/G⌋ (the integer partition that splits 128
+// k-blocks over 3 CTAs as 42/43/43).
+PROJ_HD int64_t unit_begin(int32_t c, int64_t U, int32_t G) {
+    return static_cast<int64_t>(c) * U / G;
+}
+
+// The CTA whose unit range contains unit u: the largest c with ⌊c·U/G⌋ ≤ u.
+PROJ_HD int32_t cta_of_unit(int64_t u, int64_t U, int32_t G) {
+    return static_cast<int32_t>(((u + 1) * G + U - 1) / U - 1);
+}
+
+// CTAs whose unit ranges touch split tile ts: [first, last] (some in between
+// may own no units at all when there are fewer units than CTAs).
+PROJ_HD void split_tile_ctas(int32_t ts, int32_t k_blocks, int64_t U, int32_t G, int32_t &first,
+                             int32_t &last) {
+    const int64_t x0 = static_cast<int64_t>(ts) * k_blocks;
+    first = cta_of_unit(x0, U, G);
+    last = cta_of_unit(x0 + k_blocks - 1, U, G);
+}
+
+PROJ_HD bool cta_has_units(int32_t c, int64_t U, int32_t G) {
+    return unit_begin(c, U, G) < unit_begin(c + 1, U, G);
+}
+
+// Partial-sum slot of CTA c's segment of split tile ts: 2c for the first tile
+// of c's unit range, 2c + 1 for the last (a range spans at most one partial
+// tile at each end; tiles it covers whole are never split).
+PROJ_HD int32_t split_slot(int32_t c, int32_t ts, int64_t U, int32_t G, int32_t k_blocks) {
+    return 2 * c + (ts == static_cast<int32_t>(unit_begin(c, U, G) / k_blocks) ? 0 : 1);
+}
+
+struct WorkIter {
+    int32_t cta;
+    int32_t dp_next;
+    int64_t u, u_end;
+    int32_t first_sk_tile;
+
+    PROJ_HD void init(const KernelParams &p, int32_t c) {
+        cta = c;
+        dp_next = c;
+        u = unit_begin(c, p.units_sk, p.grid);
+        u_end = unit_begin(c + 1, p.units_sk, p.grid);
+        first_sk_tile = static_cast<int32_t>(u / p.k_blocks);
+    }
+
+    // Whole tiles first (c, c+G, ... below tiles_dp), then this CTA's split-K
+    // units, cut at tile boundaries.
+    PROJ_HD bool next(const KernelParams &p, Segment &s) {
+        if (dp_next < p.tiles_dp) {
+            s.tile = dp_next;
+            s.kb0 = 0;
+            s.kb1 = p.k_blocks;
+            s.slot = -1;
+            s.split = false;
+            dp_next += p.grid;
+            return true;
+        }
+        if (u < u_end) {
+            const int32_t ts = static_cast<int32_t>(u / p.k_blocks);
+            const int32_t kb0 = static_cast<int32_t>(u - static_cast<int64_t>(ts) * p.k_blocks);
+            const int64_t left = u_end - u;
+            const int32_t kb1 = left < static_cast<int64_t>(p.k_blocks - kb0)
+                                    ? kb0 + static_cast<int32_t>(left)
+                                    : p.k_blocks;
+            s.tile = p.tiles_dp + ts;
+            s.kb0 = kb0;
+            s.kb1 = kb1;
+            s.split = (kb0 != 0) || (kb1 != p.k_blocks);
+            s.slot = s.split ? 2 * cta + (ts == first_sk_tile ? 0 : 1) : -1;
+            u += kb1 - kb0;
+            return true;
+        }
+        return false;
+    }
+};
+
+// Work-shape fields of the kernel parameters, from a plan.
+inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
+    kp.block_t = plan.block_t;
+    kp.tiles_m = static_cast<int32_t>(plan.tiles_m);
+    kp.k_blocks = static_cast<int32_t>(plan.k_blocks);
+    kp.tiles_dp = static_cast<int32_t>(plan.tiles_dp);
+    kp.grid = plan.grid;
+    kp.units_sk = plan.units_sk;
+    kp.stages = plan.stages;
+    kp.stage_bytes = stage_bytes_for(plan.block_t);
+    kp.tmem_cols = plan.tmem_cols;
+}
+
+}  // namespace projgb

@@ -1,0 +1,529 @@
+// Device code of the GB300 dense projection Y = X·Wᵀ (+ bias).
+//
+// One persistent kernel, one CTA per SM, warp-specialised:
+//   warp 0      TMA producer: streams W tiles [128 rows × 64 K] and X tiles
+//               [block_t rows × 64 K] (128-byte swizzle) into a ring of
+//               shared-memory stages ("How I made Muse's GPU projections 1.32×
+//               faster in the Open Kernel Challenge", section "How a pipeline
+//               hides waiting": load the next tile while computing this one).
+//   warp 1      allocates tensor memory and issues tcgen05.mma (bf16 × bf16 →
+//               fp32) for the swapped product Yᵀ = W·Xᵀ (section "Prove the
+//               swapped product before worrying about its speed"): weight rows
+//               are the MMA's M = 128 side, token rows its N = block_t side, so
+//               a handful of tokens still fills the tensor core's long side.
+//   warps 2..5  epilogue: tensor memory → registers → (+ bias) → fp32/bf16 Y,
+//               or → fp32 partial sums for a tile whose K range is split.
+//
+// Stage hand-off uses "full" and "empty" mbarriers with phase parity (section
+// "A transfer being issued does not mean the data is ready": ready-to-read and
+// safe-to-reuse are separate signals).  Accumulators are double-buffered in
+// tensor memory so one tile's epilogue overlaps the next tile's MMAs.
+//
+// Split-K (section "My first useful win: split up the sum"): CTAs that share a
+// tile write fp32 partials to scratch and bump a per-(tile, 32-row quarter)
+// counter; the warp that arrives last adds the partials in ascending CTA order
+// (= ascending K), adds the bias and stores Y.  The fixed order makes every
+// run bit-identical; no floating-point atomics are used (section "Could I avoid
+// reading all those router partials back?" shows why those are not).  The
+// counter returns to zero inside the run (section "Why a last-block scheme was
+// more complicated than it sounded": every replay needs a fresh counter).
+//
+// Every mbarrier wait is bounded in time; a wait that runs out records a bit in
+// the device status word, raises a CTA-wide abort flag, drains in-flight copies
+// and MMAs (again bounded), frees tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "proj_internal.h"
+
+namespace projgb {
+namespace dev {
+
+// ----------------------------------------------------------------------------
+// PTX wrappers
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity to complete.
+// Returns false (and raises the CTA abort flag, recording `code` in the status
+// word) if `limit_ns` passes, or false at once if another role aborted.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           int *status, int code, int64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (static_cast<int64_t>(globaltimer_ns() - t0) > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(status, code);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_prefetch_map(const void *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled TMA load into shared memory, completing on `bar` (transaction bytes).
+// x is the innermost (contiguous) coordinate.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint32_t bar, int32_t x,
+                                            int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] · B[smem]ᵀ, kind::f16 (bf16 operands, fp32 accumulate).
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 op this thread issued so far completes.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+// Load 16 consecutive fp32 columns of this thread's tensor-memory lane and wait
+// for them (the wait sits in the same asm block so no use can move above it).
+__device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (tcgen05 format), 128-byte swizzle.
+// lbo/sbo in bytes: for K-major tiles sbo is the 8-row group stride (1024);
+// for MN-major tiles lbo is the stride between 64-element MN blocks and sbo
+// the stride between 8-row K groups.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;  // swizzle mode: 128-byte
+    return d;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// ----------------------------------------------------------------------------
+// Shared-memory layout
+// ----------------------------------------------------------------------------
+struct SmemCtl {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// ----------------------------------------------------------------------------
+// The kernel
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    proj_tc_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ CUtensorMap tmap_w,
+                   const __grid_constant__ CUtensorMap tmap_x) {
+    extern __shared__ uint8_t smem_raw[];
+    // Stage buffers need 1024-byte alignment (128-byte swizzle atoms).
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base_addr - raw_addr);
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + p.stages * p.stage_bytes);
+    volatile int *abort_flag = &ctl->abort_flag;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const int32_t stages = p.stages;
+    const uint32_t a_bytes = kBlockN * kBlockK * 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+            mbar_init(smem_u32(&ctl->acc_empty[b]), kEpilogueThreads / 32);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_map(&tmap_w);
+        tma_prefetch_map(&tmap_x);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(p.tmem_cols));
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = ctl->tmem_base;
+    const uint32_t half_cols = static_cast<uint32_t>(p.tmem_cols / 2);
+
+    int64_t issued = 0;  // producer: stage loads issued (for the abort drain)
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = l2_policy_evict_first();  // W is read once
+            const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
+            const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
+            int32_t stage = 0;
+            uint32_t phase = 0;
+            WorkIter it;
+            it.init(p, blockIdx.x);
+            Segment s;
+            bool ok = true;
+            while (ok && it.next(p, s)) {
+                const int32_t tm = s.tile % p.tiles_m;
+                const int32_t tn = s.tile / p.tiles_m;
+                for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.status,
+                                    kErrWaitProducer, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = smem_u32(&ctl->full[stage]);
+                    const uint32_t a_dst = base_addr + stage * stage_bytes;
+                    const uint32_t b_dst = a_dst + a_bytes;
+                    mbar_arrive_expect_tx(full, stage_bytes);
+                    if (!p.w_kn) {
+                        tma_load_2d(a_dst, &tmap_w, full, kb * kBlockK, tn * kBlockN, pol_w);
+                    } else {
+                        tma_load_2d(a_dst, &tmap_w, full, tn * kBlockN, kb * kBlockK, pol_w);
+                        tma_load_2d(a_dst + a_bytes / 2, &tmap_w, full, tn * kBlockN + 64,
+                                    kb * kBlockK, pol_w);
+                    }
+                    tma_load_2d(b_dst, &tmap_x, full, kb * kBlockK, tm * p.block_t, pol_x);
+                    ++issued;
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int32_t stage = 0;
+            uint32_t phase = 0;
+            int32_t seg_idx = 0;
+            WorkIter it;
+            it.init(p, blockIdx.x);
+            Segment s;
+            bool ok = true;
+            while (ok && it.next(p, s)) {
+                const int32_t buf = seg_idx & 1;
+                const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+                if (!wait_phase(smem_u32(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, p.status,
+                                kErrWaitMma, p.wait_limit_ns))
+                    break;
+                tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * half_cols;
+                for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
+                    if (!wait_phase(smem_u32(&ctl->full[stage]), phase, abort_flag, p.status,
+                                    kErrWaitMma, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_addr = base_addr + stage * static_cast<uint32_t>(p.stage_bytes);
+                    const uint32_t b_addr = a_addr + a_bytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBlockK / kMmaK; ++kk) {
+                        // K-major: the next 16 K values start 32 bytes further
+                        // along the 128-byte swizzled row.  MN-major (W stored
+                        // [K,N]): 16 more K rows, 16 × 128 bytes further.
+                        const uint64_t a_desc =
+                            p.w_kn ? smem_desc_sw128(a_addr + kk * (kMmaK * 128), a_bytes / 2, 1024)
+                                   : smem_desc_sw128(a_addr + kk * (kMmaK * 2), 16, 1024);
+                        const uint64_t b_desc = smem_desc_sw128(b_addr + kk * (kMmaK * 2), 16, 1024);
+                        tc_mma(d_tmem, a_desc, b_desc, p.idesc, (kb > s.kb0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&ctl->empty[stage]));  // stage free once these MMAs finish
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&ctl->acc_full[buf]));  // accumulator ready
+                ++seg_idx;
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;              // tensor-memory lane quarter of this warp
+        const int r = q * 32 + lane;         // row within the 128-row weight tile
+        const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const int64_t U = p.units_sk;
+        int32_t seg_idx = 0;
+        WorkIter it;
+        it.init(p, blockIdx.x);
+        Segment s;
+        while (it.next(p, s)) {
+            const int32_t buf = seg_idx & 1;
+            const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+            if (!wait_phase(smem_u32(&ctl->acc_full[buf]), use, abort_flag, p.status,
+                            kErrWaitEpilogue, p.wait_limit_ns))
+                break;
+            tc_fence_after_sync();
+            const int32_t tm = s.tile % p.tiles_m;
+            const int32_t tn = s.tile / p.tiles_m;
+            const int32_t n = tn * kBlockN + r;
+            const int32_t m0 = tm * p.block_t;
+            const int32_t mcount = min(p.block_t, p.M - m0);
+            const int32_t nchunks = (mcount + 15) / 16;
+            const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(buf) * half_cols;
+            const bool n_ok = n < p.N;
+            const float bias_v = (p.bias != nullptr && n_ok) ? bf16_bits_to_float(p.bias[n]) : 0.f;
+
+            if (!s.split) {
+                for (int32_t ch = 0; ch < nchunks; ++ch) {
+                    float v[16];
+                    tmem_load16(tbase + ch * 16, v);
+                    if (n_ok) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int32_t m = m0 + ch * 16 + i;
+                            if (m < p.M) {
+                                const float y = v[i] + bias_v;
+                                const size_t off = static_cast<size_t>(m) * p.N + n;
+                                if (p.y_f32)
+                                    static_cast<float *>(p.Y)[off] = y;
+                                else
+                                    static_cast<__nv_bfloat16 *>(p.Y)[off] = __float2bfloat16_rn(y);
+                            }
+                        }
+                    }
+                }
+            } else {
+                float *part = p.partials + static_cast<size_t>(s.slot) * p.block_t * kBlockN;
+                for (int32_t ch = 0; ch < nchunks; ++ch) {
+                    float v[16];
+                    tmem_load16(tbase + ch * 16, v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) part[(ch * 16 + i) * kBlockN + r] = v[i];
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+
+            if (s.split) {
+                // Publish this warp's 32 rows of partials, then count arrivals.
+                const int32_t ts = s.tile - p.tiles_dp;
+                int32_t c_first, c_last;
+                split_tile_ctas(ts, p.k_blocks, U, p.grid, c_first, c_last);
+                int32_t nseg = 0;
+                for (int32_t c = c_first; c <= c_last; ++c) nseg += cta_has_units(c, U, p.grid) ? 1 : 0;
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                uint32_t *ctr = p.counters + static_cast<size_t>(ts) * 4 + q;
+                if (lane == 0) {
+                    const uint32_t old = atomicAdd(ctr, 1u);
+                    last = (old == static_cast<uint32_t>(nseg - 1)) ? 1 : 0;
+                    if (last) atomicExch(ctr, 0u);  // fresh for the next run
+                    __threadfence();
+                }
+                last = __shfl_sync(0xFFFFFFFFu, last, 0);
+                if (last) {
+                    for (int32_t ch = 0; ch < nchunks; ++ch) {
+                        float acc[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                        for (int32_t c = c_first; c <= c_last; ++c) {
+                            if (!cta_has_units(c, U, p.grid)) continue;
+                            const int32_t slot = split_slot(c, ts, U, p.grid, p.k_blocks);
+                            const float *pc =
+                                p.partials + static_cast<size_t>(slot) * p.block_t * kBlockN;
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] += __ldcg(pc + (ch * 16 + i) * kBlockN + r);
+                        }
+                        if (n_ok) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const int32_t m = m0 + ch * 16 + i;
+                                if (m < p.M) {
+                                    const float y = acc[i] + bias_v;
+                                    const size_t off = static_cast<size_t>(m) * p.N + n;
+                                    if (p.y_f32)
+                                        static_cast<float *>(p.Y)[off] = y;
+                                    else
+                                        static_cast<__nv_bfloat16 *>(p.Y)[off] = __float2bfloat16_rn(y);
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            ++seg_idx;
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (*abort_flag) {
+        // Let every copy and MMA already in flight land before the CTA leaves.
+        if (warp == 0 && lane == 0) {
+            for (int32_t st = 0; st < stages; ++st) {
+                const int64_t times = issued > st ? (issued - 1 - st) / stages + 1 : 0;
+                if (times > 0) {
+                    volatile int never = 0;
+                    wait_phase(smem_u32(&ctl->full[st]), static_cast<uint32_t>((times - 1) & 1),
+                               &never, p.status, kErrWaitDrain, p.wait_limit_ns);
+                }
+            }
+        }
+        if (warp == 1 && lane == 0) {
+            tc_commit(smem_u32(&ctl->drain));
+            volatile int never = 0;
+            wait_phase(smem_u32(&ctl->drain), 0, &never, p.status, kErrWaitDrain, p.wait_limit_ns);
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+    }
+}
+
+// K == 0: every sum is empty, so Y = bias (or 0).
+__global__ void proj_fill_kernel(int64_t M, int64_t N, const uint16_t *bias, void *Y, int y_f32) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t n = i % N;
+        const float y = bias ? bf16_bits_to_float(bias[n]) : 0.f;
+        if (y_f32)
+            static_cast<float *>(Y)[i] = y;
+        else
+            static_cast<__nv_bfloat16 *>(Y)[i] = __float2bfloat16_rn(y);
+    }
+}
+
+// Self-test of the bounded wait: a barrier nothing arrives on.
+__global__ void proj_selftest_wait_kernel(int64_t limit_ns, int *status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool ok = wait_phase(smem_u32(&bar), 0, &abort_flag, status, kErrSelfTest, limit_ns);
+        if (ok) atomicOr(status, 1 << 30);  // would mean the wait completed: it must not
+    }
+}
+
+}  // namespace dev
+}  // namespace projgb

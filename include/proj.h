@@ -1,0 +1,245 @@
+/*
+ * proj.h: C ABI of the GB300 dense projection library (libproj_gb300).
+ *
+ * Computes the dense projection of transformer inference
+ *
+ *     Y[m, n] = Σ_{k=0}^{K-1} X[m, k] · W[n, k]   (+ bias[n])
+ *
+ * ("How I made Muse's GPU projections 1.32× faster in the Open Kernel
+ * Challenge", section "The full equation, now with the letters explained";
+ * the bias makes it the affine map of section "What makes it linear?").
+ * X is [M, K] token activations, W holds N rows of K weights, Y is [M, N].
+ * Products are bf16 × bf16 with fp32 accumulation; the output is stored as
+ * fp32 or rounded once to bf16 (round-to-nearest-even), after the bias is
+ * added (section "Inputs, products, accumulators, and outputs are separate
+ * choices").
+ *
+ * Memory and ownership
+ *   - Every tensor pointer passed to proj_run is a DEVICE pointer owned by the
+ *     caller (e.g. allocated by PyTorch).  The library never frees or keeps
+ *     them beyond the call, apart from caching the tensor-map descriptors
+ *     built from them.
+ *   - Streams are owned by the caller and passed as `void*` holding a
+ *     cudaStream_t (NULL means the legacy default stream).
+ *   - A handle owns its plan, its split-K scratch (partial sums, completion
+ *     counters) and a device status word.  proj_create allocates them once;
+ *     proj_run allocates nothing, never synchronises the host and may be
+ *     captured into a CUDA graph.  Scratch partial sums are fully rewritten
+ *     before they are read and counters return to zero inside every run, so
+ *     no memset is needed between runs.
+ *   - One handle must not run on two streams at the same time (its scratch is
+ *     shared).  Different handles are independent.
+ *
+ * Layouts (section "What a matrix looks like in memory")
+ *   X: [M, K] row-major, K contiguous, bf16.
+ *   W: PROJ_W_NK: [N, K] row-major, element (n,k) at n·K + k.
+ *      PROJ_W_KN: the copied transpose [K, N], element (n,k) at k·N + n.
+ *   bias: [N] bf16 or NULL.   Y: [M, N] row-major, fp32 or bf16.
+ *
+ * Alignment (TMA global strides and addresses must be 16-byte multiples):
+ *   X and W base addresses 16-byte aligned; K % 8 == 0 (X rows and [N,K]
+ *   weight rows are whole 16-byte multiples); for PROJ_W_KN also N % 8 == 0.
+ *   Violations return PROJ_ERR_MISALIGNED and launch nothing.
+ *
+ * Errors: every call returns a proj_status_t; nothing aborts or throws across
+ * the ABI.  CUDA launch failures surface as PROJ_ERR_CUDA.  Device-side waits
+ * are bounded (about one second); a wait that runs out records itself in the
+ * handle's status word, the kernel returns early, and proj_device_status
+ * reports PROJ_ERR_DEVICE_TIMEOUT.
+ *
+ * Determinism: for one handle and the same inputs every run writes the same
+ * bytes.  The split of K across CTAs is fixed when the handle is planned, and
+ * partial sums are combined in a fixed order (no floating-point atomics).
+ */
+#ifndef PROJ_GB300_PROJ_H
+#define PROJ_GB300_PROJ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct proj_plan_s *proj_handle_t;
+
+typedef enum proj_status {
+    PROJ_OK = 0,
+    PROJ_ERR_INVALID_ARG = 1,    /* bad shape, NULL pointer, bias/has_bias mismatch */
+    PROJ_ERR_UNSUPPORTED = 2,    /* dtype or device this build does not handle */
+    PROJ_ERR_MISALIGNED = 3,     /* a TMA alignment rule above is violated */
+    PROJ_ERR_OUT_OF_MEMORY = 4,  /* scratch allocation failed */
+    PROJ_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed */
+    PROJ_ERR_DEVICE_TIMEOUT = 6  /* a bounded device-side wait ran out */
+} proj_status_t;
+
+typedef enum proj_dtype { PROJ_BF16 = 0, PROJ_F32 = 1 } proj_dtype_t;
+
+typedef enum proj_wlayout { PROJ_W_NK = 0, PROJ_W_KN = 1 } proj_wlayout_t;
+
+/* Which device code a plan runs. */
+typedef enum proj_kernel {
+    PROJ_KERNEL_NONE = 0,  /* M == 0 or N == 0: nothing to compute */
+    PROJ_KERNEL_FILL = 1,  /* K == 0: every sum is empty, Y = bias (or 0) */
+    PROJ_KERNEL_TC = 2     /* TMA + tcgen05/TMEM persistent projection kernel */
+} proj_kernel_t;
+
+/*
+ * Device properties the planner needs.  Filled from cudaGetDeviceProperties by
+ * proj_create; tests may pass their own (the planner is pure host code).
+ */
+typedef struct proj_device_desc {
+    int32_t sm_count;           /* streaming multiprocessors (152 on GB300) */
+    int32_t smem_optin_bytes;   /* max dynamic shared memory per block (opt-in) */
+} proj_device_desc_t;
+
+/*
+ * A plan: how one problem is cut into work for the GPU.
+ *
+ * Tiles: block_n weight rows (the tensor-core MMA's M side, which carries the
+ * output features: the swapped product Yᵀ = W·Xᵀ, section "Prove the swapped
+ * product before worrying about its speed") × block_t token rows (the MMA's
+ * N side) × the whole K range, cut into k_blocks blocks of block_k.
+ * Whole tiles are dealt out in data-parallel waves (tiles_dp, a multiple of
+ * grid); the remaining tiles_sk tiles are split along K into units_sk
+ * k-block units shared contiguously by all CTAs ("split-K", section "My first
+ * useful win: split up the sum"; CTA c takes units
+ * [⌊c·U/G⌋, ⌊(c+1)·U/G⌋), the integer partition of section "Why the later
+ * TMA/WGMMA kernel was a new experiment" that splits 128 tiles 42/43/43).
+ */
+typedef struct proj_plan_desc {
+    int32_t kernel;          /* proj_kernel_t */
+    int32_t block_n;         /* weight rows per tile (128) */
+    int32_t block_t;         /* token rows per tile: 16..256, multiple of 16 */
+    int32_t block_k;         /* K elements per pipeline stage (64 = 128 bytes) */
+    int32_t stages;          /* shared-memory pipeline depth */
+    int32_t grid;            /* CTAs launched (one per SM at most) */
+    int32_t threads;         /* threads per CTA */
+    int32_t smem_bytes;      /* dynamic shared memory per CTA */
+    int32_t tmem_cols;       /* tensor-memory columns allocated per CTA */
+    int32_t reserved0;
+    int64_t tiles_m;         /* ceil(M / block_t) */
+    int64_t tiles_n;         /* ceil(N / block_n) */
+    int64_t k_blocks;        /* ceil(K / block_k) */
+    int64_t tiles_dp;        /* tiles computed whole, tiles_dp % grid == 0 */
+    int64_t tiles_sk;        /* tiles split along K across CTAs */
+    int64_t units_sk;        /* tiles_sk * k_blocks */
+    int64_t scratch_bytes;   /* device scratch the handle owns */
+} proj_plan_desc_t;
+
+/*
+ * Plan a problem without touching a GPU (pure host code).
+ * Returns PROJ_ERR_INVALID_ARG for negative sizes, a bad layout, or a NULL
+ * dev/out; PROJ_ERR_UNSUPPORTED if the device cannot hold two pipeline stages.
+ */
+proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
+                                proj_dtype_t y_dtype, int has_bias,
+                                const proj_device_desc_t *dev, proj_plan_desc_t *out);
+
+/* One stretch of work a CTA executes: k-blocks [k_block_begin, k_block_end)
+ * of one tile (tile = tile_n · tiles_m + tile_m). */
+typedef struct proj_segment {
+    int32_t tile;
+    int32_t tile_m;          /* token-row tile */
+    int32_t tile_n;          /* weight-row tile */
+    int32_t k_block_begin;
+    int32_t k_block_end;
+    int32_t slot;            /* partial-sum slot when split, else -1 */
+    int32_t split;           /* 1 if other CTAs own the rest of this tile's K range */
+    int32_t reserved;
+} proj_segment_t;
+
+/*
+ * Host introspection of a PROJ_KERNEL_TC plan (pure host code, the same
+ * decomposition code the kernel runs): the segments CTA `cta` executes, in
+ * order.  Writes min(cap, total) segments to `out` and the total to *count.
+ * A plan of another kernel kind yields zero segments.  PROJ_ERR_INVALID_ARG
+ * for a NULL count/plan, a negative cap, or cta outside [0, grid).
+ */
+proj_status_t proj_plan_segments(const proj_plan_desc_t *plan, int32_t cta, proj_segment_t *out,
+                                 int64_t cap, int64_t *count);
+
+/*
+ * The order in which the partial sums of split tile `split_tile`
+ * (0 ≤ split_tile < tiles_sk; tile index tiles_dp + split_tile) are added:
+ * contributing CTAs in ascending order with their partial-sum slots.  Writes
+ * min(cap, total) pairs and the total to *count.
+ */
+proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t split_tile,
+                                        int32_t *ctas, int32_t *slots, int64_t cap,
+                                        int64_t *count);
+
+/*
+ * Create a handle for one problem shape on the current CUDA device.
+ *   M, N, K ≥ 0 (a zero M or N plans nothing; K == 0 plans Y = bias or 0).
+ *   x_dtype, w_dtype, bias_dtype: PROJ_BF16 only (else PROJ_ERR_UNSUPPORTED).
+ *   y_dtype: PROJ_BF16 or PROJ_F32.   has_bias: 0 or 1.
+ *   stream: cudaStream_t used to clear the new scratch; create synchronises it
+ *   before returning, so the handle may be used on any stream afterwards.
+ * Allocates scratch with cudaMalloc (PROJ_ERR_OUT_OF_MEMORY on failure).
+ * The device must be compute capability 10.3 (GB300); else PROJ_ERR_UNSUPPORTED.
+ * On failure *out is set to NULL.
+ */
+proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
+                          proj_wlayout_t w_layout, proj_dtype_t x_dtype,
+                          proj_dtype_t w_dtype, proj_dtype_t y_dtype, int has_bias,
+                          proj_dtype_t bias_dtype, void *stream);
+
+/*
+ * Enqueue Y = X·Wᵀ (+ bias) on `stream`.  X, W, bias, Y are device pointers
+ * with the layouts above; bias must be NULL iff the handle has no bias.
+ * Asynchronous: returns once the launch is queued.  No allocation, no host
+ * synchronisation; safe inside CUDA-graph capture.
+ */
+proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void *bias,
+                       void *Y, void *stream);
+
+/*
+ * Same projection with HOST activations: copies X_host ([M,K] bf16) to a
+ * device staging buffer, runs, and copies Y back to Y_host, all on `stream`.
+ * W and bias stay device pointers (weights are resident, as after a
+ * preparation step).  X_host / Y_host should be pinned for the copies to be
+ * asynchronous; Y_host is valid once `stream` has been synchronised.  The
+ * staging buffers are allocated by the first call on a handle (so that first
+ * call is not capturable) and reused afterwards.
+ */
+proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W,
+                            const void *bias, void *Y_host, void *stream);
+
+/*
+ * Synchronise `stream` and read the handle's device status word.  Returns
+ * PROJ_ERR_DEVICE_TIMEOUT if a bounded device wait ran out in any earlier run
+ * (the word and the split-K counters are then cleared so the handle can be
+ * reused), PROJ_ERR_CUDA if the synchronisation failed, else PROJ_OK.
+ */
+proj_status_t proj_device_status(proj_handle_t h, void *stream);
+
+/* Copy the handle's plan. */
+proj_status_t proj_get_plan(proj_handle_t h, proj_plan_desc_t *out);
+
+/*
+ * Write a one-line JSON description of the plan into buf (NUL-terminated,
+ * truncated to len).  PROJ_ERR_INVALID_ARG for a NULL handle or buffer.
+ */
+proj_status_t proj_plan_info(proj_handle_t h, char *buf, size_t len);
+
+/* Free the handle and its scratch (synchronises the device).  NULL is a no-op. */
+proj_status_t proj_destroy(proj_handle_t h);
+
+/* Static human-readable name of a status code (never NULL). */
+const char *proj_status_string(proj_status_t s);
+
+/*
+ * Self-test of the bounded device wait: launch one CTA that waits on a
+ * shared-memory barrier nothing ever arrives on, with a limit of
+ * `limit_ns` nanoseconds (1 µs .. 1 s).  The wait gives up, the kernel writes
+ * its status and returns; the call synchronises `stream` and returns
+ * PROJ_ERR_DEVICE_TIMEOUT when the timeout path worked (PROJ_OK would mean
+ * the wait did not give up).  No fault, trap or hang is involved.
+ */
+proj_status_t proj_selftest_wait_timeout(int64_t limit_ns, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PROJ_GB300_PROJ_H */
