@@ -1,0 +1,510 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 dense projection Y = X·Wᵀ (+ bias).
+
+One step = one call of the whole hot path (proj_run: weight stream, multiply-
+accumulate, split-K reduction, bias and bf16 epilogue) over one batch of
+synthetic inputs.  The default workload is the decode projection
+X [16,8192] · W [8192,8192]ᵀ + bias → bf16 Y, the M=16, K=8192 shape the
+metric is quoted on.
+
+Measurement (methodology of "How I made Muse's GPU projections 1.32× faster in
+the Open Kernel Challenge", section "How I checked whether an idea was actually
+faster": CUDA-graph replay, cold L2, fresh weights):
+  * inputs are resident in HBM; W rotates over enough copies that the copies
+    together exceed twice the L2, so every step streams W from HBM;
+  * the K timed steps are replayed from CUDA graphs, timed with CUDA events on
+    the launching stream, bracketed by a barrier and device synchronisation,
+    max over ranks;
+  * e2e repeats the K steps through proj_run_host (X copied host→device and Y
+    device→host every step, pinned buffers; W stays resident);
+  * the fp64 oracle is timed on the host cores as the CPU baseline;
+  * nvidia-smi clocks are sampled while the GPU is under load.
+
+Multi-GPU: independent replicas (one per rank, no collective on the data path);
+``value`` is the aggregate over ranks ("scaling": "weak").
+
+``--impl reference`` times the fp64 CPU oracle as the reference arm instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "projection µs & weight HBM GB/s (M=16,K=8192) / TFLOP/s at M≥512 vs roofline"
+DEFAULT_WORKLOAD = "decode_bias"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+CSRC_DIR = os.path.join(ROOT, "dense_linear_projection_gb300", "csrc")
+
+
+# ---------------------------------------------------------------- pure helpers
+def roofline_time_s(bytes_moved: float, flops: float, bw_bytes_per_s: float,
+                    flops_per_s: float) -> float:
+    """Lower bound on time: the slower of moving the bytes and doing the FLOPs
+    (section "A rough way to ask how much room was left": t ≥ max(F/P, B/Q))."""
+    return max(bytes_moved / bw_bytes_per_s, flops / flops_per_s)
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC_DIR)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(CSRC_DIR, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def profile_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this workload,
+    or None if there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(PROFILE_DIR, f"proj_tc_kernel_{workload}.md")
+    try:
+        text = open(path, encoding="utf-8").read()
+    except OSError:
+        return None, None
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`")
+        if ":" in line and line.split(":", 1)[0] in ("traffic_bytes_per_launch",
+                                                    "kernel_source_sha256"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_source_sha256") != kernel_source_hash():
+        return None, os.path.relpath(path, ROOT)
+    try:
+        return int(fields["traffic_bytes_per_launch"]), os.path.relpath(path, ROOT)
+    except (KeyError, ValueError):
+        return None, os.path.relpath(path, ROOT)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_over_ranks(value: float, op: str, device=None) -> float:
+    """max/sum of a host scalar over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, seconds_per_rank: float, device=None) -> dict:
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    t_max = reduce_over_ranks(seconds_per_rank, "max", device)
+    units = reduce_over_ranks(units_per_rank, "sum", device)
+    return {"seconds": t_max, "units": units, "per_second": units / t_max if t_max > 0 else 0.0}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) of SM clocks and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.out_path = None
+
+    def start(self):
+        import tempfile
+        fd, self.out_path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.out_path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.out_path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.out_path)
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows) -> dict:
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    sm, mx, reasons, power = [], [], set(), []
+    for r in rows:
+        try:
+            sm.append(float(r[1]))
+            mx.append(float(r[2]))
+            power.append(float(r[3]))
+        except ValueError:
+            continue
+        for i, nm in enumerate(names):
+            if r[5 + i].lower().startswith("active"):
+                reasons.add(nm)
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None,
+            "power_w_max": max(power) if power else None,
+            "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def visible_gpu_id(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------- CPU oracle
+def cpu_oracle_timing(w, inp, target_s: float) -> dict:
+    """Time the fp64 oracle on the host cores on a bounded sample of the
+    workload: all M token rows against the first n_cols output columns (or the
+    whole workload, repeated, if that is quick).  Returns weight GB/s."""
+    import numpy as np
+    import oracle
+    threads = oracle.max_threads()
+    X, W, b = inp["X"], inp["W"], inp["bias"]
+
+    def cols_slice(nc):
+        if w.w_layout == 0:
+            return np.ascontiguousarray(W[:nc]), None if b is None else b[:nc]
+        return np.ascontiguousarray(W[:, :nc]), None if b is None else b[:nc]
+
+    probe = min(w.N, 64)
+    Wp, bp = cols_slice(probe)
+    t0 = time.perf_counter()
+    oracle.project(X[: min(w.M, 256)], Wp, w.w_layout, bp)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    per_col = dt / probe * (w.M / min(w.M, 256))
+    n_cols = int(max(1, min(w.N, target_s / per_col)))
+    reps = 1
+    if n_cols == w.N:
+        reps = max(1, min(10, int(target_s / max(per_col * w.N, 1e-6))))
+    Ws, bs = cols_slice(n_cols)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.project(X, Ws, w.w_layout, bs)
+    elapsed = time.perf_counter() - t0
+    wbytes = 2.0 * n_cols * w.K * reps
+    sample = (f"all {w.M} token rows x {n_cols} of {w.N} output columns"
+              + (f", {reps} repetitions" if reps > 1 else "") + f", {elapsed:.2f} s")
+    return {"value": wbytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": sample, "seconds": elapsed}
+
+
+# ---------------------------------------------------------------- GPU arm
+def run_gpu_arm(args) -> dict:
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import dense_linear_projection_gb300 as dlp
+    import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    w = synth.workload(args.workload, args.m)
+    inp = synth.make_inputs(w)
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+    X, W0 = dev_bf16(inp["X"]), dev_bf16(inp["W"])
+    bias = dev_bf16(inp["bias"]) if w.has_bias else None
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    n_copies = max(2, math.ceil(2 * l2 / w.weight_bytes) + 1)
+    Ws = [W0] + [W0.clone() for _ in range(n_copies - 1)]
+    y_dt = torch.float32 if w.y_dtype == "f32" else torch.bfloat16
+    Y = torch.empty((w.M, w.N), dtype=y_dt, device=device)
+    # Weights are resident and constant (prepared once), so each step may start
+    # streaming W while the previous step finishes; X, bias, scratch and Y are
+    # touched only after it completes.
+    overlap = {"none": dlp.PROJ_OVERLAP_NONE, "prologue": dlp.PROJ_OVERLAP_PROLOGUE,
+               "weights": dlp.PROJ_OVERLAP_WEIGHTS}[args.overlap]
+    proj = dlp.Projection(w.M, w.N, w.K, w.w_layout,
+                          dlp.PROJ_F32 if w.y_dtype == "f32" else dlp.PROJ_BF16, w.has_bias,
+                          overlap=overlap)
+    stream = torch.cuda.Stream(device)
+
+    # Graphs of back-to-back steps, each step on the next W copy.
+    def capture(nsteps, offset):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                proj(X, Ws[(offset + i) % n_copies], bias, out=Y, stream=stream)
+        return g
+
+    with torch.cuda.stream(stream):
+        proj(X, W0, bias, out=Y, stream=stream)  # first call encodes the tensor maps
+    torch.cuda.synchronize()
+    chunk = n_copies * max(1, 64 // n_copies)
+    g_chunk = capture(chunk, 0)
+    rem = args.steps % chunk
+    g_rem = capture(rem, 0) if rem else None
+
+    def run_steps(k):
+        """Replay exactly k steps (k = the timed step count, or whole chunks)."""
+        for _ in range(k // chunk):
+            g_chunk.replay()
+        if k % chunk:
+            assert g_rem is not None and k % chunk == rem
+            g_rem.replay()
+
+    sampler = ClockSampler(visible_gpu_id(local)).start()
+    with torch.cuda.stream(stream):
+        run_steps(chunk * math.ceil(args.warmup / chunk))  # at least `warmup` steps
+        # Untimed soak so the clock sampler sees the GPU under load even when
+        # the timed region itself is only milliseconds long.
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < args.soak:
+            run_steps(chunk)
+            torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        run_steps(args.steps)
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    seconds = ev0.elapsed_time(ev1) / 1e3
+    status = proj.status(stream)
+    if status != dlp.PROJ_OK:
+        raise RuntimeError(f"device status after timing: {dlp.proj_status_string(status)}")
+
+    agg = aggregate_throughput(w.weight_bytes * args.steps, seconds, device)
+    t_step = agg["seconds"] / args.steps
+    peaks = load_peaks()
+    traffic, profile_path = profile_traffic(args.workload if args.m is None else
+                                            f"{args.workload}_m{args.m}")
+    hbm_bound = roofline_time_s(w.algorithmic_bytes, w.flops, peaks["hbm_gbs"] * 1e9,
+                                peaks["bf16_tflops"] * 1e12)
+    if w.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9) >= w.flops / (peaks["bf16_tflops"] * 1e12):
+        roof = {"bound": "hbm", "achieved": w.algorithmic_bytes / t_step / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        peak_tf = peaks["bf16_tflops_sustained"] if agg["seconds"] > 1.0 else peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": w.flops / t_step / 1e12, "peak": peak_tf,
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic
+    roof["peak_source"] = ("of measured" if peaks["source"] == "measured" else "of fallback")
+    roof["bytes_per_launch"] = w.algorithmic_bytes
+    roof["flops_per_launch"] = w.flops
+    roof["bound_us"] = hbm_bound * 1e6
+    if profile_path:
+        roof["profile"] = profile_path
+
+    # ---- e2e: the user-facing call with host activations, every step.
+    e2e = None
+    if not args.no_e2e:
+        Xh = torch.from_numpy(np.ascontiguousarray(inp["X"]).view(np.int16)).view(
+            torch.bfloat16).pin_memory()
+        Yh = torch.empty((w.M, w.N), dtype=y_dt).pin_memory()
+        sptr = stream.cuda_stream
+        for i in range(max(3, args.warmup)):
+            dlp.proj_run_host(proj.handle, Xh, Ws[i % n_copies], bias, Yh, sptr)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            dlp.proj_run_host(proj.handle, Xh, Ws[i % n_copies], bias, Yh, sptr)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e_agg = aggregate_throughput(w.weight_bytes * args.steps, e0.elapsed_time(e1) / 1e3,
+                                     device)
+        ybytes = w.M * w.N * (4 if w.y_dtype == "f32" else 2)
+        e2e = {"value": e_agg["per_second"] / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": 2 * w.M * w.K, "d2h_bytes_per_step": ybytes,
+               "us_per_step": e_agg["seconds"] / args.steps * 1e6,
+               "path": "proj_run_host per step (X H2D, kernel, Y D2H; W resident)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_timing(w, inp, args.cpu_seconds)
+        cpu.pop("seconds", None)
+
+    plan = proj.plan
+    line = {
+        "metric": METRIC,
+        "value": agg["per_second"] / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_step * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded SplitMix64/Box-Muller normals, bf16)",
+        "config": {
+            "workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+            "w_layout": "NK" if w.w_layout == 0 else "KN", "bias": w.has_bias,
+            "y_dtype": w.y_dtype, "seed": w.seed,
+            "l2": f"rotating {n_copies} W copies ({n_copies * w.weight_bytes / 2**20:.0f} MiB > "
+                  f"2x L2 of {l2 / 2**20:.0f} MiB); inputs resident in HBM",
+            "timing": "CUDA-graph replay of the K steps, CUDA events on the launching stream",
+            "overlap": f"programmatic dependent launch, mode '{args.overlap}'",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "us_per_call": t_step * 1e6,
+        "tflops": w.flops / t_step / 1e12,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "plan": {k: plan[k] for k in ("kernel", "block_t", "stages", "grid", "tiles_dp",
+                                      "tiles_sk", "units_sk")},
+    }
+    proj.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference_arm(args) -> dict:
+    """The fp64 CPU oracle as the reference implementation, on this arm's
+    workload: every step is a bounded sample (all token rows against a block of
+    output columns) sized so warm-up + timed steps take about a minute."""
+    import numpy as np
+    import oracle
+    import synth
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    w = synth.workload(args.workload, args.m)
+    inp = synth.make_inputs(w)
+    X, W, b = inp["X"], inp["W"], inp["bias"]
+    threads = oracle.max_threads()
+    probe = min(w.N, 32)
+    Wp = W[:probe] if w.w_layout == 0 else np.ascontiguousarray(W[:, :probe])
+    t0 = time.perf_counter()
+    oracle.project(X, Wp, w.w_layout, None if b is None else b[:probe])
+    per_col = max(time.perf_counter() - t0, 1e-6) / probe
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    n_cols = int(max(1, min(w.N, budget / per_col)))
+    Ws = W[:n_cols] if w.w_layout == 0 else np.ascontiguousarray(W[:, :n_cols])
+    bs = None if b is None else b[:n_cols]
+    for _ in range(args.warmup):
+        oracle.project(X, Ws, w.w_layout, bs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.project(X, Ws, w.w_layout, bs)
+    elapsed = time.perf_counter() - t0
+    value = 2.0 * n_cols * w.K * args.steps / elapsed / 1e9
+    sample = f"each step: all {w.M} token rows x {n_cols} of {w.N} output columns"
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64/Box-Muller normals, bf16)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K,
+                   "w_layout": "NK" if w.w_layout == 0 else "KN", "bias": w.has_bias,
+                   "y_dtype": w.y_dtype, "seed": w.seed},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    help="decode_f32out | decode_bias | ffn_up_sweep | qkv_kn_bias | prefill")
+    ap.add_argument("--m", type=int, default=None, help="token rows (overrides the workload's M)")
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of untimed load before timing (clock sampling)")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--overlap", choices=["none", "prologue", "weights"], default="weights",
+                    help="overlap of consecutive steps (programmatic dependent launch)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be positive")
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    line = run_reference_arm(args) if args.impl == "reference" else run_gpu_arm(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

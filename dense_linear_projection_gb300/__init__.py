@@ -26,7 +26,8 @@ __all__ = [
     "proj_plan_compute", "proj_plan_segments", "proj_plan_reduction_order", "proj_create",
     "proj_run", "proj_run_host", "proj_device_status",
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
-    "proj_selftest_wait_timeout", "Projection",
+    "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "TRACE_FIELDS",
+    "PROJ_OVERLAP_NONE", "PROJ_OVERLAP_PROLOGUE", "PROJ_OVERLAP_WEIGHTS", "Projection",
 ]
 
 PROJ_OK, PROJ_ERR_INVALID_ARG, PROJ_ERR_UNSUPPORTED, PROJ_ERR_MISALIGNED = 0, 1, 2, 3
@@ -34,11 +35,12 @@ PROJ_ERR_OUT_OF_MEMORY, PROJ_ERR_CUDA, PROJ_ERR_DEVICE_TIMEOUT = 4, 5, 6
 PROJ_BF16, PROJ_F32 = 0, 1
 PROJ_W_NK, PROJ_W_KN = 0, 1
 PROJ_KERNEL_NONE, PROJ_KERNEL_FILL, PROJ_KERNEL_TC = 0, 1, 2
+PROJ_OVERLAP_NONE, PROJ_OVERLAP_PROLOGUE, PROJ_OVERLAP_WEIGHTS = 0, 1, 2
 
 EXPORTED_SYMBOLS = (
     "proj_plan_compute", "proj_plan_segments", "proj_plan_reduction_order", "proj_create", "proj_run", "proj_run_host", "proj_device_status",
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
-    "proj_selftest_wait_timeout",
+    "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap",
 )
 
 
@@ -108,6 +110,8 @@ def lib() -> ctypes.CDLL:
     L.proj_status_string.argtypes = [st]
     L.proj_status_string.restype = ctypes.c_char_p
     L.proj_selftest_wait_timeout.argtypes = [i64, vp]
+    L.proj_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
+    L.proj_set_overlap.argtypes = [vp, i32]
     for name in EXPORTED_SYMBOLS:
         if name != "proj_status_string":
             getattr(L, name).restype = st
@@ -223,6 +227,20 @@ def proj_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     return int(lib().proj_selftest_wait_timeout(int(limit_ns), _stream(stream)))
 
 
+TRACE_FIELDS = ("entry", "setup", "first_load", "last_load", "first_data", "last_mma",
+                "first_acc", "epilogue_done", "teardown", "smid", "reductions")
+
+
+def proj_set_overlap(h: int, mode: int) -> None:
+    """Overlap with the preceding kernel: PROJ_OVERLAP_NONE / _PROLOGUE / _WEIGHTS."""
+    _check(lib().proj_set_overlap(h, int(mode)), "proj_set_overlap")
+
+
+def proj_set_trace(h: int, buf=None, nbytes: int = 0) -> None:
+    """Point the handle's phase trace at a device buffer (None turns it off)."""
+    _check(lib().proj_set_trace(h, _ptr(buf), int(nbytes)), "proj_set_trace")
+
+
 # ---------------------------------------------------------------- convenience
 class Projection:
     """A planned projection for one shape; call it with PyTorch tensors.
@@ -233,12 +251,15 @@ class Projection:
     """
 
     def __init__(self, M: int, N: int, K: int, w_layout: int = PROJ_W_NK,
-                 y_dtype: int = PROJ_BF16, has_bias: bool = False, stream=None):
+                 y_dtype: int = PROJ_BF16, has_bias: bool = False, stream=None,
+                 overlap: Optional[int] = None):
         import torch  # noqa: F401  (PyTorch provides memory and streams only)
         self.M, self.N, self.K = M, N, K
         self.w_layout, self.y_dtype, self.has_bias = w_layout, y_dtype, bool(has_bias)
         self.handle = proj_create(M, N, K, w_layout, PROJ_BF16, PROJ_BF16, y_dtype, has_bias,
                                   PROJ_BF16, stream)
+        if overlap is not None:
+            proj_set_overlap(self.handle, overlap)
 
     @property
     def plan(self) -> dict:

@@ -49,10 +49,11 @@ int32_t stage_bytes_for(int32_t block_t) {
 
 using namespace projgb;
 
-extern "C" proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K,
-                                           proj_wlayout_t w_layout, proj_dtype_t y_dtype,
-                                           int has_bias, const proj_device_desc_t *dev,
-                                           proj_plan_desc_t *out) {
+namespace projgb {
+
+proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
+                           proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t *dev,
+                           int32_t force_block_t, proj_plan_desc_t *out) {
     if (!dev || !out) return PROJ_ERR_INVALID_ARG;
     *out = proj_plan_desc_t{};
     if (M < 0 || N < 0 || K < 0) return PROJ_ERR_INVALID_ARG;
@@ -78,7 +79,22 @@ extern "C" proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K,
         return PROJ_OK;
     }
 
-    const int32_t bt = token_tile_for(M);
+    int32_t bt = token_tile_for(M);
+    if (force_block_t > 0) {
+        if (force_block_t % 16 != 0 || force_block_t > kMaxTokenTile) return PROJ_ERR_INVALID_ARG;
+        bt = force_block_t;
+    } else {
+        // With more token rows than one tile holds but fewer tiles than SMs,
+        // halve the token tile until every SM has a tile (each extra token
+        // tile rereads the weight tile, mostly from L2, instead of leaving
+        // SMs idle or splitting K three ways).
+        const int64_t tiles_n = ceil_div(N, kBlockN);
+        while (bt > 64 && ceil_div(M, bt) * tiles_n < dev->sm_count) {
+            const int32_t half = static_cast<int32_t>(ceil_div(bt / 2, 16) * 16);
+            if (half >= bt) break;
+            bt = half;
+        }
+    }
     const int32_t stage = stage_bytes_for(bt);
     const int32_t budget = dev->smem_optin_bytes - kSmemReserve;
     int32_t stages = budget / stage;
@@ -100,8 +116,23 @@ extern "C" proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K,
     const int64_t units = tiles * out->k_blocks;
     const int64_t grid = units < dev->sm_count ? units : dev->sm_count;
     out->grid = static_cast<int32_t>(grid);
-    out->tiles_dp = (tiles / grid) * grid;
-    out->tiles_sk = tiles - out->tiles_dp;
+    // Whole tiles in data-parallel waves, except that the last partial wave
+    // and one full wave before it are shared along K by every CTA (the
+    // "data-parallel + two-tile stream-K" hybrid).  Each CTA then owns at
+    // least one tile's worth of K blocks, so a split tile has exactly two
+    // contributors.  With fewer tiles than CTAs everything is split.
+    const int64_t rem = tiles % grid;
+    const int64_t waves = (tiles + grid - 1) / grid;
+    if (tiles < grid) {
+        out->tiles_sk = tiles;
+    } else if (rem == 0 || 20 * tiles >= 19 * waves * grid) {
+        // Whole tiles only: no partial wave, or the partial wave idles less
+        // than 5 % of the SM time, which costs less than splitting K.
+        out->tiles_sk = 0;
+    } else {
+        out->tiles_sk = rem + grid;
+    }
+    out->tiles_dp = tiles - out->tiles_sk;
     out->units_sk = out->tiles_sk * out->k_blocks;
 
     // Scratch: one partial tile per (CTA, first|last split segment), one
@@ -113,6 +144,15 @@ extern "C" proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K,
     out->scratch_bytes = partial_bytes + counter_bytes + 256;
     (void)has_bias;
     return PROJ_OK;
+}
+
+}  // namespace projgb
+
+extern "C" proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K,
+                                           proj_wlayout_t w_layout, proj_dtype_t y_dtype,
+                                           int has_bias, const proj_device_desc_t *dev,
+                                           proj_plan_desc_t *out) {
+    return plan_compute(M, N, K, w_layout, y_dtype, has_bias, dev, 0, out);
 }
 
 static bool plan_is_tc(const proj_plan_desc_t *plan) {

@@ -30,6 +30,8 @@ struct proj_plan_s {
     const void *map_w_ptr = nullptr;
     CUtensorMap map_x;  // CUtensorMap carries its own 64-byte alignment
     CUtensorMap map_w;
+    unsigned long long *trace = nullptr;  // caller's phase-trace buffer, if any
+    int overlap = PROJ_OVERLAP_PROLOGUE;    // programmatic dependent launch mode
     // Device staging for proj_run_host (allocated on first use).
     void *stage_x = nullptr;
     void *stage_y = nullptr;
@@ -131,7 +133,9 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
 
     proj_device_desc_t dd{prop.multiProcessorCount, static_cast<int32_t>(prop.sharedMemPerBlockOptin)};
     proj_plan_desc_t plan;
-    proj_status_t st = proj_plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, &plan);
+    int32_t force_bt = 0;
+    if (const char *e = std::getenv("PROJ_FORCE_BLOCK_T")) force_bt = std::atoi(e);
+    proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, force_bt, &plan);
     if (st != PROJ_OK) return st;
 
     proj_plan_s *h = new (std::nothrow) proj_plan_s();
@@ -222,8 +226,23 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
     KernelParams kp = h->params;
     kp.bias = static_cast<const uint16_t *>(bias);
     kp.Y = Y;
-    dev::proj_tc_kernel<<<plan.grid, plan.threads, plan.smem_bytes, s>>>(kp, h->map_w, h->map_x);
-    return check_launch();
+    kp.trace = h->trace;
+    kp.w_prefetch = h->overlap == PROJ_OVERLAP_WEIGHTS;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = h->overlap == PROJ_OVERLAP_NONE ? 0 : 1;
+    if (cudaLaunchKernelEx(&cfg, dev::proj_tc_kernel, kp, h->map_w, h->map_x) != cudaSuccess) {
+        cudaGetLastError();
+        return PROJ_ERR_CUDA;
+    }
+    return PROJ_OK;
 }
 
 proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W, const void *bias,
@@ -272,6 +291,28 @@ proj_status_t proj_device_status(proj_handle_t h, void *stream) {
                    static_cast<size_t>(plan.scratch_bytes - partial_bytes)) != cudaSuccess)
         return PROJ_ERR_CUDA;
     return PROJ_ERR_DEVICE_TIMEOUT;
+}
+
+proj_status_t proj_set_overlap(proj_handle_t h, proj_overlap_t mode) {
+    if (!h) return PROJ_ERR_INVALID_ARG;
+    if (mode != PROJ_OVERLAP_NONE && mode != PROJ_OVERLAP_PROLOGUE && mode != PROJ_OVERLAP_WEIGHTS)
+        return PROJ_ERR_INVALID_ARG;
+    h->overlap = mode;
+    return PROJ_OK;
+}
+
+proj_status_t proj_set_trace(proj_handle_t h, void *device_buffer, size_t bytes) {
+    if (!h) return PROJ_ERR_INVALID_ARG;
+    if (!device_buffer) {
+        h->trace = nullptr;
+        return PROJ_OK;
+    }
+    if (h->plan.kernel != PROJ_KERNEL_TC) return PROJ_ERR_UNSUPPORTED;
+    const size_t need = static_cast<size_t>(h->plan.grid) * kTraceSlots * sizeof(unsigned long long);
+    if (bytes < need) return PROJ_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(device_buffer) % 8 != 0) return PROJ_ERR_MISALIGNED;
+    h->trace = static_cast<unsigned long long *>(device_buffer);
+    return PROJ_OK;
 }
 
 proj_status_t proj_get_plan(proj_handle_t h, proj_plan_desc_t *out) {

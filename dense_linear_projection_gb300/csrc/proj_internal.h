@@ -24,6 +24,21 @@ constexpr int32_t kEpilogueThreads = 128;
 constexpr int32_t kSmemReserve = 2048; // 1024-byte alignment slack + barriers
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
+// Phase-trace record: kTraceSlots unsigned 64-bit words per CTA, globaltimer
+// nanoseconds unless noted.
+constexpr int kTraceSlots = 16;
+constexpr int kTraceEntry = 0;         // kernel entry (thread 0)
+constexpr int kTraceSetup = 1;         // barriers initialised, tensor memory allocated
+constexpr int kTraceFirstLoad = 2;     // producer issued its first TMA load
+constexpr int kTraceLastLoad = 3;      // producer issued its last TMA load
+constexpr int kTraceFirstData = 4;     // MMA issuer saw the first stage full
+constexpr int kTraceLastMma = 5;       // MMA issuer committed its last accumulator
+constexpr int kTraceFirstAcc = 6;      // epilogue warp 2 received its first accumulator
+constexpr int kTraceEpilogueDone = 7;  // epilogue warp 2 finished every segment
+constexpr int kTraceTeardown = 8;      // all roles joined at the final barrier
+constexpr int kTraceSmid = 9;          // SM the CTA ran on (a number, not a time)
+constexpr int kTraceReductions = 10;   // split tiles epilogue warp 2 reduced (a count)
+
 // Error bits in the device status word.
 constexpr int kErrWaitProducer = 1 << 0;
 constexpr int kErrWaitMma = 1 << 1;
@@ -32,6 +47,11 @@ constexpr int kErrWaitDrain = 1 << 3;
 constexpr int kErrSelfTest = 1 << 4;
 
 int32_t token_tile_for(int64_t M);
+// The planner behind proj_plan_compute; force_block_t > 0 overrides the token
+// tile (tuning only: proj_create takes it from PROJ_FORCE_BLOCK_T).
+proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
+                           proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t *dev,
+                           int32_t force_block_t, proj_plan_desc_t *out);
 int32_t stage_bytes_for(int32_t block_t);
 int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int w_layout,
                  int y_dtype, int has_bias, char *buf, size_t len);
@@ -46,6 +66,8 @@ struct KernelParams {
     int32_t tiles_dp;      // whole tiles, dealt round-robin: CTA c gets c, c+G, ...
     int32_t grid;
     int64_t units_sk;      // split-K units after the whole tiles
+    int32_t sk_pair;       // every CTA owns >= k_blocks units: a split tile has exactly 2 contributors
+    int32_t sk_dense;      // units_sk >= grid: no CTA has an empty unit range
     int32_t stages;
     int32_t stage_bytes;
     int32_t tmem_cols;
@@ -53,11 +75,13 @@ struct KernelParams {
     int32_t w_kn;          // W stored [K,N] (MN-major A operand)
     int32_t y_f32;         // store fp32 (else bf16)
     int64_t wait_limit_ns; // bounded device waits give up after this long
+    int32_t w_prefetch;    // stream the first stages of W before the preceding kernel completes
     const uint16_t *bias;  // [N] bf16 or nullptr
     void *Y;
-    float *partials;       // [2*grid][block_t][128] fp32
+    float *partials;       // [2*grid][128 rows][block_t] fp32 partial tiles
     uint32_t *counters;    // [4 * (tiles - tiles_dp)]: one per (split tile, row quarter)
     int *status;           // device status word
+    unsigned long long *trace;  // [grid][kTraceSlots] phase trace, or nullptr
 };
 
 // ----------------------------------------------------------------------------
@@ -73,15 +97,23 @@ struct Segment {
     bool split;     // the tile's K range is shared with other CTAs
 };
 
+// a / b for 0 ≤ a, 0 < b: a 32-bit division when both fit (the usual case; a
+// 64-bit division is a long software sequence on the GPU).
+PROJ_HD int64_t div_nonneg(int64_t a, int64_t b) {
+    if (a < (int64_t(1) << 32) && b < (int64_t(1) << 32))
+        return static_cast<int64_t>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b));
+    return a / b;
+}
+
 // First split-K unit of CTA c: ⌊c·U/G⌋ (the integer partition that splits 128
 // k-blocks over 3 CTAs as 42/43/43).
 PROJ_HD int64_t unit_begin(int32_t c, int64_t U, int32_t G) {
-    return static_cast<int64_t>(c) * U / G;
+    return div_nonneg(static_cast<int64_t>(c) * U, G);
 }
 
 // The CTA whose unit range contains unit u: the largest c with ⌊c·U/G⌋ ≤ u.
 PROJ_HD int32_t cta_of_unit(int64_t u, int64_t U, int32_t G) {
-    return static_cast<int32_t>(((u + 1) * G + U - 1) / U - 1);
+    return static_cast<int32_t>(div_nonneg((u + 1) * G + U - 1, U) - 1);
 }
 
 // CTAs whose unit ranges touch split tile ts: [first, last] (some in between
@@ -101,7 +133,7 @@ PROJ_HD bool cta_has_units(int32_t c, int64_t U, int32_t G) {
 // of c's unit range, 2c + 1 for the last (a range spans at most one partial
 // tile at each end; tiles it covers whole are never split).
 PROJ_HD int32_t split_slot(int32_t c, int32_t ts, int64_t U, int32_t G, int32_t k_blocks) {
-    return 2 * c + (ts == static_cast<int32_t>(unit_begin(c, U, G) / k_blocks) ? 0 : 1);
+    return 2 * c + (ts == static_cast<int32_t>(div_nonneg(unit_begin(c, U, G), k_blocks)) ? 0 : 1);
 }
 
 struct WorkIter {
@@ -115,7 +147,7 @@ struct WorkIter {
         dp_next = c;
         u = unit_begin(c, p.units_sk, p.grid);
         u_end = unit_begin(c + 1, p.units_sk, p.grid);
-        first_sk_tile = static_cast<int32_t>(u / p.k_blocks);
+        first_sk_tile = static_cast<int32_t>(div_nonneg(u, p.k_blocks));
     }
 
     // Whole tiles first (c, c+G, ... below tiles_dp), then this CTA's split-K
@@ -131,7 +163,7 @@ struct WorkIter {
             return true;
         }
         if (u < u_end) {
-            const int32_t ts = static_cast<int32_t>(u / p.k_blocks);
+            const int32_t ts = static_cast<int32_t>(div_nonneg(u, p.k_blocks));
             const int32_t kb0 = static_cast<int32_t>(u - static_cast<int64_t>(ts) * p.k_blocks);
             const int64_t left = u_end - u;
             const int32_t kb1 = left < static_cast<int64_t>(p.k_blocks - kb0)
@@ -157,6 +189,8 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.tiles_dp = static_cast<int32_t>(plan.tiles_dp);
     kp.grid = plan.grid;
     kp.units_sk = plan.units_sk;
+    kp.sk_pair = plan.grid > 0 && plan.units_sk / plan.grid >= plan.k_blocks;
+    kp.sk_dense = plan.units_sk >= plan.grid;
     kp.stages = plan.stages;
     kp.stage_bytes = stage_bytes_for(plan.block_t);
     kp.tmem_cols = plan.tmem_cols;

@@ -205,6 +205,50 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start its
+// set-up now / wait until the preceding kernel has completed and its memory
+// is visible.  Both are no-ops for a launch without the PDL attribute.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t sm_id() {
+    uint32_t id;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(id));
+    return id;
+}
+
+// Phase trace (off unless the handle has a trace buffer): one globaltimer
+// stamp per phase per CTA, see proj_set_trace in proj.h for the layout.
+__device__ __forceinline__ void trace_stamp(const KernelParams &p, int slot) {
+    if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + slot] = globaltimer_ns();
+}
+
+__device__ __forceinline__ void store_y(const KernelParams &p, size_t off, float y) {
+    if (p.y_f32)
+        static_cast<float *>(p.Y)[off] = y;
+    else
+        static_cast<__nv_bfloat16 *>(p.Y)[off] = __float2bfloat16_rn(y);
+}
+
+// Release/acquire fence at GPU scope (one lane publishes or observes the
+// partial sums its whole warp wrote, ordered by __syncwarp around it).
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// The 16 columns [ch·16, ch·16+16) of one partial-sum row: four 16-byte loads
+// through L2 (partials are written by other SMs).
+__device__ __forceinline__ void load_partial16(const float *row, int32_t ch, float4 (&o)[4]) {
+    const float4 *src = reinterpret_cast<const float4 *>(row + ch * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = __ldcg(src + i);
+}
+
 // ----------------------------------------------------------------------------
 // Shared-memory layout
 // ----------------------------------------------------------------------------
@@ -238,6 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t a_bytes = kBlockN * kBlockK * 2;
 
     if (threadIdx.x == 0) {
+        trace_stamp(p, kTraceEntry);
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
@@ -263,8 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = ctl->tmem_base;
     const uint32_t half_cols = static_cast<uint32_t>(p.tmem_cols / 2);
+    if (threadIdx.x == 0) {
+        // Only on-chip state has been touched so far; the next kernel may begin
+        // its own set-up.  Global memory is touched only after griddep_wait().
+        griddep_launch_dependents();
+        if (p.trace) {
+            trace_stamp(p, kTraceSetup);
+            p.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + kTraceSmid] = sm_id();
+        }
+    }
 
-    int64_t issued = 0;  // producer: stage loads issued (for the abort drain)
+    int64_t issued = 0;   // producer: stage loads issued (for the abort drain)
+    int32_t reductions = 0;  // epilogue warp 2: split tiles this warp finished
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -272,6 +327,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = l2_policy_evict_first();  // W is read once
             const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
             const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
+            auto load_w = [&](uint32_t a_dst, uint32_t full, int32_t tn, int32_t kb) {
+                if (!p.w_kn) {
+                    tma_load_2d(a_dst, &tmap_w, full, kb * kBlockK, tn * kBlockN, pol_w);
+                } else {
+                    tma_load_2d(a_dst, &tmap_w, full, tn * kBlockN, kb * kBlockK, pol_w);
+                    tma_load_2d(a_dst + a_bytes / 2, &tmap_w, full, tn * kBlockN + 64, kb * kBlockK,
+                                pol_w);
+                }
+            };
+            // Optional weight prefetch: fill the ring with W before the
+            // preceding kernel has finished (W must not be written by it).
+            int64_t pre = 0;
+            if (p.w_prefetch) {
+                WorkIter it;
+                it.init(p, blockIdx.x);
+                Segment s;
+                while (pre < stages && it.next(p, s)) {
+                    const int32_t tn = s.tile / p.tiles_m;
+                    for (int32_t kb = s.kb0; kb < s.kb1 && pre < stages; ++kb) {
+                        const uint32_t full = smem_u32(&ctl->full[pre]);
+                        mbar_arrive_expect_tx(full, stage_bytes);  // W + X bytes of the stage
+                        load_w(base_addr + static_cast<uint32_t>(pre) * stage_bytes, full, tn, kb);
+                        ++pre;
+                    }
+                }
+                if (pre > 0) trace_stamp(p, kTraceFirstLoad);
+            }
+            griddep_wait();  // X (and everything else) may come from the preceding kernel
             int32_t stage = 0;
             uint32_t phase = 0;
             WorkIter it;
@@ -282,23 +365,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int32_t tm = s.tile % p.tiles_m;
                 const int32_t tn = s.tile / p.tiles_m;
                 for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
-                    if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.status,
-                                    kErrWaitProducer, p.wait_limit_ns)) {
-                        ok = false;
-                        break;
-                    }
                     const uint32_t full = smem_u32(&ctl->full[stage]);
                     const uint32_t a_dst = base_addr + stage * stage_bytes;
                     const uint32_t b_dst = a_dst + a_bytes;
-                    mbar_arrive_expect_tx(full, stage_bytes);
-                    if (!p.w_kn) {
-                        tma_load_2d(a_dst, &tmap_w, full, kb * kBlockK, tn * kBlockN, pol_w);
-                    } else {
-                        tma_load_2d(a_dst, &tmap_w, full, tn * kBlockN, kb * kBlockK, pol_w);
-                        tma_load_2d(a_dst + a_bytes / 2, &tmap_w, full, tn * kBlockN + 64,
-                                    kb * kBlockK, pol_w);
+                    if (issued >= pre) {
+                        if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.status,
+                                        kErrWaitProducer, p.wait_limit_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(full, stage_bytes);
+                        load_w(a_dst, full, tn, kb);
                     }
                     tma_load_2d(b_dst, &tmap_x, full, kb * kBlockK, tm * p.block_t, pol_x);
+                    if (issued == 0 && pre == 0) trace_stamp(p, kTraceFirstLoad);
                     ++issued;
                     if (++stage == stages) {
                         stage = 0;
@@ -306,6 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (issued < pre) issued = pre;  // stages armed by the prefetch (abort drain)
+            trace_stamp(p, kTraceLastLoad);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -332,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after_sync();
+                    if (seg_idx == 0 && kb == s.kb0) trace_stamp(p, kTraceFirstData);
                     const uint32_t a_addr = base_addr + stage * static_cast<uint32_t>(p.stage_bytes);
                     const uint32_t b_addr = a_addr + a_bytes;
 #pragma unroll
@@ -355,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit(smem_u32(&ctl->acc_full[buf]));  // accumulator ready
                 ++seg_idx;
             }
+            trace_stamp(p, kTraceLastMma);
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -362,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;         // row within the 128-row weight tile
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const int64_t U = p.units_sk;
+        griddep_wait();  // partials, counters and Y may be in use by the preceding kernel
         int32_t seg_idx = 0;
         WorkIter it;
         it.init(p, blockIdx.x);
@@ -373,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             kErrWaitEpilogue, p.wait_limit_ns))
                 break;
             tc_fence_after_sync();
+            if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
             const int32_t tm = s.tile % p.tiles_m;
             const int32_t tn = s.tile / p.tiles_m;
             const int32_t n = tn * kBlockN + r;
@@ -380,96 +466,163 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t mcount = min(p.block_t, p.M - m0);
             const int32_t nchunks = (mcount + 15) / 16;
             const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(buf) * half_cols;
+
             const bool n_ok = n < p.N;
             const float bias_v = (p.bias != nullptr && n_ok) ? bf16_bits_to_float(p.bias[n]) : 0.f;
+            // Store one chunk of 16 output columns of this lane's row n.
+            auto store_chunk = [&](int32_t ch, const float (&y)[16]) {
+                if (!n_ok) return;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int32_t m = m0 + ch * 16 + i;
+                    if (m < p.M) store_y(p, static_cast<size_t>(m) * p.N + n, y[i] + bias_v);
+                }
+            };
+            auto release_accumulator = [&]() {
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+            };
 
             if (!s.split) {
+                // Whole tile: tensor memory -> (+ bias) -> Y.  Lane = weight row n.
                 for (int32_t ch = 0; ch < nchunks; ++ch) {
                     float v[16];
                     tmem_load16(tbase + ch * 16, v);
-                    if (n_ok) {
+                    store_chunk(ch, v);
+                }
+                release_accumulator();
+            } else {
+                // Split tile.  This lane's row of fp32 partial sums goes to
+                // scratch, laid out [slot][128 rows][block_t] (16 columns =
+                // 64 contiguous bytes per lane per chunk).
+                float *own = p.partials + (static_cast<size_t>(s.slot) * kBlockN + r) * p.block_t;
+                for (int32_t ch = 0; ch < nchunks; ++ch) {
+                    float v[16];
+                    tmem_load16(tbase + ch * 16, v);
+                    float4 *dst = reinterpret_cast<float4 *>(own + ch * 16);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const int32_t m = m0 + ch * 16 + i;
-                            if (m < p.M) {
-                                const float y = v[i] + bias_v;
-                                const size_t off = static_cast<size_t>(m) * p.N + n;
-                                if (p.y_f32)
-                                    static_cast<float *>(p.Y)[off] = y;
-                                else
-                                    static_cast<__nv_bfloat16 *>(p.Y)[off] = __float2bfloat16_rn(y);
-                            }
-                        }
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                }
+                // Contributors of this tile, in K order.
+                const int32_t ts = s.tile - p.tiles_dp;
+                int32_t c_first = 0, c_last = 0, nseg = 2, first_slot = 0;
+                if (!p.sk_pair) {
+                    split_tile_ctas(ts, p.k_blocks, U, p.grid, c_first, c_last);
+                    if (p.sk_dense) {
+                        // Every CTA owns units: c_first may have started in an
+                        // earlier tile; every later contributor starts inside
+                        // this one (slot 2c).
+                        nseg = c_last - c_first + 1;
+                        first_slot = 2 * c_first +
+                                     (unit_begin(c_first, U, p.grid) < static_cast<int64_t>(ts) * p.k_blocks ? 1 : 0);
+                    } else {
+                        nseg = 0;
+                        for (int32_t c = c_first; c <= c_last; ++c) nseg += cta_has_units(c, U, p.grid) ? 1 : 0;
                     }
                 }
-            } else {
-                float *part = p.partials + static_cast<size_t>(s.slot) * p.block_t * kBlockN;
-                for (int32_t ch = 0; ch < nchunks; ++ch) {
-                    float v[16];
-                    tmem_load16(tbase + ch * 16, v);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) part[(ch * 16 + i) * kBlockN + r] = v[i];
-                }
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
-
-            if (s.split) {
-                // Publish this warp's 32 rows of partials, then count arrivals.
-                const int32_t ts = s.tile - p.tiles_dp;
-                int32_t c_first, c_last;
-                split_tile_ctas(ts, p.k_blocks, U, p.grid, c_first, c_last);
-                int32_t nseg = 0;
-                for (int32_t c = c_first; c <= c_last; ++c) nseg += cta_has_units(c, U, p.grid) ? 1 : 0;
-                __threadfence();
+                // Publish (release) and count arrivals per 32-row quarter.
                 __syncwarp();
                 int last = 0;
                 uint32_t *ctr = p.counters + static_cast<size_t>(ts) * 4 + q;
                 if (lane == 0) {
+                    fence_acq_rel_gpu();
                     const uint32_t old = atomicAdd(ctr, 1u);
                     last = (old == static_cast<uint32_t>(nseg - 1)) ? 1 : 0;
-                    if (last) atomicExch(ctr, 0u);  // fresh for the next run
-                    __threadfence();
+                    if (last) {
+                        atomicExch(ctr, 0u);  // fresh for the next run
+                        fence_acq_rel_gpu();  // acquire the other contributors' partials
+                    }
                 }
                 last = __shfl_sync(0xFFFFFFFFu, last, 0);
-                if (last) {
-                    for (int32_t ch = 0; ch < nchunks; ++ch) {
-                        float acc[16];
+                __syncwarp();
+                if (last && warp == 2 && lane == 0) ++reductions;
+
+                if (last && p.sk_pair) {
+                    // Two contributors: own accumulator (still in tensor
+                    // memory) + the other's partial.  Two-operand addition is
+                    // commutative, so the bits do not depend on who is last.
+                    const int32_t other_slot =
+                        s.kb0 == 0 ? 2 * (static_cast<int32_t>(blockIdx.x) + 1)
+                                   : 2 * (static_cast<int32_t>(blockIdx.x) - 1) + 1;
+                    const float *other = p.partials + (static_cast<size_t>(other_slot) * kBlockN + r) * p.block_t;
+                    for (int32_t ch0 = 0; ch0 < nchunks; ch0 += 4) {
+                        float4 o[4][4];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-                        for (int32_t c = c_first; c <= c_last; ++c) {
-                            if (!cta_has_units(c, U, p.grid)) continue;
-                            const int32_t slot = split_slot(c, ts, U, p.grid, p.k_blocks);
-                            const float *pc =
-                                p.partials + static_cast<size_t>(slot) * p.block_t * kBlockN;
+                        for (int u = 0; u < 4; ++u)
+                            if (ch0 + u < nchunks) load_partial16(other, ch0 + u, o[u]);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) acc[i] += __ldcg(pc + (ch * 16 + i) * kBlockN + r);
-                        }
-                        if (n_ok) {
+                        for (int u = 0; u < 4; ++u) {
+                            if (ch0 + u >= nchunks) break;
+                            float v[16];
+                            tmem_load16(tbase + (ch0 + u) * 16, v);
 #pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int32_t m = m0 + ch * 16 + i;
-                                if (m < p.M) {
-                                    const float y = acc[i] + bias_v;
-                                    const size_t off = static_cast<size_t>(m) * p.N + n;
-                                    if (p.y_f32)
-                                        static_cast<float *>(p.Y)[off] = y;
-                                    else
-                                        static_cast<__nv_bfloat16 *>(p.Y)[off] = __float2bfloat16_rn(y);
-                                }
+                            for (int i = 0; i < 4; ++i) {
+                                v[4 * i] += o[u][i].x;
+                                v[4 * i + 1] += o[u][i].y;
+                                v[4 * i + 2] += o[u][i].z;
+                                v[4 * i + 3] += o[u][i].w;
                             }
+                            store_chunk(ch0 + u, v);
+                        }
+                    }
+                    release_accumulator();
+                } else {
+                    release_accumulator();
+                    if (last) {
+                        // Several contributors: add every partial (own
+                        // included) in ascending CTA order, i.e. ascending K,
+                        // four contributors' loads in flight at a time.
+                        for (int32_t ch = 0; ch < nchunks; ++ch) {
+                            float acc[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                            for (int32_t c = c_first; c <= c_last; c += 4) {
+                                float4 o[4][4];
+                                bool valid[4];
+#pragma unroll
+                                for (int k = 0; k < 4; ++k) {
+                                    const int32_t cc = c + k;
+                                    valid[k] = cc <= c_last && (p.sk_dense || cta_has_units(cc, U, p.grid));
+                                    if (valid[k]) {
+                                        const int32_t slot =
+                                            p.sk_dense ? (cc == c_first ? first_slot : 2 * cc)
+                                                       : split_slot(cc, ts, U, p.grid, p.k_blocks);
+                                        load_partial16(p.partials + (static_cast<size_t>(slot) * kBlockN + r) * p.block_t,
+                                                       ch, o[k]);
+                                    }
+                                }
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    if (valid[k]) {
+#pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            acc[4 * i] += o[k][i].x;
+                                            acc[4 * i + 1] += o[k][i].y;
+                                            acc[4 * i + 2] += o[k][i].z;
+                                            acc[4 * i + 3] += o[k][i].w;
+                                        }
+                                    }
+                            }
+                            store_chunk(ch, acc);
                         }
                     }
                 }
             }
             ++seg_idx;
         }
+        if (warp == 2 && lane == 0) trace_stamp(p, kTraceEpilogueDone);
     }
 
     // ---------------------------------------------------------------- teardown
     tc_fence_before_sync();
     __syncthreads();
+    if (p.trace && warp == 2 && lane == 0) {
+        trace_stamp(p, kTraceTeardown);
+        p.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + kTraceReductions] =
+            static_cast<unsigned long long>(reductions);
+    }
     if (*abort_flag) {
         // Let every copy and MMA already in flight land before the CTA leaves.
         if (warp == 0 && lane == 0) {

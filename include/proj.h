@@ -100,10 +100,12 @@ typedef struct proj_device_desc {
  * output features: the swapped product Yᵀ = W·Xᵀ, section "Prove the swapped
  * product before worrying about its speed") × block_t token rows (the MMA's
  * N side) × the whole K range, cut into k_blocks blocks of block_k.
- * Whole tiles are dealt out in data-parallel waves (tiles_dp, a multiple of
- * grid); the remaining tiles_sk tiles are split along K into units_sk
- * k-block units shared contiguously by all CTAs ("split-K", section "My first
- * useful win: split up the sum"; CTA c takes units
+ * Whole tiles are dealt out in data-parallel waves (tiles_dp); the remaining
+ * tiles_sk tiles (the last partial wave plus one full wave, or every tile when
+ * there are fewer tiles than CTAs; none when the last wave is nearly full) are
+ * split along K
+ * into units_sk k-block units shared contiguously by all CTAs ("split-K",
+ * section "My first useful win: split up the sum"; CTA c takes units
  * [⌊c·U/G⌋, ⌊(c+1)·U/G⌋), the integer partition of section "Why the later
  * TMA/WGMMA kernel was a new experiment" that splits 128 tiles 42/43/43).
  */
@@ -121,7 +123,8 @@ typedef struct proj_plan_desc {
     int64_t tiles_m;         /* ceil(M / block_t) */
     int64_t tiles_n;         /* ceil(N / block_n) */
     int64_t k_blocks;        /* ceil(K / block_k) */
-    int64_t tiles_dp;        /* tiles computed whole, tiles_dp % grid == 0 */
+    int64_t tiles_dp;        /* tiles computed whole, dealt round-robin (CTA c: c, c+grid, ...);
+                                a multiple of grid whenever tiles_sk > 0 */
     int64_t tiles_sk;        /* tiles split along K across CTAs */
     int64_t units_sk;        /* tiles_sk * k_blocks */
     int64_t scratch_bytes;   /* device scratch the handle owns */
@@ -213,6 +216,46 @@ proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W,
  * reused), PROJ_ERR_CUDA if the synchronisation failed, else PROJ_OK.
  */
 proj_status_t proj_device_status(proj_handle_t h, void *stream);
+
+/*
+ * How a run may overlap the kernel launched before it on the same stream
+ * (programmatic dependent launch; the worklog's section "The later version
+ * really did reach 1.32×" describes the idea: start the independent part
+ * early, wait where it matters).
+ *   PROJ_OVERLAP_NONE      plain stream order.
+ *   PROJ_OVERLAP_PROLOGUE  (default) the kernel may start while the preceding
+ *                          kernel finishes, but touches no global memory (no
+ *                          X, W, bias, Y or scratch) until that kernel has
+ *                          completed: always safe.
+ *   PROJ_OVERLAP_WEIGHTS   as above, and the first pipeline stages of W are
+ *                          streamed before the preceding kernel completes.
+ *                          The caller promises that W is not written by the
+ *                          kernel launched just before the run (true for
+ *                          inference weights).
+ * PROJ_ERR_INVALID_ARG for a NULL handle or an unknown mode.
+ */
+typedef enum proj_overlap {
+    PROJ_OVERLAP_NONE = 0,
+    PROJ_OVERLAP_PROLOGUE = 1,
+    PROJ_OVERLAP_WEIGHTS = 2
+} proj_overlap_t;
+
+proj_status_t proj_set_overlap(proj_handle_t h, proj_overlap_t mode);
+
+/*
+ * Phase trace (diagnostics).  With a device buffer of at least
+ * grid × 16 × 8 bytes (grid from the plan) every later proj_run writes, per
+ * CTA, 16 unsigned 64-bit words: [0] kernel entry, [1] set-up done,
+ * [2] first TMA load issued, [3] last TMA load issued, [4] first stage seen
+ * by the MMA issuer, [5] last accumulator committed, [6] first accumulator
+ * received by the epilogue, [7] epilogue finished, [8] final barrier
+ * (globaltimer nanoseconds), [9] the SM id, [10] split tiles reduced by the
+ * CTA's first epilogue warp; [11..15] unused.  The caller owns the buffer; a
+ * NULL buffer turns tracing off.  PROJ_ERR_INVALID_ARG if the buffer is too
+ * small, PROJ_ERR_MISALIGNED if not 8-byte aligned, PROJ_ERR_UNSUPPORTED for
+ * plans without the tensor-core kernel.
+ */
+proj_status_t proj_set_trace(proj_handle_t h, void *device_buffer, size_t bytes);
 
 /* Copy the handle's plan. */
 proj_status_t proj_get_plan(proj_handle_t h, proj_plan_desc_t *out);

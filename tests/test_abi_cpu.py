@@ -1,0 +1,191 @@
+"""The C-ABI library on a machine without a GPU: it loads, exports what
+include/proj.h declares, and its planner (pure host code, the same
+decomposition code the kernel runs) cuts every problem correctly."""
+import collections
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+import dense_linear_projection_gb300 as dlp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "proj.h")
+GB300 = dict(sm_count=152, smem_optin_bytes=232448)
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(proj_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert "proj_create" in names and "proj_run" in names and "proj_destroy" in names
+    lib = dlp.lib()
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in proj.h but not exported"
+    assert set(names) == set(dlp.EXPORTED_SYMBOLS)
+
+
+def test_status_strings():
+    for code, name in [(0, "PROJ_OK"), (1, "PROJ_ERR_INVALID_ARG"), (2, "PROJ_ERR_UNSUPPORTED"),
+                       (3, "PROJ_ERR_MISALIGNED"), (4, "PROJ_ERR_OUT_OF_MEMORY"),
+                       (5, "PROJ_ERR_CUDA"), (6, "PROJ_ERR_DEVICE_TIMEOUT")]:
+        assert dlp.proj_status_string(code) == name
+    assert dlp.proj_status_string(99) == "PROJ_ERR_UNKNOWN"
+
+
+def test_create_without_a_gpu_fails_cleanly():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(dlp.ProjError) as e:
+        dlp.proj_create(16, 256, 256)
+    assert e.value.status in (dlp.PROJ_ERR_CUDA, dlp.PROJ_ERR_UNSUPPORTED)
+
+
+def test_null_handle_calls_are_rejected():
+    assert dlp.lib().proj_run(None, None, None, None, None, None) == dlp.PROJ_ERR_INVALID_ARG
+    assert dlp.lib().proj_destroy(None) == dlp.PROJ_OK
+    assert dlp.proj_device_status(None) == dlp.PROJ_ERR_INVALID_ARG
+    assert dlp.lib().proj_set_trace(None, None, 0) == dlp.PROJ_ERR_INVALID_ARG
+
+
+# ---------------------------------------------------------------- planner
+def plan(M, N, K, layout=0, **dev):
+    return dlp.proj_plan_compute(M, N, K, layout, **(dev or GB300))
+
+
+def check_decomposition(p, M, N, K):
+    G, KT = p["grid"], p["k_blocks"]
+    tiles = p["tiles_m"] * p["tiles_n"]
+    assert p["tiles_m"] == -(-M // p["block_t"]) and p["tiles_n"] == -(-N // 128)
+    assert KT == -(-K // 64)
+    assert 1 <= G <= GB300["sm_count"]
+    assert p["tiles_dp"] + p["tiles_sk"] == tiles
+    if p["tiles_sk"]:
+        assert p["tiles_dp"] % G == 0
+    else:  # whole tiles only: the last wave is at least 95 % full (or exactly full)
+        waves = -(-tiles // G)
+        assert tiles % G == 0 or 20 * tiles >= 19 * waves * G
+    assert p["units_sk"] == p["tiles_sk"] * KT
+    assert p["smem_bytes"] <= GB300["smem_optin_bytes"] and p["stages"] >= 2
+    assert p["block_t"] % 16 == 0 and 16 <= p["block_t"] <= 256
+    cover = np.zeros((tiles, KT), dtype=np.int32)
+    by_tile = collections.defaultdict(list)
+    slots = set()
+    for c in range(G):
+        for (tile, tm, tn, kb0, kb1, slot, split) in dlp.proj_plan_segments(p, c):
+            assert tile == tn * p["tiles_m"] + tm and 0 <= kb0 < kb1 <= KT
+            cover[tile, kb0:kb1] += 1
+            by_tile[tile].append((c, slot, split, kb0, kb1))
+            if split:
+                assert 0 <= slot < 2 * G and slot not in slots
+                slots.add(slot)
+            else:
+                assert (kb0, kb1) == (0, KT) and slot == -1
+    assert (cover == 1).all(), "every (tile, k-block) exactly once"
+    share = p["units_sk"] // G if p["units_sk"] else 0
+    for tile, segs in by_tile.items():
+        split = len(segs) > 1
+        assert all(bool(s[2]) == split for s in segs)
+        if split:
+            ts = tile - p["tiles_dp"]
+            assert ts >= 0
+            segs.sort(key=lambda s: s[3])  # K order
+            order = dlp.proj_plan_reduction_order(p, ts)
+            assert order == [(s[0], s[1]) for s in segs]
+            assert [s[0] for s in segs] == sorted(s[0] for s in segs)
+            if share >= KT:  # the two-contributor case the kernel's pair path assumes
+                (c0, s0, _, a0, b0), (c1, s1, _, a1, b1) = segs
+                assert c1 == c0 + 1 and a0 == 0 and b1 == KT and b0 == a1
+                assert s0 == 2 * c0 + 1 and s1 == 2 * c1
+
+
+CONFIG_SHAPES = [(16, 2048, 8192, 0), (16, 8192, 8192, 0), (16, 28672, 8192, 0),
+                 (256, 12288, 4096, 1), (4096, 8192, 8192, 0)] + [
+    (m, 28672, 8192, 0) for m in (1, 2, 4, 8, 32, 64)]
+
+
+@pytest.mark.parametrize("M,N,K,layout", CONFIG_SHAPES)
+def test_plans_of_the_workloads(M, N, K, layout):
+    p = plan(M, N, K, layout)
+    assert p["kernel"] == dlp.PROJ_KERNEL_TC
+    check_decomposition(p, M, N, K)
+
+
+def test_plans_of_many_shapes():
+    rng = np.random.default_rng(0)
+    shapes = [(1, 1, 8), (1, 128, 64), (17, 300, 72), (3, 130, 72), (257, 300, 256),
+              (512, 20480, 256), (600, 1000, 1032), (9, 7, 16)]
+    shapes += [(int(rng.integers(1, 700)), int(rng.integers(1, 6000)), 8 * int(rng.integers(1, 700)))
+               for _ in range(40)]
+    for (M, N, K) in shapes:
+        for sm in (152, 148, 7, 1):
+            p = plan(M, N, K, sm_count=sm, smem_optin_bytes=232448)
+            GB300_sm = sm
+            assert p["grid"] <= GB300_sm
+            check_decomposition(p, M, N, K)
+
+
+def test_page_partition_42_43_43():
+    # 128 K tiles shared by 3 CTAs with integer boundaries: 42, 43, 43
+    # ("Why the later TMA/WGMMA kernel was a new experiment").
+    p = {"kernel": dlp.PROJ_KERNEL_TC, "grid": 3, "k_blocks": 128, "tiles_m": 1, "tiles_n": 1,
+         "tiles_dp": 0, "tiles_sk": 1, "units_sk": 128, "block_t": 16}
+    lens = [sum(kb1 - kb0 for (_, _, _, kb0, kb1, _, _) in dlp.proj_plan_segments(p, c))
+            for c in range(3)]
+    assert lens == [42, 43, 43]
+    assert [c for c, _ in dlp.proj_plan_reduction_order(p, 0)] == [0, 1, 2]
+
+
+def test_split_k_example_every_k_covered_once():
+    # Section "How splitting changes the grid" / the split-router K loop: all
+    # K positions of a 8192-long sum are covered, none twice, for any split.
+    for G in (2, 3, 16, 32, 152):
+        p = {"kernel": dlp.PROJ_KERNEL_TC, "grid": G, "k_blocks": 128, "tiles_m": 1,
+             "tiles_n": 1, "tiles_dp": 0, "tiles_sk": 1, "units_sk": 128, "block_t": 16}
+        covered = []
+        for c in range(G):
+            for seg in dlp.proj_plan_segments(p, c):
+                covered.extend(range(seg[3], seg[4]))
+        assert sorted(covered) == list(range(128))
+
+
+def test_degenerate_plans_and_errors():
+    assert plan(0, 64, 64)["kernel"] == dlp.PROJ_KERNEL_NONE
+    assert plan(4, 0, 64)["kernel"] == dlp.PROJ_KERNEL_NONE
+    assert plan(4, 64, 0)["kernel"] == dlp.PROJ_KERNEL_FILL
+    for bad in [(-1, 4, 8), (4, -1, 8), (4, 4, -8)]:
+        with pytest.raises(dlp.ProjError) as e:
+            plan(*bad)
+        assert e.value.status == dlp.PROJ_ERR_INVALID_ARG
+    with pytest.raises(dlp.ProjError):
+        dlp.proj_plan_compute(4, 4, 8, 7)
+    with pytest.raises(dlp.ProjError) as e:
+        dlp.proj_plan_compute(4, 4, 8, 0, sm_count=152, smem_optin_bytes=20000)
+    assert e.value.status == dlp.PROJ_ERR_UNSUPPORTED
+    with pytest.raises(dlp.ProjError):
+        dlp.proj_plan_segments({"kernel": 2, "grid": 4, "k_blocks": 2, "tiles_m": 1}, 4)
+
+
+def test_token_tile_choice():
+    assert plan(1, 8192, 8192)["block_t"] == 16
+    assert plan(16, 8192, 8192)["block_t"] == 16
+    assert plan(17, 8192, 8192)["block_t"] == 32
+    assert plan(64, 28672, 8192)["block_t"] == 64
+    assert plan(4096, 8192, 8192)["block_t"] == 256
+    # 256 tokens x 96 weight tiles would leave SMs idle: two 128-token tiles instead.
+    assert plan(256, 12288, 4096, 1)["block_t"] == 128
+
+
+def test_scratch_and_stages():
+    p = plan(16, 8192, 8192)
+    stage = 128 * 64 * 2 + p["block_t"] * 64 * 2
+    assert p["smem_bytes"] == p["stages"] * stage + 2048
+    assert p["scratch_bytes"] >= 2 * p["grid"] * p["block_t"] * 128 * 4 + 4 * 4 * p["tiles_sk"]
+    assert p["tmem_cols"] >= 2 * p["block_t"] and p["tmem_cols"] in (32, 64, 128, 256, 512)

@@ -27,7 +27,23 @@ SHAPES = [
     (257, 300, 256, synth.W_NK, False, "bf16"),   # two token tiles, 1-row tail
     (512, 20480, 256, synth.W_NK, True, "bf16"),  # 320 tiles: two data-parallel waves + split-K
     (600, 1000, 1032, synth.W_KN, False, "f32"),  # [K,N] with several token tiles
+    (200, 1024, 512, synth.W_NK, True, "bf16"),   # token tile halved to 64: many-way split
+    (130, 3000, 2048, synth.W_KN, True, "f32"),   # [K,N], two-contributor split tiles
+    (16, 28672, 1024, synth.W_NK, False, "bf16"), # 224 tiles, all split in pairs
 ]
+
+
+@pytest.mark.parametrize("block_t", [16, 64, 128, 256])
+def test_forced_token_tiles(block_t, monkeypatch):
+    # The same problem under every token tile: data-parallel, pair and
+    # many-way split paths all agree with the oracle.
+    monkeypatch.setenv("PROJ_FORCE_BLOCK_T", str(block_t))
+    w = _workload(256, 1536, 2048, synth.W_KN, True, "bf16", seed=21)
+    inp = synth.make_inputs(w)
+    proj, Y, _ = gu.run(w, inp)
+    assert proj.plan["block_t"] == block_t
+    r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
+    gu.assert_within_tol(gu.y_to_f64(Y), r, f"block_t={block_t}")
 
 
 def _workload(M, N, K, layout, bias, yd, seed=5):
@@ -273,3 +289,40 @@ def test_bounded_wait_gives_up_without_fault():
     torch.cuda.synchronize()
     assert proj.status() == dlp.PROJ_OK
     gu.assert_within_tol(gu.y_to_f64(Y), oracle.project(inp["X"], inp["W"], 0, inp["bias"]))
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2], ids=["none", "prologue", "weights"])
+def test_overlap_modes_see_inputs_written_just_before(mode):
+    # Programmatic dependent launch: X written by the kernel right before each
+    # run (inside one captured graph) must be the X the run uses, and
+    # back-to-back split-K runs must not disturb each other's scratch.
+    import torch
+    import dense_linear_projection_gb300 as dlp
+    w = synth.Workload("t", 16, 1000, 2048, synth.W_NK, True, "bf16", 31)
+    inp = synth.make_inputs(w)
+    X2 = synth.normal_bf16(32, synth.STREAM_X, w.M * w.K, 1.0).reshape(w.M, w.K)
+    proj = dlp.Projection(w.M, w.N, w.K, w.w_layout, dlp.PROJ_BF16, True, overlap=mode)
+    assert proj.plan["tiles_sk"] > 0
+    Xs = [gu.to_dev(inp["X"]), gu.to_dev(X2)]
+    W, b = gu.to_dev(inp["W"]), gu.to_dev(inp["bias"])
+    X = torch.empty_like(Xs[0])
+    Ys = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device="cuda") for _ in range(6)]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        X.copy_(Xs[0])
+        proj(X, W, b, out=Ys[0], stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(6):
+            X.mul_(0).add_(Xs[i % 2])  # kernels that write X just before the run
+            proj(X, W, b, out=Ys[i], stream=s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert proj.status() == dlp.PROJ_OK
+    refs = [oracle.project(inp["X"], inp["W"], 0, inp["bias"]),
+            oracle.project(X2, inp["W"], 0, inp["bias"])]
+    for i in range(6):
+        gu.assert_within_tol(gu.y_to_f64(Ys[i]), refs[i % 2], f"mode {mode} run {i}")
+    assert torch.equal(Ys[0].view(torch.int16), Ys[2].view(torch.int16))
