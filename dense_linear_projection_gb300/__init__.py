@@ -228,7 +228,8 @@ def proj_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
 
 
 TRACE_FIELDS = ("entry", "setup", "first_load", "last_load", "first_data", "last_mma",
-                "first_acc", "epilogue_done", "teardown", "smid", "reductions")
+                "first_acc", "epilogue_done", "teardown", "smid", "reductions", "dep_wait",
+                "epi_dep_wait")
 
 
 def proj_set_overlap(h: int, mode: int) -> None:

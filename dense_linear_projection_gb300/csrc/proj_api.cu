@@ -362,3 +362,4 @@ proj_status_t proj_selftest_wait_timeout(int64_t limit_ns, void *stream) {
 }
 
 }  // extern "C"
+

@@ -38,6 +38,8 @@ constexpr int kTraceEpilogueDone = 7;  // epilogue warp 2 finished every segment
 constexpr int kTraceTeardown = 8;      // all roles joined at the final barrier
 constexpr int kTraceSmid = 9;          // SM the CTA ran on (a number, not a time)
 constexpr int kTraceReductions = 10;   // split tiles epilogue warp 2 reduced (a count)
+constexpr int kTraceDepWait = 11;      // producer returned from the grid-dependency wait
+constexpr int kTraceEpiDepWait = 12;   // epilogue warp 2 returned from the grid-dependency wait
 
 // Error bits in the device status word.
 constexpr int kErrWaitProducer = 1 << 0;

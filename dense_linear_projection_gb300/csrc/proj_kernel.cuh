@@ -355,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (pre > 0) trace_stamp(p, kTraceFirstLoad);
             }
             griddep_wait();  // X (and everything else) may come from the preceding kernel
+            trace_stamp(p, kTraceDepWait);
             int32_t stage = 0;
             uint32_t phase = 0;
             WorkIter it;
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const int64_t U = p.units_sk;
         griddep_wait();  // partials, counters and Y may be in use by the preceding kernel
+        if (warp == 2 && lane == 0) trace_stamp(p, kTraceEpiDepWait);
         int32_t seg_idx = 0;
         WorkIter it;
         it.init(p, blockIdx.x);

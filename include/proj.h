@@ -250,7 +250,8 @@ proj_status_t proj_set_overlap(proj_handle_t h, proj_overlap_t mode);
  * by the MMA issuer, [5] last accumulator committed, [6] first accumulator
  * received by the epilogue, [7] epilogue finished, [8] final barrier
  * (globaltimer nanoseconds), [9] the SM id, [10] split tiles reduced by the
- * CTA's first epilogue warp; [11..15] unused.  The caller owns the buffer; a
+ * CTA's first epilogue warp, [11] producer past the grid-dependency wait,
+ * [12] epilogue past it; [13..15] unused.  The caller owns the buffer; a
  * NULL buffer turns tracing off.  PROJ_ERR_INVALID_ARG if the buffer is too
  * small, PROJ_ERR_MISALIGNED if not 8-byte aligned, PROJ_ERR_UNSUPPORTED for
  * plans without the tensor-core kernel.
