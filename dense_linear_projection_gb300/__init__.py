@@ -27,7 +27,8 @@ __all__ = [
     "proj_run", "proj_run_host", "proj_device_status",
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "TRACE_FIELDS",
-    "PROJ_OVERLAP_NONE", "PROJ_OVERLAP_PROLOGUE", "PROJ_OVERLAP_WEIGHTS", "Projection",
+    "PROJ_OVERLAP_NONE", "PROJ_OVERLAP_PROLOGUE", "PROJ_OVERLAP_WEIGHTS", "proj_run_noalloc",
+    "Projection",
 ]
 
 PROJ_OK, PROJ_ERR_INVALID_ARG, PROJ_ERR_UNSUPPORTED, PROJ_ERR_MISALIGNED = 0, 1, 2, 3
@@ -40,7 +41,7 @@ PROJ_OVERLAP_NONE, PROJ_OVERLAP_PROLOGUE, PROJ_OVERLAP_WEIGHTS = 0, 1, 2
 EXPORTED_SYMBOLS = (
     "proj_plan_compute", "proj_plan_segments", "proj_plan_reduction_order", "proj_create", "proj_run", "proj_run_host", "proj_device_status",
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
-    "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap",
+    "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "proj_run_noalloc",
 )
 
 
@@ -112,6 +113,7 @@ def lib() -> ctypes.CDLL:
     L.proj_selftest_wait_timeout.argtypes = [i64, vp]
     L.proj_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
     L.proj_set_overlap.argtypes = [vp, i32]
+    L.proj_run_noalloc.argtypes = [i64, i64, i64, i32, i32, vp, vp, vp, vp, vp]
     for name in EXPORTED_SYMBOLS:
         if name != "proj_status_string":
             getattr(L, name).restype = st
@@ -199,6 +201,17 @@ def proj_run(h: int, X, W, bias, Y, stream=None) -> None:
 def proj_run_host(h: int, X_host, W, bias, Y_host, stream=None) -> None:
     _check(lib().proj_run_host(h, _ptr(X_host), _ptr(W), _ptr(bias), _ptr(Y_host),
                                _stream(stream)), "proj_run_host")
+
+
+def proj_run_noalloc(M: int, N: int, K: int, w_layout: int, y_dtype: int, X, W, bias, Y,
+                     stream=None) -> None:
+    """proj_run without a handle or any allocation (fixed 8 MiB device scratch).
+
+    For callers that cannot allocate device memory.  The first call on a device
+    looks up the scratch address; calls that overlap on the GPU race.
+    """
+    _check(lib().proj_run_noalloc(M, N, K, w_layout, y_dtype, _ptr(X), _ptr(W), _ptr(bias),
+                                  _ptr(Y), _stream(stream)), "proj_run_noalloc")
 
 
 def proj_device_status(h: int, stream=None) -> int:

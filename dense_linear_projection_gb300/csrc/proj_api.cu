@@ -8,6 +8,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "proj.h"
@@ -363,3 +364,125 @@ proj_status_t proj_selftest_wait_timeout(int64_t limit_ns, void *stream) {
 
 }  // extern "C"
 
+// ----------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc: a serving loop where an allocation may
+// synchronise the device and stall every other stream at an unpredictable
+// moment, or a plug-in whose host application owns all device memory and
+// forbids allocating behind its back.  proj_run_noalloc serves them with the
+// same kernel as proj_run, taking its split-K scratch from the fixed-size
+// device array below instead of a handle.  Every GPU that loads this library
+// holds the array until the process exits.
+// ----------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB: partials, counters, status
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kNoAllocMaxDevices];  // device address of the array, per device
+
+// Set-up, once per device with that device current: the host-side name of the
+// array is only a stand-in, so the kernel gets the real device address.
+proj_status_t noalloc_scratch_for(int device, void **out) {
+    if (device < 0 || device >= kNoAllocMaxDevices) return PROJ_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[device]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return PROJ_ERR_CUDA;
+        }
+        g_noalloc_ptr[device] = ptr;
+    }
+    *out = g_noalloc_ptr[device];
+    return PROJ_OK;
+}
+
+}  // namespace
+
+extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
+                                          proj_dtype_t y_dtype, const void *X, const void *W,
+                                          const void *bias, void *Y, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return PROJ_ERR_INVALID_ARG;
+    if (w_layout != PROJ_W_NK && w_layout != PROJ_W_KN) return PROJ_ERR_INVALID_ARG;
+    if (y_dtype != PROJ_BF16 && y_dtype != PROJ_F32) return PROJ_ERR_INVALID_ARG;
+    if (K % 8 != 0) return PROJ_ERR_MISALIGNED;
+    if (w_layout == PROJ_W_KN && N % 8 != 0) return PROJ_ERR_MISALIGNED;
+    if (M == 0 || N == 0) return PROJ_OK;
+    if (!Y) return PROJ_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(Y) % (y_dtype == PROJ_F32 ? 4 : 2) != 0) return PROJ_ERR_MISALIGNED;
+    if (bias && reinterpret_cast<uintptr_t>(bias) % 2 != 0) return PROJ_ERR_MISALIGNED;
+    cudaStream_t s = as_stream(stream);
+
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return PROJ_ERR_CUDA;
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
+        return PROJ_ERR_CUDA;
+    if (major != 10 || minor != 3) return PROJ_ERR_UNSUPPORTED;
+
+    proj_device_desc_t dd{sms, smem};
+    proj_plan_desc_t plan;
+    proj_status_t st = proj_plan_compute(M, N, K, w_layout, y_dtype, bias != nullptr, &dd, &plan);
+    if (st != PROJ_OK) return st;
+    if (plan.kernel == PROJ_KERNEL_FILL) {
+        dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(M, N, static_cast<const uint16_t *>(bias),
+                                                                 Y, y_dtype == PROJ_F32);
+        return check_launch();
+    }
+    // The plan's scratch must fit the static array; larger problems are refused.
+    if (static_cast<size_t>(plan.scratch_bytes) > kNoAllocScratchBytes) return PROJ_ERR_UNSUPPORTED;
+    if (!X || !W) return PROJ_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(W)) return PROJ_ERR_MISALIGNED;
+
+    void *scratch = nullptr;
+    st = noalloc_scratch_for(device, &scratch);
+    if (st != PROJ_OK) return st;
+    const int64_t partial_bytes =
+        plan.tiles_sk > 0 ? int64_t(2) * plan.grid * plan.block_t * kBlockN * 4 : 0;
+    uint8_t *sc = static_cast<uint8_t *>(scratch);
+    // The array keeps the previous call's contents: counters and the status
+    // word must start at zero (partials are fully rewritten before use).
+    if (cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(plan.scratch_bytes - partial_bytes),
+                        s) != cudaSuccess) {
+        cudaGetLastError();
+        return PROJ_ERR_CUDA;
+    }
+
+    CUtensorMap map_x, map_w;
+    if (!encode_2d(&map_x, X, K, M, K * 2, kBlockK, plan.block_t)) return PROJ_ERR_CUDA;
+    const bool ok = w_layout == PROJ_W_NK ? encode_2d(&map_w, W, K, N, K * 2, kBlockK, kBlockN)
+                                          : encode_2d(&map_w, W, N, K, N * 2, 64, kBlockK);
+    if (!ok) return PROJ_ERR_CUDA;
+
+    KernelParams kp{};
+    kp.M = static_cast<int32_t>(M);
+    kp.N = static_cast<int32_t>(N);
+    kp.K = static_cast<int32_t>(K);
+    params_from_plan(plan, kp);
+    kp.idesc = make_idesc(kBlockN, plan.block_t, w_layout == PROJ_W_KN);
+    kp.w_kn = w_layout == PROJ_W_KN;
+    kp.y_f32 = y_dtype == PROJ_F32;
+    kp.wait_limit_ns = kDefaultWaitLimitNs;
+    kp.w_prefetch = 0;
+    kp.bias = static_cast<const uint16_t *>(bias);
+    kp.Y = Y;
+    kp.partials = reinterpret_cast<float *>(sc);
+    kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);
+    kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
+    kp.trace = nullptr;
+    if (cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             plan.smem_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return PROJ_ERR_CUDA;
+    }
+    dev::proj_tc_kernel<<<plan.grid, plan.threads, plan.smem_bytes, s>>>(kp, map_w, map_x);
+    return check_launch();
+}

@@ -267,6 +267,32 @@ proj_status_t proj_get_plan(proj_handle_t h, proj_plan_desc_t *out);
  */
 proj_status_t proj_plan_info(proj_handle_t h, char *buf, size_t len);
 
+/*
+ * Allocation-free variant of proj_run, for callers that cannot call
+ * cudaMalloc: a serving loop where an allocation may synchronise the device
+ * and stall every other stream, or a plug-in whose host application owns all
+ * device memory.  The worklog has no counterpart of this call; it is an
+ * interface addition of this library.
+ *
+ * Same computation, layouts and argument rules as proj_create + proj_run
+ * (bf16 X, W, bias; y_dtype PROJ_BF16 or PROJ_F32; bias NULL for none), with
+ * no handle.  The caller passes inputs and outputs; the split-K scratch comes
+ * from one fixed device array of 8 MiB inside the library, which every GPU
+ * that loads the library holds until the process exits.  Nothing is allocated
+ * and no allocating library routine is called.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - Problems whose plan needs more scratch than 8 MiB (for example M > 32
+ *     with N a few thousand, where K is split) return PROJ_ERR_UNSUPPORTED.
+ *   - Every call shares the array: calls that overlap on the GPU (other
+ *     streams, other threads) race and give wrong results.  Each call clears
+ *     the array's counters and status word on `stream` before its kernel.
+ * Returns the same status codes as proj_create/proj_run.
+ */
+proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
+                               proj_dtype_t y_dtype, const void *X, const void *W,
+                               const void *bias, void *Y, void *stream);
+
 /* Free the handle and its scratch (synchronises the device).  NULL is a no-op. */
 proj_status_t proj_destroy(proj_handle_t h);
 
