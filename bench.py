@@ -68,12 +68,16 @@ def load_peaks() -> dict:
         return dict(FALLBACK_PEAKS, source="fallback")
 
 
+# Files that decide what the kernel reads and writes: its device code, the
+# shared work decomposition and the planner (host launch code does not).
+TRAFFIC_SOURCES = ("proj_kernel.cuh", "proj_internal.h", "planner.cpp")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC_DIR)):
-        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
-            with open(os.path.join(CSRC_DIR, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in TRAFFIC_SOURCES:
+        with open(os.path.join(CSRC_DIR, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
