@@ -111,6 +111,10 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
 
     out->tiles_m = ceil_div(M, bt);
     out->tiles_n = ceil_div(N, kBlockN);
+    // Raster groups of up to 8 token tiles: with 256-token tiles of a
+    // K = 8192 problem a group's token panels take 32 MiB, leaving room in L2
+    // for the weight panels its wave shares.
+    out->raster_group = static_cast<int32_t>(out->tiles_m < 8 ? out->tiles_m : 8);
     out->k_blocks = ceil_div(K, kBlockK);
     const int64_t tiles = out->tiles_m * out->tiles_n;
     const int64_t units = tiles * out->k_blocks;
@@ -177,8 +181,7 @@ extern "C" proj_status_t proj_plan_segments(const proj_plan_desc_t *plan, int32_
         if (n < cap) {
             proj_segment_t &o = out[n];
             o.tile = s.tile;
-            o.tile_m = s.tile % kp.tiles_m;
-            o.tile_n = s.tile / kp.tiles_m;
+            tile_coords(kp, s.tile, o.tile_m, o.tile_n);
             o.k_block_begin = s.kb0;
             o.k_block_end = s.kb1;
             o.slot = s.slot;
@@ -226,11 +229,11 @@ int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int
         "{\"kernel\": \"%s\", \"M\": %lld, \"N\": %lld, \"K\": %lld, \"w_layout\": \"%s\", "
         "\"y_dtype\": \"%s\", \"bias\": %s, \"block_n\": %d, \"block_t\": %d, \"block_k\": %d, "
         "\"stages\": %d, \"grid\": %d, \"threads\": %d, \"smem_bytes\": %d, "
-        "\"tmem_cols\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
+        "\"tmem_cols\": %d, \"raster_group\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
         "\"tiles_dp\": %lld, \"tiles_sk\": %lld, \"units_sk\": %lld, \"scratch_bytes\": %lld}",
         kname, (long long)M, (long long)N, (long long)K, w_layout == PROJ_W_NK ? "NK" : "KN",
         y_dtype == PROJ_F32 ? "f32" : "bf16", has_bias ? "true" : "false", p.block_n,
-        p.block_t, p.block_k, p.stages, p.grid, p.threads, p.smem_bytes, p.tmem_cols,
+        p.block_t, p.block_k, p.stages, p.grid, p.threads, p.smem_bytes, p.tmem_cols, p.raster_group,
         (long long)p.tiles_m, (long long)p.tiles_n, (long long)p.k_blocks,
         (long long)p.tiles_dp, (long long)p.tiles_sk, (long long)p.units_sk,
         (long long)p.scratch_bytes);

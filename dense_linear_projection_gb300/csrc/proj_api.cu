@@ -138,6 +138,11 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     if (const char *e = std::getenv("PROJ_FORCE_BLOCK_T")) force_bt = std::atoi(e);
     proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, force_bt, &plan);
     if (st != PROJ_OK) return st;
+    if (const char *e = std::getenv("PROJ_FORCE_RASTER_GROUP")) {  // tuning only
+        const int g = std::atoi(e);
+        if (g > 0 && plan.kernel == PROJ_KERNEL_TC)
+            plan.raster_group = static_cast<int32_t>(g < plan.tiles_m ? g : plan.tiles_m);
+    }
 
     proj_plan_s *h = new (std::nothrow) proj_plan_s();
     if (!h) return PROJ_ERR_OUT_OF_MEMORY;

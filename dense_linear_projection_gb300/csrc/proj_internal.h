@@ -63,7 +63,9 @@ int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int
 struct KernelParams {
     int32_t M, N, K;
     int32_t block_t;       // token rows per tile (MMA N)
-    int32_t tiles_m;       // tiles along M; tile t -> (tm = t % tiles_m, tn = t / tiles_m)
+    int32_t tiles_m;       // token-row tiles
+    int32_t tiles_n;       // weight-row tiles
+    int32_t raster_group;  // token tiles per raster group (tile order, see tile_coords)
     int32_t k_blocks;
     int32_t tiles_dp;      // whole tiles, dealt round-robin: CTA c gets c, c+G, ...
     int32_t grid;
@@ -92,7 +94,7 @@ struct KernelParams {
 // the exact code the GPU runs).
 // ----------------------------------------------------------------------------
 struct Segment {
-    int32_t tile;   // tile index; tm = tile % tiles_m, tn = tile / tiles_m
+    int32_t tile;   // tile index in raster order (tile_coords gives its coordinates)
     int32_t kb0;    // first k-block
     int32_t kb1;    // one past the last k-block
     int32_t slot;   // partial-sum slot (split segments), else -1
@@ -136,6 +138,20 @@ PROJ_HD bool cta_has_units(int32_t c, int64_t U, int32_t G) {
 // tile at each end; tiles it covers whole are never split).
 PROJ_HD int32_t split_slot(int32_t c, int32_t ts, int64_t U, int32_t G, int32_t k_blocks) {
     return 2 * c + (ts == static_cast<int32_t>(div_nonneg(unit_begin(c, U, G), k_blocks)) ? 0 : 1);
+}
+
+// Tile index -> (token tile, weight tile).  Tiles are ordered in groups of
+// raster_group token tiles: within a group the token tile varies fastest, then
+// the weight tile, so the tiles running at the same time share a few token
+// panels and a band of weight panels that stay in L2 together.
+PROJ_HD void tile_coords(const KernelParams &p, int32_t tile, int32_t &tm, int32_t &tn) {
+    const int32_t per_group = p.raster_group * p.tiles_n;
+    const int32_t g = tile / per_group;
+    const int32_t idx = tile - g * per_group;
+    const int32_t m_base = g * p.raster_group;
+    const int32_t gm = p.tiles_m - m_base < p.raster_group ? p.tiles_m - m_base : p.raster_group;
+    tm = m_base + idx % gm;
+    tn = idx / gm;
 }
 
 struct WorkIter {
@@ -187,6 +203,8 @@ struct WorkIter {
 inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.block_t = plan.block_t;
     kp.tiles_m = static_cast<int32_t>(plan.tiles_m);
+    kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
+    kp.raster_group = plan.raster_group > 0 ? plan.raster_group : static_cast<int32_t>(plan.tiles_m);
     kp.k_blocks = static_cast<int32_t>(plan.k_blocks);
     kp.tiles_dp = static_cast<int32_t>(plan.tiles_dp);
     kp.grid = plan.grid;

@@ -108,6 +108,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -324,7 +330,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const uint64_t pol_w = l2_policy_evict_first();  // W is read once
+            // W tiles are read once when there is a single token tile, so they
+            // need not stay in L2; with several token tiles they are reused.
+            const uint64_t pol_w = p.tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
             const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
             auto load_w = [&](uint32_t a_dst, uint32_t full, int32_t tn, int32_t kb) {
@@ -344,7 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 it.init(p, blockIdx.x);
                 Segment s;
                 while (pre < stages && it.next(p, s)) {
-                    const int32_t tn = s.tile / p.tiles_m;
+                    int32_t tm, tn;
+                    tile_coords(p, s.tile, tm, tn);
                     for (int32_t kb = s.kb0; kb < s.kb1 && pre < stages; ++kb) {
                         const uint32_t full = smem_u32(&ctl->full[pre]);
                         mbar_arrive_expect_tx(full, stage_bytes);  // W + X bytes of the stage
@@ -363,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             Segment s;
             bool ok = true;
             while (ok && it.next(p, s)) {
-                const int32_t tm = s.tile % p.tiles_m;
-                const int32_t tn = s.tile / p.tiles_m;
+                int32_t tm, tn;
+                tile_coords(p, s.tile, tm, tn);
                 for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
                     const uint32_t full = smem_u32(&ctl->full[stage]);
                     const uint32_t a_dst = base_addr + stage * stage_bytes;
@@ -461,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after_sync();
             if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
-            const int32_t tm = s.tile % p.tiles_m;
-            const int32_t tn = s.tile / p.tiles_m;
+            int32_t tm, tn;
+            tile_coords(p, s.tile, tm, tn);
             const int32_t n = tn * kBlockN + r;
             const int32_t m0 = tm * p.block_t;
             const int32_t mcount = min(p.block_t, p.M - m0);

@@ -119,7 +119,8 @@ typedef struct proj_plan_desc {
     int32_t threads;         /* threads per CTA */
     int32_t smem_bytes;      /* dynamic shared memory per CTA */
     int32_t tmem_cols;       /* tensor-memory columns allocated per CTA */
-    int32_t reserved0;
+    int32_t raster_group;    /* token tiles per raster group: tiles are numbered group by group,
+                                token tile fastest within a group, then weight tile */
     int64_t tiles_m;         /* ceil(M / block_t) */
     int64_t tiles_n;         /* ceil(N / block_n) */
     int64_t k_blocks;        /* ceil(K / block_k) */
@@ -140,7 +141,7 @@ proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t 
                                 const proj_device_desc_t *dev, proj_plan_desc_t *out);
 
 /* One stretch of work a CTA executes: k-blocks [k_block_begin, k_block_end)
- * of one tile (tile = tile_n · tiles_m + tile_m). */
+ * of one tile (its index in raster order and its token/weight coordinates). */
 typedef struct proj_segment {
     int32_t tile;
     int32_t tile_m;          /* token-row tile */

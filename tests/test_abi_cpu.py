@@ -77,10 +77,12 @@ def check_decomposition(p, M, N, K):
     assert p["block_t"] % 16 == 0 and 16 <= p["block_t"] <= 256
     cover = np.zeros((tiles, KT), dtype=np.int32)
     by_tile = collections.defaultdict(list)
+    coords = {}
     slots = set()
     for c in range(G):
         for (tile, tm, tn, kb0, kb1, slot, split) in dlp.proj_plan_segments(p, c):
-            assert tile == tn * p["tiles_m"] + tm and 0 <= kb0 < kb1 <= KT
+            assert 0 <= tm < p["tiles_m"] and 0 <= tn < p["tiles_n"] and 0 <= kb0 < kb1 <= KT
+            assert coords.setdefault(tile, (tm, tn)) == (tm, tn)
             cover[tile, kb0:kb1] += 1
             by_tile[tile].append((c, slot, split, kb0, kb1))
             if split:
@@ -89,6 +91,7 @@ def check_decomposition(p, M, N, K):
             else:
                 assert (kb0, kb1) == (0, KT) and slot == -1
     assert (cover == 1).all(), "every (tile, k-block) exactly once"
+    assert len(set(coords.values())) == tiles, "tile -> (token, weight) tile is one-to-one"
     share = p["units_sk"] // G if p["units_sk"] else 0
     for tile, segs in by_tile.items():
         split = len(segs) > 1
@@ -189,3 +192,18 @@ def test_scratch_and_stages():
     assert p["smem_bytes"] == p["stages"] * stage + 2048
     assert p["scratch_bytes"] >= 2 * p["grid"] * p["block_t"] * 128 * 4 + 4 * 4 * p["tiles_sk"]
     assert p["tmem_cols"] >= 2 * p["block_t"] and p["tmem_cols"] in (32, 64, 128, 256, 512)
+
+
+def test_raster_groups():
+    # Prefill: 16 token tiles in groups of 8; within a group the token tile
+    # varies fastest, so the first wave covers 8 token panels x 19 weight panels.
+    p = plan(4096, 8192, 8192)
+    assert p["raster_group"] == 8 and p["tiles_m"] == 16
+    first_wave = set()
+    for c in range(p["grid"]):
+        tile, tm, tn = dlp.proj_plan_segments(p, c)[0][:3]
+        assert tile == c
+        first_wave.add((tm, tn))
+    assert {tm for tm, _ in first_wave} == set(range(8))
+    assert len({tn for _, tn in first_wave}) == 19
+    assert plan(16, 8192, 8192)["raster_group"] == 1
