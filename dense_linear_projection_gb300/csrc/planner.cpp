@@ -103,8 +103,6 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
 
     out->kernel = PROJ_KERNEL_TC;
     out->block_t = bt;
-    out->stages = stages;
-    out->smem_bytes = stages * stage + kSmemReserve;
     // Two accumulator buffers (the epilogue of one tile overlaps the MMAs of
     // the next); TMEM is allocated in powers of two, at least 32 columns.
     out->tmem_cols = pow2_ceil(2 * bt < 32 ? 32 : 2 * bt);
@@ -138,6 +136,24 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     }
     out->tiles_dp = tiles - out->tiles_sk;
     out->units_sk = out->tiles_sk * out->k_blocks;
+
+    // Pipeline depth.  When the weights stream from HBM (a single token tile,
+    // or any split plan), about kInflightTarget bytes of stages per SM keep
+    // the memory system busy; more only lengthens its queues (measured on
+    // GB300: 8 stages of 18 KiB beat 12 for the 16-token decode shapes).  A
+    // CTA with few k-blocks also pays the fill of a deep ring: at most a third
+    // of its k-blocks.  Data-parallel plans over several token tiles are
+    // tensor-bound and keep the whole ring.
+    const bool streaming = out->tiles_m == 1 || out->tiles_sk > 0;
+    if (streaming) {
+        int32_t want = kInflightTarget / stage;
+        const int64_t units_per_cta = (out->tiles_dp * out->k_blocks + out->units_sk) / grid;
+        if (units_per_cta / 3 < want) want = static_cast<int32_t>(units_per_cta / 3);
+        if (want < 2) want = 2;
+        if (want < stages) stages = want;
+    }
+    out->stages = stages;
+    out->smem_bytes = stages * stage + kSmemReserve;
 
     // Scratch: one partial tile per (CTA, first|last split segment), one
     // completion counter per (split tile, 32-row quarter), and the device

@@ -138,6 +138,13 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     if (const char *e = std::getenv("PROJ_FORCE_BLOCK_T")) force_bt = std::atoi(e);
     proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, force_bt, &plan);
     if (st != PROJ_OK) return st;
+    if (const char *e = std::getenv("PROJ_FORCE_STAGES")) {  // tuning only
+        const int st_force = std::atoi(e);
+        if (st_force >= 2 && st_force < plan.stages && plan.kernel == PROJ_KERNEL_TC) {
+            plan.stages = st_force;
+            plan.smem_bytes = st_force * stage_bytes_for(plan.block_t) + kSmemReserve;
+        }
+    }
     if (const char *e = std::getenv("PROJ_FORCE_RASTER_GROUP")) {  // tuning only
         const int g = std::atoi(e);
         if (g > 0 && plan.kernel == PROJ_KERNEL_TC)
@@ -179,8 +186,10 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         // Counters and the status word start at zero; partials need no clearing.
         if (cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(plan.scratch_bytes - partial_bytes),
                             as_stream(stream)) != cudaSuccess ||
+            // The attribute belongs to the kernel, not to this handle: set it
+            // to the device maximum so every handle's launch fits under it.
             cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 plan.smem_bytes) != cudaSuccess ||
+                                 static_cast<int>(prop.sharedMemPerBlockOptin)) != cudaSuccess ||
             cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
             cudaGetLastError();
             cudaFree(h->scratch);
@@ -484,7 +493,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
     kp.trace = nullptr;
     if (cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             plan.smem_bytes) != cudaSuccess) {
+                             smem) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }

@@ -19,6 +19,7 @@ constexpr int32_t kBlockK = 64;        // K per stage: 64 bf16 = one 128-byte sw
 constexpr int32_t kMmaK = 16;          // K per tcgen05.mma (kind::f16)
 constexpr int32_t kMaxTokenTile = 256; // tcgen05 MMA N limit for cta_group::1
 constexpr int32_t kMaxStages = 12;
+constexpr int32_t kInflightTarget = 160 * 1024;  // stage bytes per SM when streaming W from HBM
 constexpr int32_t kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int32_t kEpilogueThreads = 128;
 constexpr int32_t kSmemReserve = 2048; // 1024-byte alignment slack + barriers

@@ -326,3 +326,20 @@ def test_overlap_modes_see_inputs_written_just_before(mode):
     for i in range(6):
         gu.assert_within_tol(gu.y_to_f64(Ys[i]), refs[i % 2], f"mode {mode} run {i}")
     assert torch.equal(Ys[0].view(torch.int16), Ys[2].view(torch.int16))
+
+
+def test_handles_with_different_rings_in_any_creation_order():
+    # Plans differ in pipeline depth and so in shared memory; creating a
+    # small-ring handle after a large-ring one must not break the large one.
+    import torch
+    ws = [synth.Workload("big", 16, 8192, 8192, synth.W_NK, False, "f32", 51),
+          synth.Workload("small", 40, 520, 1024, synth.W_KN, True, "bf16", 52)]
+    inps = [synth.make_inputs(w) for w in ws]
+    runs = [gu.run(w, i) for w, i in zip(ws, inps)]
+    assert runs[0][0].plan["smem_bytes"] > runs[1][0].plan["smem_bytes"]
+    for (proj, Y, t) in runs:
+        proj(*t, out=Y)
+    torch.cuda.synchronize()
+    for w, inp, (proj, Y, _) in zip(ws, inps, runs):
+        r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
+        gu.assert_within_tol(gu.y_to_f64(Y), r, w.name)
