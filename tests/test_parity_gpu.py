@@ -329,17 +329,21 @@ def test_overlap_modes_see_inputs_written_just_before(mode):
 
 
 def test_handles_with_different_rings_in_any_creation_order():
-    # Plans differ in pipeline depth and so in shared memory; creating a
-    # small-ring handle after a large-ring one must not break the large one.
+    # Plans differ in shared memory; creating a second handle must not break
+    # launches of the first, whichever of the two needs more.
     import torch
-    ws = [synth.Workload("big", 16, 8192, 8192, synth.W_NK, False, "f32", 51),
-          synth.Workload("small", 40, 520, 1024, synth.W_KN, True, "bf16", 52)]
+    ws = [synth.Workload("a", 16, 8192, 8192, synth.W_NK, False, "f32", 51),
+          synth.Workload("b", 40, 520, 1024, synth.W_KN, True, "bf16", 52),
+          synth.Workload("c", 4096, 1024, 512, synth.W_NK, False, "bf16", 53)]
     inps = [synth.make_inputs(w) for w in ws]
-    runs = [gu.run(w, i) for w, i in zip(ws, inps)]
-    assert runs[0][0].plan["smem_bytes"] > runs[1][0].plan["smem_bytes"]
-    for (proj, Y, t) in runs:
-        proj(*t, out=Y)
-    torch.cuda.synchronize()
-    for w, inp, (proj, Y, _) in zip(ws, inps, runs):
-        r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
-        gu.assert_within_tol(gu.y_to_f64(Y), r, w.name)
+    for order in ([0, 1, 2], [2, 1, 0]):
+        runs = {i: gu.run(ws[i], inps[i]) for i in order}
+        assert len({runs[i][0].plan["smem_bytes"] for i in order}) > 1
+        for i in order:
+            proj, Y, t = runs[i]
+            proj(*t, out=Y)
+        torch.cuda.synchronize()
+        for i in order:
+            w, inp, (proj, Y, _) = ws[i], inps[i], runs[i]
+            r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
+            gu.assert_within_tol(gu.y_to_f64(Y), r, w.name)
