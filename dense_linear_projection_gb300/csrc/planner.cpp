@@ -41,8 +41,8 @@ int32_t token_tile_for(int64_t M) {
     return static_cast<int32_t>(bt < 16 ? 16 : bt);
 }
 
-int32_t stage_bytes_for(int32_t block_t) {
-    return kBlockN * kBlockK * 2 + block_t * kBlockK * 2;
+int32_t stage_bytes_for(int32_t b_rows) {
+    return kBlockA * kBlockK * 2 + b_rows * kBlockK * 2;
 }
 
 }  // namespace projgb
@@ -53,7 +53,7 @@ namespace projgb {
 
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
                            proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t *dev,
-                           int32_t force_block_t, proj_plan_desc_t *out) {
+                           int32_t force_block_t, int32_t force_block_n, proj_plan_desc_t *out) {
     if (!dev || !out) return PROJ_ERR_INVALID_ARG;
     *out = proj_plan_desc_t{};
     if (M < 0 || N < 0 || K < 0) return PROJ_ERR_INVALID_ARG;
@@ -63,7 +63,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     if (has_bias != 0 && has_bias != 1) return PROJ_ERR_INVALID_ARG;
     if (dev->sm_count < 1) return PROJ_ERR_INVALID_ARG;
 
-    out->block_n = kBlockN;
+    out->block_n = kBlockA;
     out->block_k = kBlockK;
     out->threads = kThreads;
     if (M == 0 || N == 0) {
@@ -78,59 +78,103 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         out->threads = 256;
         return PROJ_OK;
     }
+    if (force_block_t > 0 && (force_block_t % 16 != 0 || force_block_t > kMaxTokenTile))
+        return PROJ_ERR_INVALID_ARG;
+    const int32_t n_step = w_layout == PROJ_W_KN ? 64 : 16;  // [K,N] weights load in 64-row boxes
+    if (force_block_n > 0 && (force_block_n % n_step != 0 || force_block_n > kMaxTokenTile))
+        return PROJ_ERR_INVALID_ARG;
+    const int64_t sms = dev->sm_count;
 
-    int32_t bt = token_tile_for(M);
-    if (force_block_t > 0) {
-        if (force_block_t % 16 != 0 || force_block_t > kMaxTokenTile) return PROJ_ERR_INVALID_ARG;
-        bt = force_block_t;
+    // Orientation.  The swapped product (128 weight rows on the MMA's M side,
+    // up to 256 token rows on its N side) serves every shape whose swapped
+    // tiles cover the SMs; it measures faster than the token-major tiles of
+    // the same size for the 4096-token prefill shape.  When 256-token swapped
+    // tiles would leave SMs idle and there are at least 128 token rows, the
+    // tokens take the M side and the weight rows the N side, whose width (a
+    // multiple of 16) is free: it is chosen so the tiles fill whole waves.
+    const bool swap_fills = ceil_div(M, kMaxTokenTile) * ceil_div(N, kBlockA) >= sms;
+    const bool swap = force_block_n > 0 ? false
+                                        : (force_block_t > 0 || M < kBlockA || swap_fills);
+    int32_t bt, bn;
+    if (swap) {
+        bn = kBlockA;
+        bt = force_block_t > 0 ? force_block_t : token_tile_for(M);
+        if (force_block_t <= 0) {
+            // With more token rows than one tile holds but fewer tiles than
+            // SMs, halve the token tile until every SM has a tile.
+            const int64_t tiles_n = ceil_div(N, kBlockA);
+            while (bt > 64 && ceil_div(M, bt) * tiles_n < sms) {
+                const int32_t half = static_cast<int32_t>(ceil_div(bt / 2, 16) * 16);
+                if (half >= bt) break;
+                bt = half;
+            }
+        }
     } else {
-        // With more token rows than one tile holds but fewer tiles than SMs,
-        // halve the token tile until every SM has a tile (each extra token
-        // tile rereads the weight tile, mostly from L2, instead of leaving
-        // SMs idle or splitting K three ways).
-        const int64_t tiles_n = ceil_div(N, kBlockN);
-        while (bt > 64 && ceil_div(M, bt) * tiles_n < dev->sm_count) {
-            const int32_t half = static_cast<int32_t>(ceil_div(bt / 2, 16) * 16);
-            if (half >= bt) break;
-            bt = half;
+        bt = kBlockA;
+        if (force_block_n > 0) {
+            bn = force_block_n;
+        } else {
+            // Per-SM time ~ waves x (block_n + a fixed share for the token
+            // tile's own loads); the widest block_n wins ties.
+            const int64_t tiles_m = ceil_div(M, bt);
+            int64_t best_cost = -1;
+            bn = kMaxTokenTile;
+            for (int32_t cand = kMaxTokenTile; cand >= 64; cand -= n_step) {
+                const int64_t tiles = tiles_m * ceil_div(N, cand);
+                const int64_t waves = ceil_div(tiles, sms);
+                const int64_t cost = waves * (cand + 32);
+                if (best_cost < 0 || cost < best_cost) {
+                    best_cost = cost;
+                    bn = cand;
+                }
+            }
         }
     }
-    const int32_t stage = stage_bytes_for(bt);
+    const int32_t b_rows = swap ? bt : bn;
+    const int32_t stage = stage_bytes_for(b_rows);
     const int32_t budget = dev->smem_optin_bytes - kSmemReserve;
     int32_t stages = budget / stage;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return PROJ_ERR_UNSUPPORTED;
 
     out->kernel = PROJ_KERNEL_TC;
+    out->swap_ab = swap ? 1 : 0;
     out->block_t = bt;
+    out->block_n = bn;
     // Two accumulator buffers (the epilogue of one tile overlaps the MMAs of
     // the next); TMEM is allocated in powers of two, at least 32 columns.
-    out->tmem_cols = pow2_ceil(2 * bt < 32 ? 32 : 2 * bt);
+    out->tmem_cols = pow2_ceil(2 * b_rows < 32 ? 32 : 2 * b_rows);
 
     out->tiles_m = ceil_div(M, bt);
-    out->tiles_n = ceil_div(N, kBlockN);
-    // Raster groups of up to 8 token tiles: with 256-token tiles of a
-    // K = 8192 problem a group's token panels take 32 MiB, leaving room in L2
-    // for the weight panels its wave shares.
-    out->raster_group = static_cast<int32_t>(out->tiles_m < 8 ? out->tiles_m : 8);
+    out->tiles_n = ceil_div(N, bn);
+    // Raster groups of about 2048 token rows: with K = 8192 a group's token
+    // panels take 32 MiB, leaving room in L2 for the weight panels its wave
+    // shares.
+    {
+        int64_t g = 2048 / bt;
+        if (g < 1) g = 1;
+        out->raster_group = static_cast<int32_t>(out->tiles_m < g ? out->tiles_m : g);
+    }
     out->k_blocks = ceil_div(K, kBlockK);
     const int64_t tiles = out->tiles_m * out->tiles_n;
     const int64_t units = tiles * out->k_blocks;
-    const int64_t grid = units < dev->sm_count ? units : dev->sm_count;
+    const int64_t grid = units < sms ? units : sms;
     out->grid = static_cast<int32_t>(grid);
     // Whole tiles in data-parallel waves, except that the last partial wave
     // and one full wave before it are shared along K by every CTA (the
     // "data-parallel + two-tile stream-K" hybrid).  Each CTA then owns at
     // least one tile's worth of K blocks, so a split tile has exactly two
-    // contributors.  With fewer tiles than CTAs everything is split.
+    // contributors.  With fewer tiles than CTAs everything is split.  Whole
+    // tiles only when the last wave is nearly full: 95 % for the swapped
+    // (weight-streaming) plans, 80 % for the tensor-bound token-major plans,
+    // whose split partial tiles are large.
     const int64_t rem = tiles % grid;
     const int64_t waves = (tiles + grid - 1) / grid;
-    if (tiles < grid) {
-        out->tiles_sk = tiles;
-    } else if (rem == 0 || 20 * tiles >= 19 * waves * grid) {
-        // Whole tiles only: no partial wave, or the partial wave idles less
-        // than 5 % of the SM time, which costs less than splitting K.
+    const int64_t fill_pct = swap ? 95 : 80;
+    if (rem == 0 || 100 * tiles >= fill_pct * waves * grid) {
         out->tiles_sk = 0;
+    } else if (tiles < grid) {
+        out->tiles_sk = tiles;
     } else {
         out->tiles_sk = rem + grid;
     }
@@ -159,7 +203,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // completion counter per (split tile, 32-row quarter), and the device
     // status word.
     int64_t partial_bytes = 0;
-    if (out->tiles_sk > 0) partial_bytes = 2 * grid * int64_t(bt) * kBlockN * 4;
+    if (out->tiles_sk > 0) partial_bytes = 2 * grid * int64_t(kBlockA) * b_rows * 4;
     const int64_t counter_bytes = ((out->tiles_sk * 4 * 4 + 255) / 256) * 256;
     out->scratch_bytes = partial_bytes + counter_bytes + 256;
     (void)has_bias;
@@ -172,7 +216,7 @@ extern "C" proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K,
                                            proj_wlayout_t w_layout, proj_dtype_t y_dtype,
                                            int has_bias, const proj_device_desc_t *dev,
                                            proj_plan_desc_t *out) {
-    return plan_compute(M, N, K, w_layout, y_dtype, has_bias, dev, 0, out);
+    return plan_compute(M, N, K, w_layout, y_dtype, has_bias, dev, 0, 0, out);
 }
 
 static bool plan_is_tc(const proj_plan_desc_t *plan) {
@@ -245,11 +289,12 @@ int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int
         "{\"kernel\": \"%s\", \"M\": %lld, \"N\": %lld, \"K\": %lld, \"w_layout\": \"%s\", "
         "\"y_dtype\": \"%s\", \"bias\": %s, \"block_n\": %d, \"block_t\": %d, \"block_k\": %d, "
         "\"stages\": %d, \"grid\": %d, \"threads\": %d, \"smem_bytes\": %d, "
-        "\"tmem_cols\": %d, \"raster_group\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
+        "\"tmem_cols\": %d, \"raster_group\": %d, \"swap_ab\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
         "\"tiles_dp\": %lld, \"tiles_sk\": %lld, \"units_sk\": %lld, \"scratch_bytes\": %lld}",
         kname, (long long)M, (long long)N, (long long)K, w_layout == PROJ_W_NK ? "NK" : "KN",
         y_dtype == PROJ_F32 ? "f32" : "bf16", has_bias ? "true" : "false", p.block_n,
         p.block_t, p.block_k, p.stages, p.grid, p.threads, p.smem_bytes, p.tmem_cols, p.raster_group,
+        p.swap_ab,
         (long long)p.tiles_m, (long long)p.tiles_n, (long long)p.k_blocks,
         (long long)p.tiles_dp, (long long)p.tiles_sk, (long long)p.units_sk,
         (long long)p.scratch_bytes);

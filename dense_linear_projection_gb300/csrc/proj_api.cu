@@ -75,18 +75,40 @@ bool encode_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-uint32_t make_idesc(int mma_m, int mma_n, bool a_mn_major) {
+uint32_t make_idesc(int mma_m, int mma_n, bool a_mn_major, bool b_mn_major) {
     // tcgen05 instruction descriptor, kind::f16: fp32 accumulator (bits 4-5),
-    // bf16 A (7-9) and B (10-12), A major-ness (15), B K-major (16 = 0),
+    // bf16 A (7-9) and B (10-12), A major-ness (15), B major-ness (16),
     // N >> 3 (17-22), M >> 4 (24-28).
     uint32_t d = 0;
     d |= 1u << 4;
     d |= 1u << 7;
     d |= 1u << 10;
     if (a_mn_major) d |= 1u << 15;
+    if (b_mn_major) d |= 1u << 16;
     d |= static_cast<uint32_t>(mma_n >> 3) << 17;
     d |= static_cast<uint32_t>(mma_m >> 4) << 24;
     return d;
+}
+
+// Instruction descriptor of a plan: M = 128, N = B rows; [K,N] weights are
+// MN-major in whichever operand they occupy.
+uint32_t idesc_of(const proj_plan_desc_t &plan, int w_layout) {
+    const bool kn = w_layout == PROJ_W_KN;
+    const int b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
+    return make_idesc(kBlockA, b_rows, plan.swap_ab && kn, !plan.swap_ab && kn);
+}
+
+// Bytes of split-K partial tiles in the scratch (the rest is counters and
+// the status word).
+int64_t partial_bytes_of(const proj_plan_desc_t &plan) {
+    const int64_t b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
+    return plan.tiles_sk > 0 ? int64_t(2) * plan.grid * kBlockA * b_rows * 4 : 0;
+}
+
+// Y rows start on 16-byte boundaries: vector stores of 16 outputs are safe.
+int y_vec_of(const void *Y, int64_t N, int y_dtype) {
+    const int64_t row_bytes = N * (y_dtype == PROJ_F32 ? 4 : 2);
+    return (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(Y) % 16 == 0);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -134,15 +156,24 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
 
     proj_device_desc_t dd{prop.multiProcessorCount, static_cast<int32_t>(prop.sharedMemPerBlockOptin)};
     proj_plan_desc_t plan;
-    int32_t force_bt = 0;
+    int32_t force_bt = 0, force_bn = 0;  // tuning only
     if (const char *e = std::getenv("PROJ_FORCE_BLOCK_T")) force_bt = std::atoi(e);
-    proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, force_bt, &plan);
+    if (const char *e = std::getenv("PROJ_FORCE_BLOCK_N")) force_bn = std::atoi(e);
+    proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, force_bt, force_bn, &plan);
     if (st != PROJ_OK) return st;
+    if (const char *e = std::getenv("PROJ_FORCE_WHOLE_TILES")) {  // tuning only
+        if (std::atoi(e) == 1 && plan.kernel == PROJ_KERNEL_TC && plan.tiles_sk > 0) {
+            plan.tiles_dp += plan.tiles_sk;
+            plan.tiles_sk = 0;
+            plan.units_sk = 0;
+        }
+    }
     if (const char *e = std::getenv("PROJ_FORCE_STAGES")) {  // tuning only
         const int st_force = std::atoi(e);
         if (st_force >= 2 && st_force < plan.stages && plan.kernel == PROJ_KERNEL_TC) {
             plan.stages = st_force;
-            plan.smem_bytes = st_force * stage_bytes_for(plan.block_t) + kSmemReserve;
+            plan.smem_bytes =
+                st_force * stage_bytes_for(plan.swap_ab ? plan.block_t : plan.block_n) + kSmemReserve;
         }
     }
     if (const char *e = std::getenv("PROJ_FORCE_RASTER_GROUP")) {  // tuning only
@@ -168,15 +199,14 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
             delete h;
             return PROJ_ERR_OUT_OF_MEMORY;
         }
-        const int64_t partial_bytes =
-            plan.tiles_sk > 0 ? int64_t(2) * plan.grid * plan.block_t * kBlockN * 4 : 0;
+        const int64_t partial_bytes = partial_bytes_of(plan);
         uint8_t *sc = static_cast<uint8_t *>(h->scratch);
         KernelParams &kp = h->params;
         kp.M = static_cast<int32_t>(M);
         kp.N = static_cast<int32_t>(N);
         kp.K = static_cast<int32_t>(K);
         params_from_plan(plan, kp);
-        kp.idesc = make_idesc(kBlockN, plan.block_t, w_layout == PROJ_W_KN);
+        kp.idesc = idesc_of(plan, w_layout);
         kp.w_kn = w_layout == PROJ_W_KN;
         kp.y_f32 = y_dtype == PROJ_F32;
         kp.wait_limit_ns = kDefaultWaitLimitNs;
@@ -230,7 +260,7 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
     }
     if (W != h->map_w_ptr) {
         const bool ok = h->w_layout == PROJ_W_NK
-                            ? encode_2d(&h->map_w, W, h->K, h->N, h->K * 2, kBlockK, kBlockN)
+                            ? encode_2d(&h->map_w, W, h->K, h->N, h->K * 2, kBlockK, plan.block_n)
                             : encode_2d(&h->map_w, W, h->N, h->K, h->N * 2, 64, kBlockK);
         if (!ok) {
             h->map_w_ptr = nullptr;
@@ -241,6 +271,7 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
     KernelParams kp = h->params;
     kp.bias = static_cast<const uint16_t *>(bias);
     kp.Y = Y;
+    kp.y_vec = y_vec_of(Y, h->N, h->y_dtype);
     kp.trace = h->trace;
     kp.w_prefetch = h->overlap == PROJ_OVERLAP_WEIGHTS;
     cudaLaunchConfig_t cfg = {};
@@ -297,15 +328,15 @@ proj_status_t proj_device_status(proj_handle_t h, void *stream) {
     if (cudaMemcpy(&word, h->params.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
         return PROJ_ERR_CUDA;
     if (word == 0) return PROJ_OK;
+    const proj_status_t what = (word & kErrSmemTooSmall) ? PROJ_ERR_CUDA : PROJ_ERR_DEVICE_TIMEOUT;
     // Clear the word and the split-K counters (a run that gave up may have
     // left some mid-count) so the handle is usable again.
     const proj_plan_desc_t &plan = h->plan;
-    const int64_t partial_bytes =
-        plan.tiles_sk > 0 ? int64_t(2) * plan.grid * plan.block_t * kBlockN * 4 : 0;
+    const int64_t partial_bytes = partial_bytes_of(plan);
     if (cudaMemset(static_cast<uint8_t *>(h->scratch) + partial_bytes, 0,
                    static_cast<size_t>(plan.scratch_bytes - partial_bytes)) != cudaSuccess)
         return PROJ_ERR_CUDA;
-    return PROJ_ERR_DEVICE_TIMEOUT;
+    return what;
 }
 
 proj_status_t proj_set_overlap(proj_handle_t h, proj_overlap_t mode) {
@@ -459,8 +490,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     void *scratch = nullptr;
     st = noalloc_scratch_for(device, &scratch);
     if (st != PROJ_OK) return st;
-    const int64_t partial_bytes =
-        plan.tiles_sk > 0 ? int64_t(2) * plan.grid * plan.block_t * kBlockN * 4 : 0;
+    const int64_t partial_bytes = partial_bytes_of(plan);
     uint8_t *sc = static_cast<uint8_t *>(scratch);
     // The array keeps the previous call's contents: counters and the status
     // word must start at zero (partials are fully rewritten before use).
@@ -472,7 +502,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
 
     CUtensorMap map_x, map_w;
     if (!encode_2d(&map_x, X, K, M, K * 2, kBlockK, plan.block_t)) return PROJ_ERR_CUDA;
-    const bool ok = w_layout == PROJ_W_NK ? encode_2d(&map_w, W, K, N, K * 2, kBlockK, kBlockN)
+    const bool ok = w_layout == PROJ_W_NK ? encode_2d(&map_w, W, K, N, K * 2, kBlockK, plan.block_n)
                                           : encode_2d(&map_w, W, N, K, N * 2, 64, kBlockK);
     if (!ok) return PROJ_ERR_CUDA;
 
@@ -481,13 +511,14 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.N = static_cast<int32_t>(N);
     kp.K = static_cast<int32_t>(K);
     params_from_plan(plan, kp);
-    kp.idesc = make_idesc(kBlockN, plan.block_t, w_layout == PROJ_W_KN);
+    kp.idesc = idesc_of(plan, w_layout);
     kp.w_kn = w_layout == PROJ_W_KN;
     kp.y_f32 = y_dtype == PROJ_F32;
     kp.wait_limit_ns = kDefaultWaitLimitNs;
     kp.w_prefetch = 0;
     kp.bias = static_cast<const uint16_t *>(bias);
     kp.Y = Y;
+    kp.y_vec = y_vec_of(Y, N, y_dtype);
     kp.partials = reinterpret_cast<float *>(sc);
     kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);
     kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);

@@ -14,7 +14,7 @@
 
 namespace projgb {
 
-constexpr int32_t kBlockN = 128;       // weight rows per tile = tcgen05 MMA M
+constexpr int32_t kBlockA = 128;       // rows of the MMA's A operand (tcgen05 M)
 constexpr int32_t kBlockK = 64;        // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int32_t kMmaK = 16;          // K per tcgen05.mma (kind::f16)
 constexpr int32_t kMaxTokenTile = 256; // tcgen05 MMA N limit for cta_group::1
@@ -48,14 +48,19 @@ constexpr int kErrWaitMma = 1 << 1;
 constexpr int kErrWaitEpilogue = 1 << 2;
 constexpr int kErrWaitDrain = 1 << 3;
 constexpr int kErrSelfTest = 1 << 4;
+constexpr int kErrSmemTooSmall = 1 << 5;  // launch gave less shared memory than the ring needs
 
 int32_t token_tile_for(int64_t M);
-// The planner behind proj_plan_compute; force_block_t > 0 overrides the token
-// tile (tuning only: proj_create takes it from PROJ_FORCE_BLOCK_T).
+// The planner behind proj_plan_compute.  Tuning overrides (proj_create takes
+// them from PROJ_FORCE_BLOCK_T / PROJ_FORCE_BLOCK_N): force_block_t > 0 forces
+// the swapped orientation with that token tile; force_block_n > 0 forces the
+// token-rows-on-M orientation with that weight tile.
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
                            proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t *dev,
-                           int32_t force_block_t, proj_plan_desc_t *out);
-int32_t stage_bytes_for(int32_t block_t);
+                           int32_t force_block_t, int32_t force_block_n, proj_plan_desc_t *out);
+// Shared-memory bytes of one pipeline stage: A (128 rows x 64 K) plus B
+// (b_rows x 64 K), bf16.
+int32_t stage_bytes_for(int32_t b_rows);
 int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int w_layout,
                  int y_dtype, int has_bias, char *buf, size_t len);
 
@@ -63,7 +68,10 @@ int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int
 // __grid_constant__ arguments).
 struct KernelParams {
     int32_t M, N, K;
-    int32_t block_t;       // token rows per tile (MMA N)
+    int32_t swap;          // 1: A = weight rows, B = token rows; 0: A = token rows, B = weight rows
+    int32_t block_t;       // token rows per tile
+    int32_t block_n;       // weight rows per tile
+    int32_t b_rows;        // rows of the B operand (MMA N): block_t if swap, else block_n
     int32_t tiles_m;       // token-row tiles
     int32_t tiles_n;       // weight-row tiles
     int32_t raster_group;  // token tiles per raster group (tile order, see tile_coords)
@@ -76,14 +84,15 @@ struct KernelParams {
     int32_t stages;
     int32_t stage_bytes;
     int32_t tmem_cols;
-    uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128, N=block_t)
+    uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128, N=b_rows)
     int32_t w_kn;          // W stored [K,N] (MN-major A operand)
     int32_t y_f32;         // store fp32 (else bf16)
+    int32_t y_vec;         // Y rows start 16-byte aligned (N·size % 16 == 0, aligned base)
     int64_t wait_limit_ns; // bounded device waits give up after this long
     int32_t w_prefetch;    // stream the first stages of W before the preceding kernel completes
     const uint16_t *bias;  // [N] bf16 or nullptr
     void *Y;
-    float *partials;       // [2*grid][128 rows][block_t] fp32 partial tiles
+    float *partials;       // [2*grid][128 rows][b_rows] fp32 partial tiles
     uint32_t *counters;    // [4 * (tiles - tiles_dp)]: one per (split tile, row quarter)
     int *status;           // device status word
     unsigned long long *trace;  // [grid][kTraceSlots] phase trace, or nullptr
@@ -202,7 +211,10 @@ struct WorkIter {
 
 // Work-shape fields of the kernel parameters, from a plan.
 inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
+    kp.swap = plan.swap_ab;
     kp.block_t = plan.block_t;
+    kp.block_n = plan.block_n;
+    kp.b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
     kp.tiles_m = static_cast<int32_t>(plan.tiles_m);
     kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
     kp.raster_group = plan.raster_group > 0 ? plan.raster_group : static_cast<int32_t>(plan.tiles_m);
@@ -213,7 +225,7 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.sk_pair = plan.grid > 0 && plan.units_sk / plan.grid >= plan.k_blocks;
     kp.sk_dense = plan.units_sk >= plan.grid;
     kp.stages = plan.stages;
-    kp.stage_bytes = stage_bytes_for(plan.block_t);
+    kp.stage_bytes = stage_bytes_for(kp.b_rows);
     kp.tmem_cols = plan.tmem_cols;
 }
 

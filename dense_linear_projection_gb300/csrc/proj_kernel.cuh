@@ -278,6 +278,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Stage buffers need 1024-byte alignment (128-byte swizzle atoms).
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t base_addr = (raw_addr + 1023u) & ~1023u;
+    {
+        // The ring, its barriers and the alignment slack must fit the dynamic
+        // shared memory this launch received; otherwise record the error and
+        // leave before touching any of it.
+        uint32_t dyn_bytes;
+        asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+        const uint64_t need = static_cast<uint64_t>(base_addr - raw_addr) +
+                              static_cast<uint64_t>(p.stages) * static_cast<uint32_t>(p.stage_bytes) +
+                              sizeof(SmemCtl);
+        if (p.stages > kMaxStages || need > dyn_bytes) {
+            if (threadIdx.x == 0) atomicOr(p.status, kErrSmemTooSmall);
+            return;
+        }
+    }
     uint8_t *smem = smem_raw + (base_addr - raw_addr);
     SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + p.stages * p.stage_bytes);
     volatile int *abort_flag = &ctl->abort_flag;
@@ -285,7 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int32_t stages = p.stages;
-    const uint32_t a_bytes = kBlockN * kBlockK * 2;
+    const uint32_t a_bytes = kBlockA * kBlockK * 2;  // A region of a stage (16 KiB)
+    // Where W and X land in a stage: W is the A operand when swapped, else B.
+    const uint32_t w_off = p.swap ? 0u : a_bytes;
+    const uint32_t x_off = p.swap ? a_bytes : 0u;
 
     if (threadIdx.x == 0) {
         trace_stamp(p, kTraceEntry);
@@ -335,13 +352,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = p.tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
             const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
-            auto load_w = [&](uint32_t a_dst, uint32_t full, int32_t tn, int32_t kb) {
+            // One k-block of a weight tile: a [block_n rows x 64 K] box for
+            // [N,K] weights; for [K,N] weights, block_n/64 boxes of 64 N-rows
+            // x 64 K, 8 KiB apart (the MN-major operand layout).
+            auto load_w = [&](uint32_t dst, uint32_t full, int32_t tn, int32_t kb) {
                 if (!p.w_kn) {
-                    tma_load_2d(a_dst, &tmap_w, full, kb * kBlockK, tn * kBlockN, pol_w);
+                    tma_load_2d(dst, &tmap_w, full, kb * kBlockK, tn * p.block_n, pol_w);
                 } else {
-                    tma_load_2d(a_dst, &tmap_w, full, tn * kBlockN, kb * kBlockK, pol_w);
-                    tma_load_2d(a_dst + a_bytes / 2, &tmap_w, full, tn * kBlockN + 64, kb * kBlockK,
-                                pol_w);
+                    for (int32_t j = 0; j < p.block_n / 64; ++j)
+                        tma_load_2d(dst + static_cast<uint32_t>(j) * 8192u, &tmap_w, full,
+                                    tn * p.block_n + 64 * j, kb * kBlockK, pol_w);
                 }
             };
             // Optional weight prefetch: fill the ring with W before the
@@ -357,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int32_t kb = s.kb0; kb < s.kb1 && pre < stages; ++kb) {
                         const uint32_t full = smem_u32(&ctl->full[pre]);
                         mbar_arrive_expect_tx(full, stage_bytes);  // W + X bytes of the stage
-                        load_w(base_addr + static_cast<uint32_t>(pre) * stage_bytes, full, tn, kb);
+                        load_w(base_addr + static_cast<uint32_t>(pre) * stage_bytes + w_off, full, tn, kb);
                         ++pre;
                     }
                 }
@@ -376,8 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tile_coords(p, s.tile, tm, tn);
                 for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
                     const uint32_t full = smem_u32(&ctl->full[stage]);
-                    const uint32_t a_dst = base_addr + stage * stage_bytes;
-                    const uint32_t b_dst = a_dst + a_bytes;
+                    const uint32_t st_base = base_addr + stage * stage_bytes;
                     if (issued >= pre) {
                         if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.status,
                                         kErrWaitProducer, p.wait_limit_ns)) {
@@ -385,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(full, stage_bytes);
-                        load_w(a_dst, full, tn, kb);
+                        load_w(st_base + w_off, full, tn, kb);
                     }
-                    tma_load_2d(b_dst, &tmap_x, full, kb * kBlockK, tm * p.block_t, pol_x);
+                    tma_load_2d(st_base + x_off, &tmap_x, full, kb * kBlockK, tm * p.block_t, pol_x);
                     if (issued == 0 && pre == 0) trace_stamp(p, kTraceFirstLoad);
                     ++issued;
                     if (++stage == stages) {
@@ -402,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            const bool a_mn = p.swap && p.w_kn;   // weights [K,N] as the A operand
+            const bool b_mn = !p.swap && p.w_kn;  // weights [K,N] as the B operand
             int32_t stage = 0;
             uint32_t phase = 0;
             int32_t seg_idx = 0;
@@ -431,11 +452,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kBlockK / kMmaK; ++kk) {
                         // K-major: the next 16 K values start 32 bytes further
                         // along the 128-byte swizzled row.  MN-major (W stored
-                        // [K,N]): 16 more K rows, 16 × 128 bytes further.
+                        // [K,N]): 16 more K rows, 16 × 128 bytes further; its
+                        // 64-wide MN blocks are 8 KiB apart.
                         const uint64_t a_desc =
-                            p.w_kn ? smem_desc_sw128(a_addr + kk * (kMmaK * 128), a_bytes / 2, 1024)
-                                   : smem_desc_sw128(a_addr + kk * (kMmaK * 2), 16, 1024);
-                        const uint64_t b_desc = smem_desc_sw128(b_addr + kk * (kMmaK * 2), 16, 1024);
+                            a_mn ? smem_desc_sw128(a_addr + kk * (kMmaK * 128), 8192, 1024)
+                                 : smem_desc_sw128(a_addr + kk * (kMmaK * 2), 16, 1024);
+                        const uint64_t b_desc =
+                            b_mn ? smem_desc_sw128(b_addr + kk * (kMmaK * 128), 8192, 1024)
+                                 : smem_desc_sw128(b_addr + kk * (kMmaK * 2), 16, 1024);
                         tc_mma(d_tmem, a_desc, b_desc, p.idesc, (kb > s.kb0 || kk > 0) ? 1u : 0u);
                     }
                     tc_commit(smem_u32(&ctl->empty[stage]));  // stage free once these MMAs finish
@@ -472,21 +496,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
             int32_t tm, tn;
             tile_coords(p, s.tile, tm, tn);
-            const int32_t n = tn * kBlockN + r;
+            // Tensor-memory lane r holds one A row, columns hold B rows.
+            // Swapped: lane = weight row n, columns = token rows m.
+            // Otherwise: lane = token row m, columns = weight rows n.
             const int32_t m0 = tm * p.block_t;
-            const int32_t mcount = min(p.block_t, p.M - m0);
-            const int32_t nchunks = (mcount + 15) / 16;
+            const int32_t n0 = tn * p.block_n;
+            const int32_t lane_row = (p.swap ? n0 : m0) + r;
+            const bool lane_ok = lane_row < (p.swap ? p.N : p.M);
+            const int32_t ccount = p.swap ? min(p.block_t, p.M - m0) : min(p.block_n, p.N - n0);
+            const int32_t nchunks = (ccount + 15) / 16;
             const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(buf) * half_cols;
-
-            const bool n_ok = n < p.N;
-            const float bias_v = (p.bias != nullptr && n_ok) ? bf16_bits_to_float(p.bias[n]) : 0.f;
-            // Store one chunk of 16 output columns of this lane's row n.
+            const float bias_lane =
+                (p.swap && p.bias != nullptr && lane_ok) ? bf16_bits_to_float(p.bias[lane_row]) : 0.f;
+            // Store one chunk of 16 columns of this lane's row (+ bias).
             auto store_chunk = [&](int32_t ch, const float (&y)[16]) {
-                if (!n_ok) return;
+                if (!lane_ok) return;
+                if (p.swap) {
+                    const int32_t n = lane_row;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int32_t m = m0 + ch * 16 + i;
-                    if (m < p.M) store_y(p, static_cast<size_t>(m) * p.N + n, y[i] + bias_v);
+                    for (int i = 0; i < 16; ++i) {
+                        const int32_t m = m0 + ch * 16 + i;
+                        if (m < p.M) store_y(p, static_cast<size_t>(m) * p.N + n, y[i] + bias_lane);
+                    }
+                } else {
+                    const int32_t m = lane_row;
+                    const int32_t nb = n0 + ch * 16;
+                    float v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        v[i] = y[i] + ((p.bias != nullptr && nb + i < p.N) ? bf16_bits_to_float(p.bias[nb + i]) : 0.f);
+                    const size_t off = static_cast<size_t>(m) * p.N + nb;
+                    if (p.y_vec && nb + 16 <= p.N) {
+                        // 16 consecutive outputs of one row: vector stores.
+                        if (p.y_f32) {
+                            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.Y) + off);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                        } else {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                                w[i] = *reinterpret_cast<uint32_t *>(&h);
+                            }
+                            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) + off);
+                            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (nb + i < p.N) store_y(p, off + i, v[i]);
+                    }
                 }
             };
             auto release_accumulator = [&]() {
@@ -496,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
 
             if (!s.split) {
-                // Whole tile: tensor memory -> (+ bias) -> Y.  Lane = weight row n.
+                // Whole tile: tensor memory -> (+ bias) -> Y.
                 for (int32_t ch = 0; ch < nchunks; ++ch) {
                     float v[16];
                     tmem_load16(tbase + ch * 16, v);
@@ -505,9 +567,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 release_accumulator();
             } else {
                 // Split tile.  This lane's row of fp32 partial sums goes to
-                // scratch, laid out [slot][128 rows][block_t] (16 columns =
+                // scratch, laid out [slot][128 rows][b_rows] (16 columns =
                 // 64 contiguous bytes per lane per chunk).
-                float *own = p.partials + (static_cast<size_t>(s.slot) * kBlockN + r) * p.block_t;
+                float *own = p.partials + (static_cast<size_t>(s.slot) * kBlockA + r) * p.b_rows;
                 for (int32_t ch = 0; ch < nchunks; ++ch) {
                     float v[16];
                     tmem_load16(tbase + ch * 16, v);
@@ -557,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t other_slot =
                         s.kb0 == 0 ? 2 * (static_cast<int32_t>(blockIdx.x) + 1)
                                    : 2 * (static_cast<int32_t>(blockIdx.x) - 1) + 1;
-                    const float *other = p.partials + (static_cast<size_t>(other_slot) * kBlockN + r) * p.block_t;
+                    const float *other = p.partials + (static_cast<size_t>(other_slot) * kBlockA + r) * p.b_rows;
                     for (int32_t ch0 = 0; ch0 < nchunks; ch0 += 4) {
                         float4 o[4][4];
 #pragma unroll
@@ -600,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         const int32_t slot =
                                             p.sk_dense ? (cc == c_first ? first_slot : 2 * cc)
                                                        : split_slot(cc, ts, U, p.grid, p.k_blocks);
-                                        load_partial16(p.partials + (static_cast<size_t>(slot) * kBlockN + r) * p.block_t,
+                                        load_partial16(p.partials + (static_cast<size_t>(slot) * kBlockA + r) * p.b_rows,
                                                        ch, o[k]);
                                     }
                                 }

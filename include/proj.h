@@ -96,10 +96,13 @@ typedef struct proj_device_desc {
 /*
  * A plan: how one problem is cut into work for the GPU.
  *
- * Tiles: block_n weight rows (the tensor-core MMA's M side, which carries the
- * output features: the swapped product Yᵀ = W·Xᵀ, section "Prove the swapped
- * product before worrying about its speed") × block_t token rows (the MMA's
- * N side) × the whole K range, cut into k_blocks blocks of block_k.
+ * Tiles: block_t token rows × block_n weight rows × the whole K range, cut
+ * into k_blocks blocks of block_k.  With few tokens (M < 128) the swapped
+ * product Yᵀ = W·Xᵀ puts 128 weight rows on the tensor-core MMA's M side and
+ * the tokens (16..112) on its N side (section "Prove the swapped product
+ * before worrying about its speed"); with M ≥ 128, 128 tokens take the M side
+ * and block_n weight rows (a multiple of 16, of 64 for [K,N] weights) the N
+ * side, block_n chosen so the tiles fill whole waves of SMs.
  * Whole tiles are dealt out in data-parallel waves (tiles_dp); the remaining
  * tiles_sk tiles (the last partial wave plus one full wave, or every tile when
  * there are fewer tiles than CTAs; none when the last wave is nearly full) are
@@ -111,8 +114,8 @@ typedef struct proj_device_desc {
  */
 typedef struct proj_plan_desc {
     int32_t kernel;          /* proj_kernel_t */
-    int32_t block_n;         /* weight rows per tile (128) */
-    int32_t block_t;         /* token rows per tile: 16..256, multiple of 16 */
+    int32_t block_n;         /* weight rows per tile: 128 when swap_ab, else 64..256 */
+    int32_t block_t;         /* token rows per tile: 16..256 when swap_ab, else 128 */
     int32_t block_k;         /* K elements per pipeline stage (64 = 128 bytes) */
     int32_t stages;          /* shared-memory pipeline depth */
     int32_t grid;            /* CTAs launched (one per SM at most) */
@@ -121,6 +124,10 @@ typedef struct proj_plan_desc {
     int32_t tmem_cols;       /* tensor-memory columns allocated per CTA */
     int32_t raster_group;    /* token tiles per raster group: tiles are numbered group by group,
                                 token tile fastest within a group, then weight tile */
+    int32_t swap_ab;         /* 1: weight rows on the MMA's M side (128), tokens on its N side
+                                (block_t); 0: tokens on the M side (128), weight rows on the N
+                                side (block_n) */
+    int32_t reserved0;
     int64_t tiles_m;         /* ceil(M / block_t) */
     int64_t tiles_n;         /* ceil(N / block_n) */
     int64_t k_blocks;        /* ceil(K / block_k) */
@@ -212,9 +219,11 @@ proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W,
 
 /*
  * Synchronise `stream` and read the handle's device status word.  Returns
- * PROJ_ERR_DEVICE_TIMEOUT if a bounded device wait ran out in any earlier run
- * (the word and the split-K counters are then cleared so the handle can be
- * reused), PROJ_ERR_CUDA if the synchronisation failed, else PROJ_OK.
+ * PROJ_ERR_DEVICE_TIMEOUT if a bounded device wait ran out in any earlier run,
+ * PROJ_ERR_CUDA if a run found its launch given less shared memory than its
+ * pipeline needs (an internal planning error; the kernel then did nothing) or
+ * the synchronisation failed, else PROJ_OK.  A non-zero word is cleared,
+ * together with the split-K counters, so the handle can be reused.
  */
 proj_status_t proj_device_status(proj_handle_t h, void *stream);
 
@@ -283,8 +292,9 @@ proj_status_t proj_plan_info(proj_handle_t h, char *buf, size_t len);
  * and no allocating library routine is called.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
- *   - Problems whose plan needs more scratch than 8 MiB (for example M > 32
- *     with N a few thousand, where K is split) return PROJ_ERR_UNSUPPORTED.
+ *   - Problems whose plan needs more scratch than 8 MiB (for example 64
+ *     token rows against 20,000 weight rows, where K is split) return
+ *     PROJ_ERR_UNSUPPORTED.
  *   - Every call shares the array: calls that overlap on the GPU (other
  *     streams, other threads) race and give wrong results.  Each call clears
  *     the array's counters and status word on `stream` before its kernel.

@@ -63,18 +63,28 @@ def plan(M, N, K, layout=0, **dev):
 def check_decomposition(p, M, N, K):
     G, KT = p["grid"], p["k_blocks"]
     tiles = p["tiles_m"] * p["tiles_n"]
-    assert p["tiles_m"] == -(-M // p["block_t"]) and p["tiles_n"] == -(-N // 128)
+    assert p["tiles_m"] == -(-M // p["block_t"]) and p["tiles_n"] == -(-N // p["block_n"])
+    if p["swap_ab"]:
+        assert p["block_n"] == 128 and p["block_t"] % 16 == 0
+    else:
+        assert p["block_t"] == 128 and p["block_n"] % 16 == 0 and 64 <= p["block_n"] <= 256
     assert KT == -(-K // 64)
     assert 1 <= G <= GB300["sm_count"]
     assert p["tiles_dp"] + p["tiles_sk"] == tiles
     if p["tiles_sk"]:
         assert p["tiles_dp"] % G == 0
-    else:  # whole tiles only: the last wave is at least 95 % full (or exactly full)
+    else:  # whole tiles only: the last wave is nearly full (95 % swapped, 80 % token-major)
         waves = -(-tiles // G)
-        assert tiles % G == 0 or 20 * tiles >= 19 * waves * G
+        pct = 95 if p["swap_ab"] else 80
+        assert tiles % G == 0 or 100 * tiles >= pct * waves * G
     assert p["units_sk"] == p["tiles_sk"] * KT
     assert p["smem_bytes"] <= GB300["smem_optin_bytes"] and p["stages"] >= 2
     assert p["block_t"] % 16 == 0 and 16 <= p["block_t"] <= 256
+    b_rows = p["block_t"] if p["swap_ab"] else p["block_n"]
+    assert p["tmem_cols"] >= 2 * b_rows
+    # The launch's shared memory covers the ring (A 128 rows + B rows, 64 K each),
+    # its barriers and 1024-byte alignment slack.
+    assert p["smem_bytes"] == p["stages"] * (128 + b_rows) * 128 + 2048
     cover = np.zeros((tiles, KT), dtype=np.int32)
     by_tile = collections.defaultdict(list)
     coords = {}
@@ -182,21 +192,21 @@ def test_token_tile_choice():
     assert plan(17, 8192, 8192)["block_t"] == 32
     assert plan(64, 28672, 8192)["block_t"] == 64
     assert plan(4096, 8192, 8192)["block_t"] == 256
-    # 256 tokens x 96 weight tiles would leave SMs idle: two 128-token tiles instead.
-    assert plan(256, 12288, 4096, 1)["block_t"] == 128
+    assert plan(256, 12288, 4096, 1)["block_t"] == 128  # token-major: 128-row token tiles
 
 
 def test_scratch_and_stages():
     p = plan(16, 8192, 8192)
-    stage = 128 * 64 * 2 + p["block_t"] * 64 * 2
+    stage = 128 * 64 * 2 + p["block_t"] * 64 * 2  # swapped: B holds the token rows
     assert p["smem_bytes"] == p["stages"] * stage + 2048
     assert p["scratch_bytes"] >= 2 * p["grid"] * p["block_t"] * 128 * 4 + 4 * 4 * p["tiles_sk"]
     assert p["tmem_cols"] >= 2 * p["block_t"] and p["tmem_cols"] in (32, 64, 128, 256, 512)
 
 
 def test_raster_groups():
-    # Prefill: 16 token tiles in groups of 8; within a group the token tile
-    # varies fastest, so the first wave covers 8 token panels x 19 weight panels.
+    # Prefill: 16 token tiles of 256 rows in groups of 8 (2048 token rows);
+    # within a group the token tile varies fastest, so the first wave covers
+    # 8 token panels x 19 weight panels.
     p = plan(4096, 8192, 8192)
     assert p["raster_group"] == 8 and p["tiles_m"] == 16
     first_wave = set()
@@ -207,3 +217,21 @@ def test_raster_groups():
     assert {tm for tm, _ in first_wave} == set(range(8))
     assert len({tn for _, tn in first_wave}) == 19
     assert plan(16, 8192, 8192)["raster_group"] == 1
+
+
+def test_orientation_and_weight_tile_choice():
+    # Fewer than 128 tokens: weight rows on the MMA's M side (swapped).
+    for M in (1, 16, 64, 127):
+        assert plan(M, 8192, 8192)["swap_ab"] == 1
+    # From 128 tokens: tokens on the M side, weight tile sized to fill waves.
+    qkv = plan(256, 12288, 4096, 1)
+    assert qkv["swap_ab"] == 0 and qkv["block_t"] == 128
+    assert qkv["block_n"] == 192 and qkv["tiles_m"] * qkv["tiles_n"] == 128
+    assert qkv["tiles_sk"] == 0  # one whole wave (84 % of the SMs) beats splitting
+    # Many tiles either way (prefill): the swapped 256-token x 128-row tiles.
+    pre = plan(4096, 8192, 8192)
+    assert (pre["swap_ab"], pre["block_t"], pre["block_n"], pre["tiles_sk"]) == (1, 256, 128, 0)
+    # [K,N] weights load in 64-row boxes: the weight tile is a multiple of 64.
+    for N in (1000, 3000, 9000):  # few enough weight rows that swapped tiles leave SMs idle
+        p = plan(300, N, 1024, 1)
+        assert p["swap_ab"] == 0 and p["block_n"] % 64 == 0

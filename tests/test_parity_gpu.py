@@ -46,6 +46,43 @@ def test_forced_token_tiles(block_t, monkeypatch):
     gu.assert_within_tol(gu.y_to_f64(Y), r, f"block_t={block_t}")
 
 
+@pytest.mark.parametrize("layout,block_n", [(synth.W_NK, 64), (synth.W_NK, 80), (synth.W_NK, 176),
+                                            (synth.W_NK, 256), (synth.W_KN, 64), (synth.W_KN, 192),
+                                            (synth.W_KN, 256)])
+def test_forced_weight_tiles(layout, block_n, monkeypatch):
+    # Token rows on the MMA's M side with every kind of weight tile: widths
+    # that are and are not multiples of 64, ragged last tiles, both layouts,
+    # data-parallel and split plans.
+    monkeypatch.setenv("PROJ_FORCE_BLOCK_N", str(block_n))
+    w = _workload(300, 1000, 2056, layout, True, "bf16", seed=22)
+    inp = synth.make_inputs(w)
+    proj, Y, _ = gu.run(w, inp)
+    assert proj.plan["swap_ab"] == 0 and proj.plan["block_n"] == block_n
+    r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
+    gu.assert_within_tol(gu.y_to_f64(Y), r, f"block_n={block_n}")
+
+
+@pytest.mark.parametrize("env", [{"PROJ_FORCE_BLOCK_N": "192", "PROJ_FORCE_STAGES": "3"},
+                                 {"PROJ_FORCE_BLOCK_N": "176", "PROJ_FORCE_STAGES": "2"},
+                                 {"PROJ_FORCE_BLOCK_T": "64", "PROJ_FORCE_STAGES": "2"}])
+def test_forced_pipeline_depth(env, monkeypatch):
+    # A shallower ring than planned, in both orientations: the launch's shared
+    # memory must follow the B operand of the orientation in use.
+    import dense_linear_projection_gb300 as dlp
+    for k, v in env.items():
+        monkeypatch.setenv(k, v)
+    layout = synth.W_KN if env.get("PROJ_FORCE_BLOCK_N") == "192" else synth.W_NK
+    w = _workload(256, 1536, 8192, layout, True, "bf16", seed=23)  # planned depth 4-6
+    inp = synth.make_inputs(w)
+    proj, Y, _ = gu.run(w, inp)
+    assert proj.plan["stages"] == int(env["PROJ_FORCE_STAGES"])
+    import torch
+    torch.cuda.synchronize()
+    assert proj.status() == dlp.PROJ_OK
+    r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
+    gu.assert_within_tol(gu.y_to_f64(Y), r, str(env))
+
+
 def _workload(M, N, K, layout, bias, yd, seed=5):
     return synth.Workload("t", M, N, K, layout, bias, yd, seed)
 

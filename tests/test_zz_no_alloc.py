@@ -48,10 +48,11 @@ def test_noalloc_matches_proj_run_twice(M, N, K, layout, bias, yd):
 def test_noalloc_refuses_plans_beyond_its_scratch():
     import torch
     import dense_linear_projection_gb300 as dlp
-    M, N, K = 256, 12288, 4096  # split tiles of 128 tokens: more scratch than the array
+    M, N, K = 64, 20000, 512  # split tiles of 64 tokens: about 9.5 MiB of scratch
+    assert dlp.proj_plan_compute(M, N, K)["scratch_bytes"] > 8 << 20
     X = torch.zeros((M, K), dtype=torch.bfloat16, device="cuda")
-    W = torch.zeros((K, N), dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros((N, K), dtype=torch.bfloat16, device="cuda")
     Y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(dlp.ProjError) as e:
-        dlp.proj_run_noalloc(M, N, K, dlp.PROJ_W_KN, dlp.PROJ_BF16, X, W, None, Y)
+        dlp.proj_run_noalloc(M, N, K, dlp.PROJ_W_NK, dlp.PROJ_BF16, X, W, None, Y)
     assert e.value.status == dlp.PROJ_ERR_UNSUPPORTED
