@@ -241,10 +241,20 @@ __device__ __forceinline__ void store_y(const KernelParams &p, size_t off, float
         static_cast<__nv_bfloat16 *>(p.Y)[off] = __float2bfloat16_rn(y);
 }
 
-// Release/acquire fence at GPU scope (one lane publishes or observes the
-// partial sums its whole warp wrote, ordered by __syncwarp around it).
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+// Acquire-release add at GPU scope: one lane publishes the partial sums its
+// whole warp wrote (ordered before it by __syncwarp) and observes the other
+// contributors' partials.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *ptr, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(ptr), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void store_relaxed_gpu(uint32_t *ptr, uint32_t v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
 // The 16 columns [ch·16, ch·16+16) of one partial-sum row: four 16-byte loads
@@ -600,13 +610,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int last = 0;
                 uint32_t *ctr = p.counters + static_cast<size_t>(ts) * 4 + q;
                 if (lane == 0) {
-                    fence_acq_rel_gpu();
-                    const uint32_t old = atomicAdd(ctr, 1u);
+                    // One acquire-release add: releases this warp's partials
+                    // (ordered before it by the __syncwarp above) and, for the
+                    // last contributor, acquires everyone else's.
+                    const uint32_t old = atom_add_acq_rel_gpu(ctr, 1u);
                     last = (old == static_cast<uint32_t>(nseg - 1)) ? 1 : 0;
-                    if (last) {
-                        atomicExch(ctr, 0u);  // fresh for the next run
-                        fence_acq_rel_gpu();  // acquire the other contributors' partials
-                    }
+                    if (last) store_relaxed_gpu(ctr, 0u);  // fresh for the next run
                 }
                 last = __shfl_sync(0xFFFFFFFFu, last, 0);
                 __syncwarp();
