@@ -99,10 +99,70 @@ uint32_t idesc_of(const proj_plan_desc_t &plan, int w_layout) {
 }
 
 // Bytes of split-K partial tiles in the scratch (the rest is counters and
-// the status word).
+// the status word).  Cluster-split plans reduce in shared memory: none.
 int64_t partial_bytes_of(const proj_plan_desc_t &plan) {
     const int64_t b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
-    return plan.tiles_sk > 0 ? int64_t(2) * plan.grid * kBlockA * b_rows * 4 : 0;
+    return plan.tiles_sk > 0 && plan.cluster_split < 2 ? int64_t(2) * plan.grid * kBlockA * b_rows * 4 : 0;
+}
+
+// The kernel may use up to the device's opt-in shared memory.  The attribute
+// belongs to the kernel, not to a handle: every launch fits under it.
+bool set_kernel_smem_limit(int smem_optin) {
+    if (cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem_optin) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
+// Launch configuration of a tensor-core plan: the cluster shape of a
+// cluster-split plan and, unless off, programmatic dependent launch.
+struct TcLaunch {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[2];
+    TcLaunch(const proj_plan_desc_t &plan, cudaStream_t s, bool pdl) {
+        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
+        cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
+        cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
+        cfg.stream = s;
+        unsigned n = 0;
+        if (plan.cluster_split > 1) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = static_cast<unsigned>(plan.cluster_split);
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = n;
+    }
+};
+
+// Plan for this device.  A cluster split is kept only if every tile's cluster
+// can be resident at once (GPCs hold whole clusters, so not every SM count
+// divides into clusters); otherwise the split size is lowered, down to the
+// global-scratch split-K plans.  Needs the kernel's shared-memory limit set.
+proj_status_t plan_for_device(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
+                              proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t &dd,
+                              PlanOptions opt, proj_plan_desc_t *plan) {
+    while (true) {
+        proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, opt, plan);
+        if (st != PROJ_OK || plan->cluster_split < 2) return st;
+        TcLaunch l(*plan, nullptr, false);
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, dev::proj_tc_kernel, &l.cfg) == cudaSuccess &&
+            static_cast<int64_t>(clusters) >= plan->tiles_sk)
+            return PROJ_OK;
+        cudaGetLastError();
+        opt.max_cluster = plan->cluster_split - 1;
+        if (opt.max_cluster < 2) opt.max_cluster = 0;
+    }
 }
 
 // Y rows start on 16-byte boundaries: vector stores of 16 outputs are safe.
@@ -155,14 +215,34 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     if (prop.major != 10 || prop.minor != 3) return PROJ_ERR_UNSUPPORTED;  // built for sm_103a
 
     proj_device_desc_t dd{prop.multiProcessorCount, static_cast<int32_t>(prop.sharedMemPerBlockOptin)};
+    if (!set_kernel_smem_limit(static_cast<int>(prop.sharedMemPerBlockOptin))) return PROJ_ERR_CUDA;
     proj_plan_desc_t plan;
-    int32_t force_bt = 0, force_bn = 0;  // tuning only
-    if (const char *e = std::getenv("PROJ_FORCE_BLOCK_T")) force_bt = std::atoi(e);
-    if (const char *e = std::getenv("PROJ_FORCE_BLOCK_N")) force_bn = std::atoi(e);
-    proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, force_bt, force_bn, &plan);
+    PlanOptions opt;  // environment overrides: tuning only
+    if (const char *e = std::getenv("PROJ_FORCE_BLOCK_T")) opt.force_block_t = std::atoi(e);
+    if (const char *e = std::getenv("PROJ_FORCE_BLOCK_N")) opt.force_block_n = std::atoi(e);
+    if (const char *e = std::getenv("PROJ_MAX_CLUSTER")) {
+        const int c = std::atoi(e);
+        opt.max_cluster = c >= 2 && c <= kMaxClusterSplit ? c : 0;
+    }
+    if (const char *e = std::getenv("PROJ_CLUSTER_FILL_PCT")) {
+        const int f = std::atoi(e);
+        if (f >= 1 && f <= 100) opt.cluster_fill_pct = f;
+    }
+    proj_status_t st = plan_for_device(M, N, K, w_layout, y_dtype, has_bias, dd, opt, &plan);
     if (st != PROJ_OK) return st;
+    if (const char *e = std::getenv("PROJ_FORCE_GRID")) {  // tuning only: fewer CTAs, all-split plans
+        const int g = std::atoi(e);
+        if (g >= 1 && g < plan.grid && plan.kernel == PROJ_KERNEL_TC && plan.tiles_dp == 0 &&
+            plan.cluster_split < 2) {
+            plan.grid = g;
+            const int64_t b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
+            const int64_t counter_bytes = ((plan.tiles_sk * 4 * 4 + 255) / 256) * 256;
+            plan.scratch_bytes = int64_t(2) * g * kBlockA * b_rows * 4 + counter_bytes + 256;
+        }
+    }
     if (const char *e = std::getenv("PROJ_FORCE_WHOLE_TILES")) {  // tuning only
-        if (std::atoi(e) == 1 && plan.kernel == PROJ_KERNEL_TC && plan.tiles_sk > 0) {
+        if (std::atoi(e) == 1 && plan.kernel == PROJ_KERNEL_TC && plan.tiles_sk > 0 &&
+            plan.cluster_split < 2) {
             plan.tiles_dp += plan.tiles_sk;
             plan.tiles_sk = 0;
             plan.units_sk = 0;
@@ -216,10 +296,6 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         // Counters and the status word start at zero; partials need no clearing.
         if (cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(plan.scratch_bytes - partial_bytes),
                             as_stream(stream)) != cudaSuccess ||
-            // The attribute belongs to the kernel, not to this handle: set it
-            // to the device maximum so every handle's launch fits under it.
-            cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(prop.sharedMemPerBlockOptin)) != cudaSuccess ||
             cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
             cudaGetLastError();
             cudaFree(h->scratch);
@@ -274,17 +350,8 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
     kp.y_vec = y_vec_of(Y, h->N, h->y_dtype);
     kp.trace = h->trace;
     kp.w_prefetch = h->overlap == PROJ_OVERLAP_WEIGHTS;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(plan.threads));
-    cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = h->overlap == PROJ_OVERLAP_NONE ? 0 : 1;
-    if (cudaLaunchKernelEx(&cfg, dev::proj_tc_kernel, kp, h->map_w, h->map_x) != cudaSuccess) {
+    TcLaunch l(plan, s, h->overlap != PROJ_OVERLAP_NONE);
+    if (cudaLaunchKernelEx(&l.cfg, dev::proj_tc_kernel, kp, h->map_w, h->map_x) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }
@@ -328,7 +395,8 @@ proj_status_t proj_device_status(proj_handle_t h, void *stream) {
     if (cudaMemcpy(&word, h->params.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
         return PROJ_ERR_CUDA;
     if (word == 0) return PROJ_OK;
-    const proj_status_t what = (word & kErrSmemTooSmall) ? PROJ_ERR_CUDA : PROJ_ERR_DEVICE_TIMEOUT;
+    const proj_status_t what =
+        (word & (kErrSmemTooSmall | kErrLaunchShape)) ? PROJ_ERR_CUDA : PROJ_ERR_DEVICE_TIMEOUT;
     // Clear the word and the split-K counters (a run that gave up may have
     // left some mid-count) so the handle is usable again.
     const proj_plan_desc_t &plan = h->plan;
@@ -474,8 +542,9 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     if (major != 10 || minor != 3) return PROJ_ERR_UNSUPPORTED;
 
     proj_device_desc_t dd{sms, smem};
+    if (!set_kernel_smem_limit(smem)) return PROJ_ERR_CUDA;
     proj_plan_desc_t plan;
-    proj_status_t st = proj_plan_compute(M, N, K, w_layout, y_dtype, bias != nullptr, &dd, &plan);
+    proj_status_t st = plan_for_device(M, N, K, w_layout, y_dtype, bias != nullptr, dd, PlanOptions{}, &plan);
     if (st != PROJ_OK) return st;
     if (plan.kernel == PROJ_KERNEL_FILL) {
         dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(M, N, static_cast<const uint16_t *>(bias),
@@ -523,11 +592,10 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);
     kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
     kp.trace = nullptr;
-    if (cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem) != cudaSuccess) {
+    TcLaunch l(plan, s, false);
+    if (cudaLaunchKernelEx(&l.cfg, dev::proj_tc_kernel, kp, map_w, map_x) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }
-    dev::proj_tc_kernel<<<plan.grid, plan.threads, plan.smem_bytes, s>>>(kp, map_w, map_x);
-    return check_launch();
+    return PROJ_OK;
 }

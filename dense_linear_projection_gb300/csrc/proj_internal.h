@@ -20,6 +20,8 @@ constexpr int32_t kMmaK = 16;          // K per tcgen05.mma (kind::f16)
 constexpr int32_t kMaxTokenTile = 256; // tcgen05 MMA N limit for cta_group::1
 constexpr int32_t kMaxStages = 12;
 constexpr int32_t kInflightTarget = 160 * 1024;  // stage bytes per SM when streaming W from HBM
+constexpr int32_t kMaxClusterSplit = 8;           // portable thread-block cluster size
+constexpr int32_t kClusterFillPct = 60;           // SMs a cluster split must keep busy (%)
 constexpr int32_t kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int32_t kEpilogueThreads = 128;
 constexpr int32_t kSmemReserve = 2048; // 1024-byte alignment slack + barriers
@@ -49,15 +51,26 @@ constexpr int kErrWaitEpilogue = 1 << 2;
 constexpr int kErrWaitDrain = 1 << 3;
 constexpr int kErrSelfTest = 1 << 4;
 constexpr int kErrSmemTooSmall = 1 << 5;  // launch gave less shared memory than the ring needs
+constexpr int kErrLaunchShape = 1 << 6;   // cluster shape of the launch differs from the plan's
 
 int32_t token_tile_for(int64_t M);
-// The planner behind proj_plan_compute.  Tuning overrides (proj_create takes
-// them from PROJ_FORCE_BLOCK_T / PROJ_FORCE_BLOCK_N): force_block_t > 0 forces
-// the swapped orientation with that token tile; force_block_n > 0 forces the
-// token-rows-on-M orientation with that weight tile.
+// Planner options.  force_block_t > 0 forces the swapped orientation with
+// that token tile; force_block_n > 0 forces the token-rows-on-M orientation
+// with that weight tile (both tuning overrides, from PROJ_FORCE_BLOCK_T /
+// PROJ_FORCE_BLOCK_N in proj_create).  max_cluster bounds the cluster-split
+// size (0 disables it; proj_create lowers it when the clusters would not all
+// be resident at once); a cluster split must keep cluster_fill_pct percent of
+// the SMs busy.
+struct PlanOptions {
+    int32_t force_block_t = 0;
+    int32_t force_block_n = 0;
+    int32_t max_cluster = kMaxClusterSplit;
+    int32_t cluster_fill_pct = kClusterFillPct;
+};
+// The planner behind proj_plan_compute (which uses the default options).
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
                            proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t *dev,
-                           int32_t force_block_t, int32_t force_block_n, proj_plan_desc_t *out);
+                           const PlanOptions &opt, proj_plan_desc_t *out);
 // Shared-memory bytes of one pipeline stage: A (128 rows x 64 K) plus B
 // (b_rows x 64 K), bf16.
 int32_t stage_bytes_for(int32_t b_rows);
@@ -81,6 +94,7 @@ struct KernelParams {
     int64_t units_sk;      // split-K units after the whole tiles
     int32_t sk_pair;       // every CTA owns >= k_blocks units: a split tile has exactly 2 contributors
     int32_t sk_dense;      // units_sk >= grid: no CTA has an empty unit range
+    int32_t cluster_split; // S >= 2: tile c / S split over the S CTAs of a cluster (DSMEM reduction)
     int32_t stages;
     int32_t stage_bytes;
     int32_t tmem_cols;
@@ -172,6 +186,16 @@ struct WorkIter {
 
     PROJ_HD void init(const KernelParams &p, int32_t c) {
         cta = c;
+        if (p.cluster_split > 1) {
+            // One segment: rank c % S of tile c / S, an integer share of K.
+            const int32_t S = p.cluster_split;
+            const int32_t r = c % S;
+            dp_next = -1;
+            u = static_cast<int64_t>(c / S) * p.k_blocks + (static_cast<int64_t>(r) * p.k_blocks) / S;
+            u_end = static_cast<int64_t>(c / S) * p.k_blocks + (static_cast<int64_t>(r + 1) * p.k_blocks) / S;
+            first_sk_tile = c / S;
+            return;
+        }
         dp_next = c;
         u = unit_begin(c, p.units_sk, p.grid);
         u_end = unit_begin(c + 1, p.units_sk, p.grid);
@@ -181,6 +205,16 @@ struct WorkIter {
     // Whole tiles first (c, c+G, ... below tiles_dp), then this CTA's split-K
     // units, cut at tile boundaries.
     PROJ_HD bool next(const KernelParams &p, Segment &s) {
+        if (p.cluster_split > 1) {
+            if (u >= u_end) return false;
+            s.tile = first_sk_tile;
+            s.kb0 = static_cast<int32_t>(u - static_cast<int64_t>(first_sk_tile) * p.k_blocks);
+            s.kb1 = static_cast<int32_t>(u_end - static_cast<int64_t>(first_sk_tile) * p.k_blocks);
+            s.split = true;
+            s.slot = -1;
+            u = u_end;
+            return true;
+        }
         if (dp_next < p.tiles_dp) {
             s.tile = dp_next;
             s.kb0 = 0;
@@ -224,6 +258,8 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.units_sk = plan.units_sk;
     kp.sk_pair = plan.grid > 0 && plan.units_sk / plan.grid >= plan.k_blocks;
     kp.sk_dense = plan.units_sk >= plan.grid;
+    kp.cluster_split = plan.cluster_split;
+    if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;
     kp.stages = plan.stages;
     kp.stage_bytes = stage_bytes_for(kp.b_rows);
     kp.tmem_cols = plan.tmem_cols;

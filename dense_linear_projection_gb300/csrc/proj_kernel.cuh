@@ -28,6 +28,11 @@
 // counter returns to zero inside the run (section "Why a last-block scheme was
 // more complicated than it sounded": every replay needs a fresh counter).
 //
+// Cluster split (decode shapes with fewer narrow tiles than SMs): each tile's
+// K range is shared by the S CTAs of one thread-block cluster.  The partial
+// sums meet in distributed shared memory and are added in rank (= K) order by
+// one rank per 32-row quarter; no scratch, no counters.
+//
 // Every mbarrier wait is bounded in time; a wait that runs out records a bit in
 // the device status word, raises a CTA-wide abort flag, drains in-flight copies
 // and MMAs (again bounded), frees tensor memory and returns.
@@ -84,15 +89,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// The same test with acquire at cluster scope: the arrivals came from other
+// CTAs of the cluster, whose shared-memory writes must then be visible.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Bounded wait for the phase of `bar` with the given parity to complete.
 // Returns false (and raises the CTA abort flag, recording `code` in the status
 // word) if `limit_ns` passes, or false at once if another role aborted.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                            int *status, int code, int64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto test = [&]() {
+        return kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (test()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (test()) return true;
         if (*abort_flag) return false;
         if (static_cast<int64_t>(globaltimer_ns() - t0) > limit_ns) {
             *abort_flag = 1;
@@ -100,6 +123,61 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
             return false;
         }
     }
+}
+
+// Thread-block clusters (cluster split): this CTA's rank, the address of the
+// same shared-memory location in another CTA of the cluster, arrivals and
+// loads through that window, and the cluster-wide barrier.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t c;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(c));
+    return c;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+    return d;
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_f4(uint32_t saddr, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -274,6 +352,7 @@ struct SmemCtl {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t ready[4];  // cluster split: the other ranks' partials of a quarter are in place
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -301,7 +380,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (threadIdx.x == 0) atomicOr(p.status, kErrSmemTooSmall);
             return;
         }
+        // A cluster-split plan needs clusters of exactly its size (every CTA
+        // of the launch sees the same cluster size, so all leave together,
+        // before any cluster barrier).
+        if (p.cluster_split > 1 && cluster_nctarank() != static_cast<uint32_t>(p.cluster_split)) {
+            if (threadIdx.x == 0) atomicOr(p.status, kErrLaunchShape);
+            return;
+        }
     }
+    // The CTA's index in the plan: in a cluster split, cluster c's rank r is
+    // CTA c·S + r (tile c, K range r), taken from the hardware's own numbering.
+    const int32_t cta = p.cluster_split > 1
+                            ? static_cast<int32_t>(cluster_id_x() * static_cast<uint32_t>(p.cluster_split) +
+                                                   cluster_ctarank())
+                            : static_cast<int32_t>(blockIdx.x);
     uint8_t *smem = smem_raw + (base_addr - raw_addr);
     SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + p.stages * p.stage_bytes);
     volatile int *abort_flag = &ctl->abort_flag;
@@ -325,6 +417,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl->acc_empty[b]), kEpilogueThreads / 32);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
+        if (p.cluster_split > 1)
+            for (int qq = 0; qq < 4; ++qq)
+                mbar_init(smem_u32(&ctl->ready[qq]), static_cast<uint32_t>(p.cluster_split - 1));
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -339,6 +434,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // Cluster split: announce that this CTA's barriers exist.  A thread waits
+    // for the whole cluster's announcement (cluster_waited) before its first
+    // access to another CTA's shared memory, and at the latest at teardown.
+    const bool clustered = p.cluster_split > 1;
+    bool cluster_waited = false;
+    if (clustered) cluster_arrive();
     const uint32_t tmem_base = ctl->tmem_base;
     const uint32_t half_cols = static_cast<uint32_t>(p.tmem_cols / 2);
     if (threadIdx.x == 0) {
@@ -379,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t pre = 0;
             if (p.w_prefetch) {
                 WorkIter it;
-                it.init(p, blockIdx.x);
+                it.init(p, cta);
                 Segment s;
                 while (pre < stages && it.next(p, s)) {
                     int32_t tm, tn;
@@ -398,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int32_t stage = 0;
             uint32_t phase = 0;
             WorkIter it;
-            it.init(p, blockIdx.x);
+            it.init(p, cta);
             Segment s;
             bool ok = true;
             while (ok && it.next(p, s)) {
@@ -437,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             int32_t seg_idx = 0;
             WorkIter it;
-            it.init(p, blockIdx.x);
+            it.init(p, cta);
             Segment s;
             bool ok = true;
             while (ok && it.next(p, s)) {
@@ -492,9 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t U = p.units_sk;
         griddep_wait();  // partials, counters and Y may be in use by the preceding kernel
         if (warp == 2 && lane == 0) trace_stamp(p, kTraceEpiDepWait);
+        if (clustered) {
+            cluster_wait();  // every CTA of the cluster has initialised its barriers
+            cluster_waited = true;
+        }
         int32_t seg_idx = 0;
         WorkIter it;
-        it.init(p, blockIdx.x);
+        it.init(p, cta);
         Segment s;
         while (it.next(p, s)) {
             const int32_t buf = seg_idx & 1;
@@ -575,6 +680,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_chunk(ch, v);
                 }
                 release_accumulator();
+            } else if (clustered) {
+                // Cluster split: the S CTAs of this cluster hold the tile's
+                // partial sums over consecutive K ranges (rank order = K
+                // order).  Every rank leaves its rows of quarter q in its own
+                // shared memory (the drained ring); rank q mod S (S <= 4) or q
+                // (S = 8) waits for the others' signals and adds all ranks in
+                // ascending order, so every run gives the same bits.
+                const uint32_t S = static_cast<uint32_t>(p.cluster_split);
+                const uint32_t rank = static_cast<uint32_t>(cta) % S;  // = %cluster_ctarank
+                const uint32_t reducer = S <= 4 ? static_cast<uint32_t>(q) % S : static_cast<uint32_t>(q);
+                // [16-column chunk][float4 of the chunk][lane]: 16 consecutive
+                // bytes per lane, a warp's accesses contiguous.
+                const uint32_t region = base_addr + static_cast<uint32_t>(q) * 32u *
+                                                        static_cast<uint32_t>(p.b_rows) * 4u;
+                const uint32_t lane_off16 = static_cast<uint32_t>(lane) * 16u;
+                for (int32_t ch = 0; ch < nchunks; ++ch) {
+                    float v[16];
+                    tmem_load16(tbase + ch * 16, v);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_shared_f4(region + static_cast<uint32_t>(ch * 4 + i) * 512u + lane_off16,
+                                     make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                }
+                release_accumulator();  // (its __syncwarp also orders the stores above)
+                if (rank != reducer) {
+                    if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&ctl->ready[q]), reducer));
+                } else if (wait_phase<true>(smem_u32(&ctl->ready[q]), 0u, abort_flag, p.status,
+                                            kErrWaitEpilogue, p.wait_limit_ns)) {
+                    if (warp == 2 && lane == 0) ++reductions;
+                    for (int32_t ch = 0; ch < nchunks; ++ch) {
+                        float acc[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                        // One rank at a time: the epilogue has no registers
+                        // to spare for more loads in flight.
+                        for (uint32_t rk = 0; rk < S; ++rk) {
+                            const uint32_t src = map_to_rank(region, rk) + lane_off16;
+                            float4 o[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                o[i] = ld_cluster_f4(src + static_cast<uint32_t>(ch * 4 + i) * 512u);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                acc[4 * i] += o[i].x;
+                                acc[4 * i + 1] += o[i].y;
+                                acc[4 * i + 2] += o[i].z;
+                                acc[4 * i + 3] += o[i].w;
+                            }
+                        }
+                        store_chunk(ch, acc);
+                    }
+                }
             } else {
                 // Split tile.  This lane's row of fp32 partial sums goes to
                 // scratch, laid out [slot][128 rows][b_rows] (16 columns =
@@ -626,8 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // memory) + the other's partial.  Two-operand addition is
                     // commutative, so the bits do not depend on who is last.
                     const int32_t other_slot =
-                        s.kb0 == 0 ? 2 * (static_cast<int32_t>(blockIdx.x) + 1)
-                                   : 2 * (static_cast<int32_t>(blockIdx.x) - 1) + 1;
+                        s.kb0 == 0 ? 2 * (cta + 1) : 2 * (cta - 1) + 1;
                     const float *other = p.partials + (static_cast<size_t>(other_slot) * kBlockA + r) * p.b_rows;
                     for (int32_t ch0 = 0; ch0 < nchunks; ch0 += 4) {
                         float4 o[4][4];
@@ -723,6 +879,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_phase(smem_u32(&ctl->drain), 0, &never, p.status, kErrWaitDrain, p.wait_limit_ns);
         }
         __syncthreads();
+    }
+    if (clustered) {
+        // No CTA leaves while another may still read its shared memory or
+        // arrive on its barriers.  Every role reaches this point: all of its
+        // waits are bounded.
+        if (!cluster_waited) cluster_wait();
+        cluster_arrive();
+        cluster_wait();
     }
     if (warp == 1) {
         tc_fence_after_sync();

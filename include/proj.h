@@ -111,6 +111,11 @@ typedef struct proj_device_desc {
  * section "My first useful win: split up the sum"; CTA c takes units
  * [⌊c·U/G⌋, ⌊(c+1)·U/G⌋), the integer partition of section "Why the later
  * TMA/WGMMA kernel was a new experiment" that splits 128 tiles 42/43/43).
+ * Cluster split instead (cluster_split = S ≥ 2): when fewer narrow swapped
+ * tiles than SMs exist and S CTAs per tile keep at least 60 % of the SMs busy,
+ * each tile gets its own cluster of S CTAs, grid = tiles_sk · S, and the
+ * partial sums meet in distributed shared memory; no partial-sum scratch and
+ * no counters.
  */
 typedef struct proj_plan_desc {
     int32_t kernel;          /* proj_kernel_t */
@@ -127,7 +132,10 @@ typedef struct proj_plan_desc {
     int32_t swap_ab;         /* 1: weight rows on the MMA's M side (128), tokens on its N side
                                 (block_t); 0: tokens on the M side (128), weight rows on the N
                                 side (block_n) */
-    int32_t reserved0;
+    int32_t cluster_split;   /* 0, or S >= 2: every tile is split along K over the S CTAs of one
+                                thread-block cluster (CTA c: tile c / S, rank c % S, k-blocks
+                                [⌊r·k_blocks/S⌋, ⌊(r+1)·k_blocks/S⌋)), and the partial sums are
+                                added through distributed shared memory in rank order */
     int64_t tiles_m;         /* ceil(M / block_t) */
     int64_t tiles_n;         /* ceil(N / block_n) */
     int64_t k_blocks;        /* ceil(K / block_k) */
@@ -142,6 +150,9 @@ typedef struct proj_plan_desc {
  * Plan a problem without touching a GPU (pure host code).
  * Returns PROJ_ERR_INVALID_ARG for negative sizes, a bad layout, or a NULL
  * dev/out; PROJ_ERR_UNSUPPORTED if the device cannot hold two pipeline stages.
+ * This is the plan proj_create uses, except that proj_create lowers
+ * cluster_split (down to a plain split-K plan) when the device cannot keep
+ * every tile's cluster resident at once.
  */
 proj_status_t proj_plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
                                 proj_dtype_t y_dtype, int has_bias,
@@ -155,7 +166,7 @@ typedef struct proj_segment {
     int32_t tile_n;          /* weight-row tile */
     int32_t k_block_begin;
     int32_t k_block_end;
-    int32_t slot;            /* partial-sum slot when split, else -1 */
+    int32_t slot;            /* partial-sum slot when split, else -1 (also -1 in cluster splits) */
     int32_t split;           /* 1 if other CTAs own the rest of this tile's K range */
     int32_t reserved;
 } proj_segment_t;
@@ -174,7 +185,9 @@ proj_status_t proj_plan_segments(const proj_plan_desc_t *plan, int32_t cta, proj
  * The order in which the partial sums of split tile `split_tile`
  * (0 ≤ split_tile < tiles_sk; tile index tiles_dp + split_tile) are added:
  * contributing CTAs in ascending order with their partial-sum slots.  Writes
- * min(cap, total) pairs and the total to *count.
+ * min(cap, total) pairs and the total to *count.  For a cluster split the
+ * CTAs are the tile's cluster ranks, split_tile·S .. split_tile·S + S − 1,
+ * each with slot −1.
  */
 proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t split_tile,
                                         int32_t *ctas, int32_t *slots, int64_t cap,
@@ -221,8 +234,9 @@ proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W,
  * Synchronise `stream` and read the handle's device status word.  Returns
  * PROJ_ERR_DEVICE_TIMEOUT if a bounded device wait ran out in any earlier run,
  * PROJ_ERR_CUDA if a run found its launch given less shared memory than its
- * pipeline needs (an internal planning error; the kernel then did nothing) or
- * the synchronisation failed, else PROJ_OK.  A non-zero word is cleared,
+ * pipeline needs or clusters of another size than its plan's (internal
+ * launch errors; the kernel then did nothing) or the synchronisation failed,
+ * else PROJ_OK.  A non-zero word is cleared,
  * together with the split-K counters, so the handle can be reused.
  */
 proj_status_t proj_device_status(proj_handle_t h, void *stream);

@@ -60,7 +60,7 @@ def plan(M, N, K, layout=0, **dev):
     return dlp.proj_plan_compute(M, N, K, layout, **(dev or GB300))
 
 
-def check_decomposition(p, M, N, K):
+def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     G, KT = p["grid"], p["k_blocks"]
     tiles = p["tiles_m"] * p["tiles_n"]
     assert p["tiles_m"] == -(-M // p["block_t"]) and p["tiles_n"] == -(-N // p["block_n"])
@@ -71,6 +71,14 @@ def check_decomposition(p, M, N, K):
     assert KT == -(-K // 64)
     assert 1 <= G <= GB300["sm_count"]
     assert p["tiles_dp"] + p["tiles_sk"] == tiles
+    S = p["cluster_split"]
+    if S:
+        # Cluster split: every tile its own cluster of S CTAs, at least 60 %
+        # of the SMs busy, narrow swapped tiles, partials in shared memory.
+        assert 2 <= S <= 8 and S <= KT and p["swap_ab"] == 1 and p["block_t"] <= 64
+        assert p["tiles_dp"] == 0 and G == tiles * S and 10 * G >= 6 * sms
+        assert p["scratch_bytes"] == 256
+        assert p["stages"] * (128 + p["block_t"]) * 128 >= 128 * p["block_t"] * 4
     if p["tiles_sk"]:
         assert p["tiles_dp"] % G == 0
     else:  # whole tiles only: the last wave is nearly full (95 % swapped, 80 % token-major)
@@ -95,7 +103,10 @@ def check_decomposition(p, M, N, K):
             assert coords.setdefault(tile, (tm, tn)) == (tm, tn)
             cover[tile, kb0:kb1] += 1
             by_tile[tile].append((c, slot, split, kb0, kb1))
-            if split:
+            if split and S:
+                r = c % S
+                assert (tile, kb0, kb1, slot) == (c // S, r * KT // S, (r + 1) * KT // S, -1)
+            elif split:
                 assert 0 <= slot < 2 * G and slot not in slots
                 slots.add(slot)
             else:
@@ -131,6 +142,36 @@ def test_plans_of_the_workloads(M, N, K, layout):
     check_decomposition(p, M, N, K)
 
 
+def test_cluster_split_plans():
+    # Decode shapes with fewer 128-row weight tiles than SMs: 64 tiles in
+    # clusters of 2 (128 CTAs), 16 tiles in clusters of 8 (128 CTAs).
+    for (N, S) in ((8192, 2), (2048, 8)):
+        p = plan(16, N, 8192)
+        assert (p["cluster_split"], p["grid"], p["tiles_sk"], p["tiles_dp"]) == (S, 128, 128 // S, 0)
+        assert dlp.proj_plan_reduction_order(p, 3) == [(3 * S + r, -1) for r in range(S)]
+    # Enough tiles for every SM (the 28672-row FFN weight): no clusters.
+    assert plan(16, 28672, 8192)["cluster_split"] == 0
+    # 77 or more tiles leave no room for two CTAs each: stream-K; 76 tiles
+    # take clusters of 2 on every SM; 45 tiles clusters of 3 (135 SMs).
+    p = plan(16, 100 * 128, 8192)
+    assert p["cluster_split"] == 0 and p["tiles_sk"] == 100
+    assert plan(16, 77 * 128, 8192)["cluster_split"] == 0
+    assert plan(16, 76 * 128, 8192)["cluster_split"] == 2
+    assert plan(16, 45 * 128, 8192)["cluster_split"] == 3
+    # Below 60 % of the SMs (8 SMs, 3 tiles: clusters of 2 on 6 SMs = 75 %,
+    # 5 tiles of one CTA each on 5 SMs: no split possible).
+    assert plan(16, 3 * 128, 8192, sm_count=8, smem_optin_bytes=232448)["cluster_split"] == 2
+    assert plan(16, 5 * 128, 8192, sm_count=8, smem_optin_bytes=232448)["cluster_split"] == 0
+    # S is capped by the k-blocks there are to share (5 SMs, 1 tile, 4 k-blocks).
+    p = plan(16, 128, 256, sm_count=5, smem_optin_bytes=232448)
+    assert p["k_blocks"] == 4 and p["cluster_split"] == 4 and p["grid"] == 4
+    # Several token tiles (100 tokens in two 64-row tiles) are clustered too.
+    p = plan(100, 1024, 8192)
+    assert (p["block_t"], p["tiles_m"], p["cluster_split"], p["grid"]) == (64, 2, 8, 128)
+    # Token-major tiles are never cluster-split.
+    assert plan(256, 2048, 8192)["cluster_split"] == 0
+
+
 def test_plans_of_many_shapes():
     rng = np.random.default_rng(0)
     shapes = [(1, 1, 8), (1, 128, 64), (17, 300, 72), (3, 130, 72), (257, 300, 256),
@@ -140,9 +181,8 @@ def test_plans_of_many_shapes():
     for (M, N, K) in shapes:
         for sm in (152, 148, 7, 1):
             p = plan(M, N, K, sm_count=sm, smem_optin_bytes=232448)
-            GB300_sm = sm
-            assert p["grid"] <= GB300_sm
-            check_decomposition(p, M, N, K)
+            assert p["grid"] <= sm
+            check_decomposition(p, M, N, K, sms=sm)
 
 
 def test_page_partition_42_43_43():
@@ -196,7 +236,8 @@ def test_token_tile_choice():
 
 
 def test_scratch_and_stages():
-    p = plan(16, 8192, 8192)
+    p = plan(16, 28672, 8192)
+    assert p["tiles_sk"] > 0 and p["cluster_split"] == 0
     stage = 128 * 64 * 2 + p["block_t"] * 64 * 2  # swapped: B holds the token rows
     assert p["smem_bytes"] == p["stages"] * stage + 2048
     assert p["scratch_bytes"] >= 2 * p["grid"] * p["block_t"] * 128 * 4 + 4 * 4 * p["tiles_sk"]
