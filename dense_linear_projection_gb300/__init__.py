@@ -242,7 +242,7 @@ def proj_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
 
 TRACE_FIELDS = ("entry", "setup", "first_load", "last_load", "first_data", "last_mma",
                 "first_acc", "epilogue_done", "teardown", "smid", "reductions", "dep_wait",
-                "epi_dep_wait")
+                "epi_dep_wait", "split_partial", "split_ready", "split_stored")
 
 
 def proj_set_overlap(h: int, mode: int) -> None:

@@ -183,9 +183,12 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         if (s_try > opt.max_cluster) s_try = opt.max_cluster;
         if (s_try > out->k_blocks) s_try = out->k_blocks;
         if (s_try >= 2 && 100 * tiles * s_try >= int64_t(opt.cluster_fill_pct) * sms &&
-            static_cast<int64_t>(stages) * stage >= int64_t(kBlockA) * b_rows * 4)
+            budget - cluster_red_bytes(static_cast<int32_t>(s_try), b_rows) >= 2 * stage)
             S = static_cast<int32_t>(s_try);
     }
+    // The peers' partial sums get their own shared memory after the ring.
+    const int32_t red_bytes = cluster_red_bytes(S, b_rows);
+    if (stages * stage + red_bytes > budget) stages = (budget - red_bytes) / stage;
     const int64_t rem = tiles % grid;
     const int64_t waves = (tiles + grid - 1) / grid;
     const int64_t fill_pct = swap ? 95 : 80;
@@ -219,7 +222,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         if (want < stages) stages = want;
     }
     out->stages = stages;
-    out->smem_bytes = stages * stage + kSmemReserve;
+    out->smem_bytes = stages * stage + red_bytes + kSmemReserve;
 
     // Scratch: one partial tile per (CTA, first|last split segment), one
     // completion counter per (split tile, 32-row quarter), and the device

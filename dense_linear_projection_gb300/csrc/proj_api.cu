@@ -33,6 +33,8 @@ struct proj_plan_s {
     CUtensorMap map_w;
     unsigned long long *trace = nullptr;  // caller's phase-trace buffer, if any
     int overlap = PROJ_OVERLAP_PROLOGUE;    // programmatic dependent launch mode
+    int prefetch_stages = kMaxStages;       // PROJ_OVERLAP_WEIGHTS: W stages before the wait
+    int sm_count = 0;
     // Device staging for proj_run_host (allocated on first use).
     void *stage_x = nullptr;
     void *stage_y = nullptr;
@@ -252,8 +254,9 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int st_force = std::atoi(e);
         if (st_force >= 2 && st_force < plan.stages && plan.kernel == PROJ_KERNEL_TC) {
             plan.stages = st_force;
-            plan.smem_bytes =
-                st_force * stage_bytes_for(plan.swap_ab ? plan.block_t : plan.block_n) + kSmemReserve;
+            const int32_t b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
+            plan.smem_bytes = st_force * stage_bytes_for(b_rows) +
+                              cluster_red_bytes(plan.cluster_split, b_rows) + kSmemReserve;
         }
     }
     if (const char *e = std::getenv("PROJ_FORCE_RASTER_GROUP")) {  // tuning only
@@ -265,6 +268,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     proj_plan_s *h = new (std::nothrow) proj_plan_s();
     if (!h) return PROJ_ERR_OUT_OF_MEMORY;
     h->device = device;
+    h->sm_count = prop.multiProcessorCount;
     h->M = M;
     h->N = N;
     h->K = K;
@@ -272,6 +276,10 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     h->y_dtype = y_dtype;
     h->has_bias = has_bias;
     h->plan = plan;
+    if (const char *e = std::getenv("PROJ_PREFETCH_STAGES")) {  // tuning only
+        const int n = std::atoi(e);
+        if (n >= 0 && n <= kMaxStages) h->prefetch_stages = n;
+    }
 
     if (plan.kernel == PROJ_KERNEL_TC) {
         if (cudaMalloc(&h->scratch, static_cast<size_t>(plan.scratch_bytes)) != cudaSuccess) {
@@ -349,7 +357,12 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
     kp.Y = Y;
     kp.y_vec = y_vec_of(Y, h->N, h->y_dtype);
     kp.trace = h->trace;
-    kp.w_prefetch = h->overlap == PROJ_OVERLAP_WEIGHTS;
+    // Weights stream early only when every SM has a CTA: the next kernel's
+    // CTAs then start as the preceding kernel's leave, in its tail.  With SMs
+    // idle they would start at once and compete with its weight stream
+    // (measured slower on GB300 for the cluster-split and 128-tile plans).
+    kp.w_prefetch =
+        h->overlap == PROJ_OVERLAP_WEIGHTS && plan.grid >= h->sm_count ? h->prefetch_stages : 0;
     TcLaunch l(plan, s, h->overlap != PROJ_OVERLAP_NONE);
     if (cudaLaunchKernelEx(&l.cfg, dev::proj_tc_kernel, kp, h->map_w, h->map_x) != cudaSuccess) {
         cudaGetLastError();

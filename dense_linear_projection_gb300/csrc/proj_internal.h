@@ -24,7 +24,7 @@ constexpr int32_t kMaxClusterSplit = 8;           // portable thread-block clust
 constexpr int32_t kClusterFillPct = 60;           // SMs a cluster split must keep busy (%)
 constexpr int32_t kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int32_t kEpilogueThreads = 128;
-constexpr int32_t kSmemReserve = 2048; // 1024-byte alignment slack + barriers
+constexpr int32_t kSmemReserve = 16384; // 1024-byte alignment slack + barriers + epilogue staging
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 // Phase-trace record: kTraceSlots unsigned 64-bit words per CTA, globaltimer
@@ -43,6 +43,10 @@ constexpr int kTraceSmid = 9;          // SM the CTA ran on (a number, not a tim
 constexpr int kTraceReductions = 10;   // split tiles epilogue warp 2 reduced (a count)
 constexpr int kTraceDepWait = 11;      // producer returned from the grid-dependency wait
 constexpr int kTraceEpiDepWait = 12;   // epilogue warp 2 returned from the grid-dependency wait
+// Epilogue warp 2, first split tile only:
+constexpr int kTraceSplitPartial = 13; // its partial sums are written (shared or global memory)
+constexpr int kTraceSplitReady = 14;   // it knows every partial of the tile is in (or it is not the reducer)
+constexpr int kTraceSplitStored = 15;  // it stored the reduced rows (or gave them to the reducer)
 
 // Error bits in the device status word.
 constexpr int kErrWaitProducer = 1 << 0;
@@ -97,13 +101,14 @@ struct KernelParams {
     int32_t cluster_split; // S >= 2: tile c / S split over the S CTAs of a cluster (DSMEM reduction)
     int32_t stages;
     int32_t stage_bytes;
+    int32_t red_bytes;     // cluster split: shared memory after the ring for peers' partial sums
     int32_t tmem_cols;
     uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128, N=b_rows)
     int32_t w_kn;          // W stored [K,N] (MN-major A operand)
     int32_t y_f32;         // store fp32 (else bf16)
     int32_t y_vec;         // Y rows start 16-byte aligned (N·size % 16 == 0, aligned base)
     int64_t wait_limit_ns; // bounded device waits give up after this long
-    int32_t w_prefetch;    // stream the first stages of W before the preceding kernel completes
+    int32_t w_prefetch;    // stages of W streamed before the preceding kernel completes (0: none)
     const uint16_t *bias;  // [N] bf16 or nullptr
     void *Y;
     float *partials;       // [2*grid][128 rows][b_rows] fp32 partial tiles
@@ -244,6 +249,15 @@ struct WorkIter {
 };
 
 // Work-shape fields of the kernel parameters, from a plan.
+// Cluster split: every CTA reserves shared memory for the partial sums its
+// peers send it, S - 1 partials of 32 rows x b_rows fp32 for each row quarter
+// it reduces: quarter q is reduced by rank q mod S (S <= 4, so ceil(4 / S)
+// quarters per reducer) or by rank q (S > 4, one quarter each).
+PROJ_HD int32_t cluster_quarters_per_reducer(int32_t S) { return S <= 4 ? (4 + S - 1) / S : 1; }
+PROJ_HD int32_t cluster_red_bytes(int32_t S, int32_t b_rows) {
+    return S > 1 ? cluster_quarters_per_reducer(S) * (S - 1) * 32 * b_rows * 4 : 0;
+}
+
 inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.swap = plan.swap_ab;
     kp.block_t = plan.block_t;
@@ -262,6 +276,7 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;
     kp.stages = plan.stages;
     kp.stage_bytes = stage_bytes_for(kp.b_rows);
+    kp.red_bytes = cluster_red_bytes(plan.cluster_split, kp.b_rows);
     kp.tmem_cols = plan.tmem_cols;
 }
 

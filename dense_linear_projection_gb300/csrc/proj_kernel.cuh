@@ -30,8 +30,8 @@
 //
 // Cluster split (decode shapes with fewer narrow tiles than SMs): each tile's
 // K range is shared by the S CTAs of one thread-block cluster.  The partial
-// sums meet in distributed shared memory and are added in rank (= K) order by
-// one rank per 32-row quarter; no scratch, no counters.
+// sums are sent through distributed shared memory to one rank per 32-row
+// quarter, which adds them in rank (= K) order; no scratch, no counters.
 //
 // Every mbarrier wait is bounded in time; a wait that runs out records a bit in
 // the device status word, raises a CTA-wide abort flag, drains in-flight copies
@@ -40,6 +40,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "proj_internal.h"
@@ -157,19 +158,19 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
                  : "memory");
 }
 
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t cluster_addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(cluster_addr)
+__device__ __forceinline__ void st_cluster_f4(uint32_t cluster_addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(cluster_addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
                  : "memory");
-    return v;
 }
 
-__device__ __forceinline__ void st_shared_f4(uint32_t saddr, float4 v) {
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
+__device__ __forceinline__ float4 ld_shared_f4(uint32_t saddr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(saddr)
                  : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void cluster_arrive() {
@@ -346,6 +347,8 @@ __device__ __forceinline__ void load_partial16(const float *row, int32_t ch, flo
 // ----------------------------------------------------------------------------
 // Shared-memory layout
 // ----------------------------------------------------------------------------
+constexpr int kYTileStride = 36;  // floats per token row of y_tile (32 + 4: 16-byte rows, fewer conflicts)
+
 struct SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
@@ -355,7 +358,11 @@ struct SmemCtl {
     uint64_t ready[4];  // cluster split: the other ranks' partials of a quarter are in place
     uint32_t tmem_base;
     int abort_flag;
+    float bias_tile[4][kMaxTokenTile];  // token-major: each epilogue warp's copy of the tile's bias
+    float y_tile[4][16 * kYTileStride]; // swapped: each epilogue warp's 16 tokens x 32 rows, transposed
 };
+static_assert(offsetof(SmemCtl, y_tile) % 16 == 0, "y_tile rows are read as 16-byte vectors");
+static_assert(sizeof(SmemCtl) + 1023 <= kSmemReserve, "the reserve holds SmemCtl and the alignment slack");
 
 // ----------------------------------------------------------------------------
 // The kernel
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
         const uint64_t need = static_cast<uint64_t>(base_addr - raw_addr) +
                               static_cast<uint64_t>(p.stages) * static_cast<uint32_t>(p.stage_bytes) +
-                              sizeof(SmemCtl);
+                              static_cast<uint32_t>(p.red_bytes) + sizeof(SmemCtl);
         if (p.stages > kMaxStages || need > dyn_bytes) {
             if (threadIdx.x == 0) atomicOr(p.status, kErrSmemTooSmall);
             return;
@@ -395,7 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    cluster_ctarank())
                             : static_cast<int32_t>(blockIdx.x);
     uint8_t *smem = smem_raw + (base_addr - raw_addr);
-    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + p.stages * p.stage_bytes);
+    // [ring: stages x stage_bytes][peers' partial sums: red_bytes][SmemCtl]
+    const uint32_t red_addr = base_addr + static_cast<uint32_t>(p.stages * p.stage_bytes);
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(smem + p.stages * p.stage_bytes + p.red_bytes);
     volatile int *abort_flag = &ctl->abort_flag;
 
     const int warp = threadIdx.x / 32;
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&ctl->drain), 1);
         if (p.cluster_split > 1)
             for (int qq = 0; qq < 4; ++qq)
-                mbar_init(smem_u32(&ctl->ready[qq]), static_cast<uint32_t>(p.cluster_split - 1));
+                mbar_init(smem_u32(&ctl->ready[qq]), static_cast<uint32_t>(32 * (p.cluster_split - 1)));
         ctl->abort_flag = 0;
         fence_barrier_init();
     }
@@ -478,14 +487,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Optional weight prefetch: fill the ring with W before the
             // preceding kernel has finished (W must not be written by it).
             int64_t pre = 0;
-            if (p.w_prefetch) {
+            if (p.w_prefetch > 0) {
+                const int32_t pre_max = min(p.w_prefetch, stages);
                 WorkIter it;
                 it.init(p, cta);
                 Segment s;
-                while (pre < stages && it.next(p, s)) {
+                while (pre < pre_max && it.next(p, s)) {
                     int32_t tm, tn;
                     tile_coords(p, s.tile, tm, tn);
-                    for (int32_t kb = s.kb0; kb < s.kb1 && pre < stages; ++kb) {
+                    for (int32_t kb = s.kb0; kb < s.kb1 && pre < pre_max; ++kb) {
                         const uint32_t full = smem_u32(&ctl->full[pre]);
                         mbar_arrive_expect_tx(full, stage_bytes);  // W + X bytes of the stage
                         load_w(base_addr + static_cast<uint32_t>(pre) * stage_bytes + w_off, full, tn, kb);
@@ -598,17 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             cluster_waited = true;
         }
         int32_t seg_idx = 0;
+        bool split_traced = false;  // the split-epilogue stamps cover the first split tile
+        float *bias_s = ctl->bias_tile[q];
         WorkIter it;
         it.init(p, cta);
         Segment s;
         while (it.next(p, s)) {
             const int32_t buf = seg_idx & 1;
             const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
-            if (!wait_phase(smem_u32(&ctl->acc_full[buf]), use, abort_flag, p.status,
-                            kErrWaitEpilogue, p.wait_limit_ns))
-                break;
-            tc_fence_after_sync();
-            if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
             int32_t tm, tn;
             tile_coords(p, s.tile, tm, tn);
             // Tensor-memory lane r holds one A row, columns hold B rows.
@@ -621,25 +628,82 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int32_t ccount = p.swap ? min(p.block_t, p.M - m0) : min(p.block_n, p.N - n0);
             const int32_t nchunks = (ccount + 15) / 16;
             const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(buf) * half_cols;
+            // The bias is fetched before the accumulator wait, so that a DRAM
+            // round trip under the weight stream's load overlaps the MMAs:
+            // swapped, one value per lane (its weight row); token-major, the
+            // tile's block_n values into this warp's shared-memory slice.
             const float bias_lane =
                 (p.swap && p.bias != nullptr && lane_ok) ? bf16_bits_to_float(p.bias[lane_row]) : 0.f;
+            if (!p.swap && p.bias != nullptr) {
+                for (int32_t j = lane; j < p.block_n; j += 32)
+                    bias_s[j] = n0 + j < p.N ? bf16_bits_to_float(p.bias[n0 + j]) : 0.f;
+                __syncwarp();
+            }
+            if (!wait_phase(smem_u32(&ctl->acc_full[buf]), use, abort_flag, p.status,
+                            kErrWaitEpilogue, p.wait_limit_ns))
+                break;
+            tc_fence_after_sync();
+            if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
+            const bool stamp_split = s.split && !split_traced && warp == 2 && lane == 0;
+            if (s.split) split_traced = true;
             // Store one chunk of 16 columns of this lane's row (+ bias).
+            // Store one chunk of 16 columns of this lane's row (+ bias).  Every
+            // lane of the warp calls it (the swapped path shuffles through
+            // shared memory).
             auto store_chunk = [&](int32_t ch, const float (&y)[16]) {
-                if (!lane_ok) return;
                 if (p.swap) {
+                    // The warp holds 32 consecutive weight rows (lanes) x 16
+                    // tokens (registers), but Y rows run along the weight rows:
+                    // transpose through shared memory and store 16-byte vectors
+                    // (2 stores a lane for bf16, 4 for fp32, instead of 16).
+                    const int32_t mb = m0 + ch * 16;   // first token of the chunk
+                    const int32_t nw = n0 + q * 32;    // first weight row of the warp
+                    if (p.y_vec && nw + 32 <= p.N && mb + 16 <= p.M) {
+                        float *t = ctl->y_tile[q];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) t[i * kYTileStride + lane] = y[i] + bias_lane;
+                        __syncwarp();
+                        if (p.y_f32) {
+#pragma unroll
+                            for (int pass = 0; pass < 4; ++pass) {
+                                const int32_t mi = pass * 4 + lane / 8, nc = (lane % 8) * 4;
+                                const float4 v = *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc);
+                                *reinterpret_cast<float4 *>(static_cast<float *>(p.Y) +
+                                                            static_cast<size_t>(mb + mi) * p.N + nw + nc) = v;
+                            }
+                        } else {
+#pragma unroll
+                            for (int pass = 0; pass < 2; ++pass) {
+                                const int32_t mi = pass * 8 + lane / 4, nc = (lane % 4) * 8;
+                                const float4 a = *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc);
+                                const float4 b = *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc + 4);
+                                __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y);
+                                __nv_bfloat162 h1 = __floats2bfloat162_rn(a.z, a.w);
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y);
+                                __nv_bfloat162 h3 = __floats2bfloat162_rn(b.z, b.w);
+                                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) +
+                                                           static_cast<size_t>(mb + mi) * p.N + nw + nc) =
+                                    make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                                               *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                            }
+                        }
+                        __syncwarp();  // the tile is reused by the next chunk
+                        return;
+                    }
+                    if (!lane_ok) return;
                     const int32_t n = lane_row;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const int32_t m = m0 + ch * 16 + i;
+                        const int32_t m = mb + i;
                         if (m < p.M) store_y(p, static_cast<size_t>(m) * p.N + n, y[i] + bias_lane);
                     }
                 } else {
+                    if (!lane_ok) return;
                     const int32_t m = lane_row;
                     const int32_t nb = n0 + ch * 16;
                     float v[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        v[i] = y[i] + ((p.bias != nullptr && nb + i < p.N) ? bf16_bits_to_float(p.bias[nb + i]) : 0.f);
+                    for (int i = 0; i < 16; ++i) v[i] = y[i] + (p.bias != nullptr ? bias_s[ch * 16 + i] : 0.f);
                     const size_t off = static_cast<size_t>(m) * p.N + nb;
                     if (p.y_vec && nb + 16 <= p.N) {
                         // 16 consecutive outputs of one row: vector stores.
@@ -683,54 +747,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if (clustered) {
                 // Cluster split: the S CTAs of this cluster hold the tile's
                 // partial sums over consecutive K ranges (rank order = K
-                // order).  Every rank leaves its rows of quarter q in its own
-                // shared memory (the drained ring); rank q mod S (S <= 4) or q
-                // (S = 8) waits for the others' signals and adds all ranks in
-                // ascending order, so every run gives the same bits.
+                // order).  Quarter q is reduced by rank q mod S (S <= 4) or q
+                // (S > 4).  Every other rank stores its 32 rows straight into
+                // the reducer's shared memory and arrives there (every lane,
+                // releasing its own stores); the reducer then reads them
+                // locally and adds all ranks in ascending order, so every run
+                // gives the same bits.
                 const uint32_t S = static_cast<uint32_t>(p.cluster_split);
                 const uint32_t rank = static_cast<uint32_t>(cta) % S;  // = %cluster_ctarank
                 const uint32_t reducer = S <= 4 ? static_cast<uint32_t>(q) % S : static_cast<uint32_t>(q);
-                // [16-column chunk][float4 of the chunk][lane]: 16 consecutive
-                // bytes per lane, a warp's accesses contiguous.
-                const uint32_t region = base_addr + static_cast<uint32_t>(q) * 32u *
-                                                        static_cast<uint32_t>(p.b_rows) * 4u;
+                const uint32_t slot_q = S <= 4 ? static_cast<uint32_t>(q) / S : 0u;
+                const uint32_t part_bytes = 32u * static_cast<uint32_t>(p.b_rows) * 4u;
+                // A partial is [16-column chunk][float4 of the chunk][lane]:
+                // 16 consecutive bytes per lane, a warp's accesses contiguous.
                 const uint32_t lane_off16 = static_cast<uint32_t>(lane) * 16u;
-                for (int32_t ch = 0; ch < nchunks; ++ch) {
-                    float v[16];
-                    tmem_load16(tbase + ch * 16, v);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        st_shared_f4(region + static_cast<uint32_t>(ch * 4 + i) * 512u + lane_off16,
-                                     make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
-                }
-                release_accumulator();  // (its __syncwarp also orders the stores above)
+                const uint32_t quarter_base = red_addr + slot_q * (S - 1u) * part_bytes + lane_off16;
                 if (rank != reducer) {
-                    if (lane == 0) mbar_arrive_remote(map_to_rank(smem_u32(&ctl->ready[q]), reducer));
-                } else if (wait_phase<true>(smem_u32(&ctl->ready[q]), 0u, abort_flag, p.status,
-                                            kErrWaitEpilogue, p.wait_limit_ns)) {
-                    if (warp == 2 && lane == 0) ++reductions;
+                    const uint32_t j = rank < reducer ? rank : rank - 1u;  // contributor index
+                    const uint32_t dst = map_to_rank(quarter_base + j * part_bytes, reducer);
                     for (int32_t ch = 0; ch < nchunks; ++ch) {
-                        float acc[16];
+                        float v[16];
+                        tmem_load16(tbase + ch * 16, v);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-                        // One rank at a time: the epilogue has no registers
-                        // to spare for more loads in flight.
-                        for (uint32_t rk = 0; rk < S; ++rk) {
-                            const uint32_t src = map_to_rank(region, rk) + lane_off16;
-                            float4 o[4];
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                o[i] = ld_cluster_f4(src + static_cast<uint32_t>(ch * 4 + i) * 512u);
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                acc[4 * i] += o[i].x;
-                                acc[4 * i + 1] += o[i].y;
-                                acc[4 * i + 2] += o[i].z;
-                                acc[4 * i + 3] += o[i].w;
-                            }
-                        }
-                        store_chunk(ch, acc);
+                        for (int i = 0; i < 4; ++i)
+                            st_cluster_f4(dst + static_cast<uint32_t>(ch * 4 + i) * 512u,
+                                          make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
                     }
+                    release_accumulator();
+                    if (stamp_split) trace_stamp(p, kTraceSplitPartial);
+                    mbar_arrive_remote(map_to_rank(smem_u32(&ctl->ready[q]), reducer));
+                    if (stamp_split) {
+                        trace_stamp(p, kTraceSplitReady);
+                        trace_stamp(p, kTraceSplitStored);
+                    }
+                } else {
+                    if (stamp_split) trace_stamp(p, kTraceSplitPartial);
+                    if (wait_phase<true>(smem_u32(&ctl->ready[q]), 0u, abort_flag, p.status,
+                                         kErrWaitEpilogue, p.wait_limit_ns)) {
+                        if (stamp_split) trace_stamp(p, kTraceSplitReady);
+                        if (warp == 2 && lane == 0) ++reductions;
+                        for (int32_t ch = 0; ch < nchunks; ++ch) {
+                            float own[16], acc[16];
+                            tmem_load16(tbase + ch * 16, own);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                            for (uint32_t rk = 0; rk < S; ++rk) {
+                                if (rk == rank) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) acc[i] += own[i];
+                                    continue;
+                                }
+                                const uint32_t src = quarter_base + (rk < rank ? rk : rk - 1u) * part_bytes +
+                                                     static_cast<uint32_t>(ch * 4) * 512u;
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float4 o = ld_shared_f4(src + static_cast<uint32_t>(i) * 512u);
+                                    acc[4 * i] += o.x;
+                                    acc[4 * i + 1] += o.y;
+                                    acc[4 * i + 2] += o.z;
+                                    acc[4 * i + 3] += o.w;
+                                }
+                            }
+                            store_chunk(ch, acc);
+                        }
+                        if (stamp_split) trace_stamp(p, kTraceSplitStored);
+                    }
+                    release_accumulator();
                 }
             } else {
                 // Split tile.  This lane's row of fp32 partial sums goes to
@@ -762,6 +844,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int32_t c = c_first; c <= c_last; ++c) nseg += cta_has_units(c, U, p.grid) ? 1 : 0;
                     }
                 }
+                if (stamp_split) trace_stamp(p, kTraceSplitPartial);
                 // Publish (release) and count arrivals per 32-row quarter.
                 __syncwarp();
                 int last = 0;
@@ -776,6 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 last = __shfl_sync(0xFFFFFFFFu, last, 0);
                 __syncwarp();
+                if (stamp_split) trace_stamp(p, kTraceSplitReady);
                 if (last && warp == 2 && lane == 0) ++reductions;
 
                 if (last && p.sk_pair) {
@@ -847,6 +931,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                if (stamp_split) trace_stamp(p, kTraceSplitStored);
             }
             ++seg_idx;
         }

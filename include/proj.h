@@ -252,7 +252,11 @@ proj_status_t proj_device_status(proj_handle_t h, void *stream);
  *                          X, W, bias, Y or scratch) until that kernel has
  *                          completed: always safe.
  *   PROJ_OVERLAP_WEIGHTS   as above, and the first pipeline stages of W are
- *                          streamed before the preceding kernel completes.
+ *                          streamed before the preceding kernel completes,
+ *                          for plans that occupy every SM.  (A plan that
+ *                          leaves SMs idle would start streaming there while
+ *                          the preceding kernel still streams its own data,
+ *                          and delay it: such plans behave as PROLOGUE.)
  *                          The caller promises that W is not written by the
  *                          kernel launched just before the run (true for
  *                          inference weights).
@@ -275,7 +279,10 @@ proj_status_t proj_set_overlap(proj_handle_t h, proj_overlap_t mode);
  * received by the epilogue, [7] epilogue finished, [8] final barrier
  * (globaltimer nanoseconds), [9] the SM id, [10] split tiles reduced by the
  * CTA's first epilogue warp, [11] producer past the grid-dependency wait,
- * [12] epilogue past it; [13..15] unused.  The caller owns the buffer; a
+ * [12] epilogue past it; for the first split tile of that warp: [13] its
+ * partial sums written, [14] all partials of the tile known to be in (or,
+ * for a warp that does not reduce, the same as [13]), [15] the reduced rows
+ * stored (or handed over).  The caller owns the buffer; a
  * NULL buffer turns tracing off.  PROJ_ERR_INVALID_ARG if the buffer is too
  * small, PROJ_ERR_MISALIGNED if not 8-byte aligned, PROJ_ERR_UNSUPPORTED for
  * plans without the tensor-core kernel.

@@ -78,7 +78,6 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
         assert 2 <= S <= 8 and S <= KT and p["swap_ab"] == 1 and p["block_t"] <= 64
         assert p["tiles_dp"] == 0 and G == tiles * S and 10 * G >= 6 * sms
         assert p["scratch_bytes"] == 256
-        assert p["stages"] * (128 + p["block_t"]) * 128 >= 128 * p["block_t"] * 4
     if p["tiles_sk"]:
         assert p["tiles_dp"] % G == 0
     else:  # whole tiles only: the last wave is nearly full (95 % swapped, 80 % token-major)
@@ -91,8 +90,15 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     b_rows = p["block_t"] if p["swap_ab"] else p["block_n"]
     assert p["tmem_cols"] >= 2 * b_rows
     # The launch's shared memory covers the ring (A 128 rows + B rows, 64 K each),
-    # its barriers and 1024-byte alignment slack.
-    assert p["smem_bytes"] == p["stages"] * (128 + b_rows) * 128 + 2048
+    # its barriers, the epilogue's bias and output staging, 1024-byte alignment slack,
+    # and in a cluster split the peers' partial sums: S - 1 partials of 32 rows
+    # for each quarter the CTA reduces (quarter q goes to rank q mod S, S <= 4,
+    # or to rank q).
+    red = 0
+    if S:
+        quarters = -(-4 // S) if S <= 4 else 1
+        red = quarters * (S - 1) * 32 * b_rows * 4
+    assert p["smem_bytes"] == p["stages"] * (128 + b_rows) * 128 + red + 16384
     cover = np.zeros((tiles, KT), dtype=np.int32)
     by_tile = collections.defaultdict(list)
     coords = {}
@@ -239,7 +245,7 @@ def test_scratch_and_stages():
     p = plan(16, 28672, 8192)
     assert p["tiles_sk"] > 0 and p["cluster_split"] == 0
     stage = 128 * 64 * 2 + p["block_t"] * 64 * 2  # swapped: B holds the token rows
-    assert p["smem_bytes"] == p["stages"] * stage + 2048
+    assert p["smem_bytes"] == p["stages"] * stage + 16384
     assert p["scratch_bytes"] >= 2 * p["grid"] * p["block_t"] * 128 * 4 + 4 * 4 * p["tiles_sk"]
     assert p["tmem_cols"] >= 2 * p["block_t"] and p["tmem_cols"] in (32, 64, 128, 256, 512)
 
