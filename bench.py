@@ -17,7 +17,13 @@ faster": CUDA-graph replay, cold L2, fresh weights):
     max over ranks;
   * e2e repeats the K steps through proj_run_host (X copied host→device and Y
     device→host every step, pinned buffers; W stays resident);
-  * the fp64 oracle is timed on the host cores as the CPU baseline;
+  * ``repeats``: the spread (median, p10, p90 of per-call µs) over 7 shorter
+    timed regions of the same kind; ``cold_call``: single calls, each after
+    writing twice the L2, timed alone;
+  * ``library_baseline``: the same projection through cuBLAS (torch.addmm /
+    torch.mm), informational only;
+  * the fp64 oracle is timed on the host cores as the CPU baseline, and the
+    output of the timed steps is checked against it on the sampled columns;
   * nvidia-smi clocks are sampled while the GPU is under load.
 
 Multi-GPU: independent replicas (one per rank, no collective on the data path);
@@ -201,10 +207,12 @@ def visible_gpu_id(local_rank: int) -> str:
 
 
 # ---------------------------------------------------------------- CPU oracle
-def cpu_oracle_timing(w, inp, target_s: float) -> dict:
+def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None) -> dict:
     """Time the fp64 oracle on the host cores on a bounded sample of the
     workload: all M token rows against the first n_cols output columns (or the
-    whole workload, repeated, if that is quick).  Returns weight GB/s."""
+    whole workload, repeated, if that is quick).  Returns weight GB/s.  With
+    ``y_gpu`` (the output the timed steps left, as float64), the sampled
+    columns of it are also checked against the oracle's result."""
     import numpy as np
     import oracle
     threads = oracle.max_threads()
@@ -228,13 +236,19 @@ def cpu_oracle_timing(w, inp, target_s: float) -> dict:
     Ws, bs = cols_slice(n_cols)
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.project(X, Ws, w.w_layout, bs)
+        r = oracle.project(X, Ws, w.w_layout, bs)
     elapsed = time.perf_counter() - t0
     wbytes = 2.0 * n_cols * w.K * reps
     sample = (f"all {w.M} token rows x {n_cols} of {w.N} output columns"
               + (f", {reps} repetitions" if reps > 1 else "") + f", {elapsed:.2f} s")
-    return {"value": wbytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": sample, "seconds": elapsed}
+    out = {"value": wbytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": sample, "seconds": elapsed}
+    if y_gpu is not None:
+        # The tolerance of the parity tests: |u - r| <= 1e-3 + 5e-3·|r|.
+        u = y_gpu[:, :n_cols]
+        bad = int(np.count_nonzero(~(np.abs(u - r) <= 1e-3 + 5e-3 * np.abs(r))))
+        out["timed_output_check"] = {"cells": int(u.size), "out_of_tolerance": bad}
+    return out
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -327,6 +341,77 @@ def run_gpu_arm(args) -> dict:
 
     agg = aggregate_throughput(w.weight_bytes * args.steps, seconds, device)
     t_step = agg["seconds"] / args.steps
+
+    # ---- Spread: R shorter timed regions of the same kind (per-call µs).
+    repeats = None
+    if args.repeats > 0:
+        r_steps = chunk * max(1, (args.steps // 10) // chunk)
+        per_call = []
+        with torch.cuda.stream(stream):
+            for _ in range(args.repeats):
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(r_steps // chunk):
+                    g_chunk.replay()
+                b_.record(stream)
+                b_.synchronize()
+                per_call.append(a.elapsed_time(b_) * 1e3 / r_steps)
+        qs = statistics.quantiles(per_call, n=10)
+        repeats = {"n": args.repeats, "steps_each": r_steps, "median_us": statistics.median(per_call),
+                   "p10_us": qs[0], "p90_us": qs[-1]}
+
+    # ---- One call after an L2 flush (a write of twice the L2), not overlapped.
+    cold = None
+    if args.cold_calls > 0:
+        flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(args.cold_calls):
+                flush.fill_(float(i))
+                a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                proj(X, Ws[i % n_copies], bias, out=Y, stream=stream)
+                b_.record(stream)
+                b_.synchronize()
+                times.append(a.elapsed_time(b_) * 1e3)
+        del flush
+        cold = {"calls": args.cold_calls, "median_us": statistics.median(times),
+                "what": "one proj_run after writing 2x L2, events around the call alone"}
+
+    # ---- Informational: the same projection through cuBLAS (torch), never the target.
+    library = None
+    if args.library:
+        Yl = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+
+        def lib_call(Wc):
+            Wm = Wc.t() if w.w_layout == 0 else Wc
+            if bias is not None:
+                torch.addmm(bias, X, Wm, out=Yl)
+            else:
+                torch.mm(X, Wm, out=Yl)
+
+        with torch.cuda.stream(stream):
+            lib_call(W0)
+        torch.cuda.synchronize()
+        gl = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gl, stream=stream):
+            for i in range(chunk):
+                lib_call(Ws[i % n_copies])
+        l_steps = chunk * max(1, (args.steps // 4) // chunk)
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, math.ceil(args.warmup / chunk))):
+                gl.replay()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(l_steps // chunk):
+                gl.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        t_lib = a.elapsed_time(b_) / 1e3 / l_steps
+        library = {"impl": "torch.addmm / torch.mm (cuBLAS), bf16 output", "steps": l_steps,
+                   "us_per_call": t_lib * 1e6, "value": w.weight_bytes / t_lib / 1e9, "unit": "GB/s",
+                   "note": "informational; same inputs, W rotation and CUDA-graph replay"}
+        del Yl, gl
     peaks = load_peaks()
     traffic, profile_path = profile_traffic(args.workload if args.m is None else
                                             f"{args.workload}_m{args.m}")
@@ -378,7 +463,11 @@ def run_gpu_arm(args) -> dict:
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_timing(w, inp, args.cpu_seconds)
+        # Y still holds the timed steps' output (every W copy is the same W).
+        proj(X, W0, bias, out=Y, stream=stream)  # the output of one plain call, to be safe
+        torch.cuda.synchronize()
+        y64 = Y.float().cpu().numpy().astype(np.float64)
+        cpu = cpu_oracle_timing(w, inp, args.cpu_seconds, y_gpu=y64)
         cpu.pop("seconds", None)
 
     plan = proj.plan
@@ -407,6 +496,9 @@ def run_gpu_arm(args) -> dict:
         },
         "us_per_call": t_step * 1e6,
         "tflops": w.flops / t_step / 1e12,
+        "repeats": repeats,
+        "cold_call": cold,
+        "library_baseline": library,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -495,6 +587,12 @@ def parse_args(argv=None):
                     help="overlap of consecutive steps (programmatic dependent launch)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--repeats", type=int, default=7,
+                    help="shorter timed regions for the median/p10/p90 spread (0: none)")
+    ap.add_argument("--cold-calls", type=int, default=10,
+                    help="single calls timed after an L2 flush (0: none)")
+    ap.add_argument("--no-library", dest="library", action="store_false",
+                    help="skip the informational cuBLAS timing")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -205,6 +205,8 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     }
     out->tiles_dp = tiles - out->tiles_sk;
     out->units_sk = out->tiles_sk * out->k_blocks;
+    // Whole tiles only: no more CTAs than tiles (the rest would have no work).
+    if (out->tiles_sk == 0 && tiles < out->grid) out->grid = static_cast<int32_t>(tiles);
 
     // Pipeline depth.  When the weights stream from HBM (a single token tile,
     // or any split plan), about kInflightTarget bytes of stages per SM keep

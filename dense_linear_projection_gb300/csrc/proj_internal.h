@@ -24,7 +24,7 @@ constexpr int32_t kMaxClusterSplit = 8;           // portable thread-block clust
 constexpr int32_t kClusterFillPct = 60;           // SMs a cluster split must keep busy (%)
 constexpr int32_t kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int32_t kEpilogueThreads = 128;
-constexpr int32_t kSmemReserve = 16384; // 1024-byte alignment slack + barriers + epilogue staging
+constexpr int32_t kSmemReserve = 25600; // 1024-byte alignment slack + barriers + epilogue staging
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
 // Phase-trace record: kTraceSlots unsigned 64-bit words per CTA, globaltimer

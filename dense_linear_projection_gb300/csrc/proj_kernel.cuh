@@ -272,6 +272,21 @@ __device__ __forceinline__ void tmem_load16(uint32_t taddr, float (&v)[16]) {
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive fp32 columns of this thread's tensor-memory lane in one load
+// and one wait (four 16-column chunks: one round trip instead of four).
+__device__ __forceinline__ void tmem_load64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // Shared-memory matrix descriptor (tcgen05 format), 128-byte swizzle.
 // lbo/sbo in bytes: for K-major tiles sbo is the 8-row group stride (1024);
 // for MN-major tiles lbo is the stride between 64-element MN blocks and sbo
@@ -359,7 +374,10 @@ struct SmemCtl {
     uint32_t tmem_base;
     int abort_flag;
     float bias_tile[4][kMaxTokenTile];  // token-major: each epilogue warp's copy of the tile's bias
-    float y_tile[4][16 * kYTileStride]; // swapped: each epilogue warp's 16 tokens x 32 rows, transposed
+    // Output staging, one area per epilogue warp: swapped tiles, 16 tokens x
+    // 32 weight rows (fp32, stride kYTileStride); token-major tiles, 32 token
+    // rows x 32 columns (fp32 stride kYTileStride, or bf16 stride 40).
+    float y_tile[4][32 * kYTileStride];
 };
 static_assert(offsetof(SmemCtl, y_tile) % 16 == 0, "y_tile rows are read as 16-byte vectors");
 static_assert(sizeof(SmemCtl) + 1023 <= kSmemReserve, "the reserve holds SmemCtl and the alignment slack");
@@ -504,8 +522,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (pre > 0) trace_stamp(p, kTraceFirstLoad);
             }
-            griddep_wait();  // X (and everything else) may come from the preceding kernel
-            trace_stamp(p, kTraceDepWait);
+            // X (and everything else) may come from the preceding kernel: the
+            // grid-dependency wait comes right before the first load of this
+            // loop, after the work decomposition and the first stage's barrier
+            // are ready (that code's first run, instruction fetch included,
+            // then overlaps the preceding kernel instead of following it).
+            bool dep_done = false;
+            auto dep_wait = [&]() {
+                if (!dep_done) {
+                    griddep_wait();
+                    trace_stamp(p, kTraceDepWait);
+                    dep_done = true;
+                }
+            };
             int32_t stage = 0;
             uint32_t phase = 0;
             WorkIter it;
@@ -525,8 +554,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         mbar_arrive_expect_tx(full, stage_bytes);
+                        dep_wait();
                         load_w(st_base + w_off, full, tn, kb);
                     }
+                    dep_wait();
                     tma_load_2d(st_base + x_off, &tmap_x, full, kb * kBlockK, tm * p.block_t, pol_x);
                     if (issued == 0 && pre == 0) trace_stamp(p, kTraceFirstLoad);
                     ++issued;
@@ -730,6 +761,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             };
+            // Token-major: store 32 columns [n0 + 16·ch, +32) of the warp's 32
+            // token rows (+ bias).  Each lane holds one row, so the block goes
+            // through shared memory and leaves as whole row segments (bf16: 8
+            // rows of 64 bytes per store instruction, fp32: 4 rows of 128),
+            // not 32 rows touched by every instruction.  Every lane calls it.
+            auto store_cols32 = [&](int32_t ch, const float *y) {
+                const int32_t nb = n0 + ch * 16;
+                const int32_t mw = m0 + q * 32;
+                float *t = ctl->y_tile[q];
+                float b[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) b[i] = y[i] + (p.bias != nullptr ? bias_s[ch * 16 + i] : 0.f);
+                if (p.y_f32) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4 *>(t + lane * kYTileStride + 4 * j) =
+                            make_float4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int pass = 0; pass < 8; ++pass) {
+                        const int32_t r = pass * 4 + lane / 8, c = (lane % 8) * 4;
+                        if (mw + r < p.M)
+                            *reinterpret_cast<float4 *>(static_cast<float *>(p.Y) +
+                                                        static_cast<size_t>(mw + r) * p.N + nb + c) =
+                                *reinterpret_cast<const float4 *>(t + r * kYTileStride + c);
+                    }
+                } else {
+                    uint8_t *tb = reinterpret_cast<uint8_t *>(t);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            __nv_bfloat162 h = __floats2bfloat162_rn(b[8 * j + 2 * k], b[8 * j + 2 * k + 1]);
+                            w4[k] = *reinterpret_cast<uint32_t *>(&h);
+                        }
+                        *reinterpret_cast<uint4 *>(tb + lane * 80 + 16 * j) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int pass = 0; pass < 4; ++pass) {
+                        const int32_t r = pass * 8 + lane / 4, c = (lane % 4) * 8;
+                        if (mw + r < p.M)
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) +
+                                                       static_cast<size_t>(mw + r) * p.N + nb + c) =
+                                *reinterpret_cast<const uint4 *>(tb + r * 80 + c * 2);
+                    }
+                }
+                __syncwarp();  // the staging area is reused by the next block
+            };
             auto release_accumulator = [&]() {
                 tc_fence_before_sync();
                 __syncwarp();
@@ -737,8 +818,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
 
             if (!s.split) {
-                // Whole tile: tensor memory -> (+ bias) -> Y.
-                for (int32_t ch = 0; ch < nchunks; ++ch) {
+                // Whole tile: tensor memory -> (+ bias) -> Y, four chunks per
+                // tensor-memory round trip while whole groups of four remain.
+                int32_t ch = 0;
+                for (; ch + 4 <= nchunks; ch += 4) {
+                    float v[64];
+                    tmem_load64(tbase + ch * 16, v);
+                    if (!p.swap && p.y_vec && n0 + (ch + 4) * 16 <= p.N) {
+                        store_cols32(ch, v);
+                        store_cols32(ch + 2, v + 32);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            store_chunk(ch + u, *reinterpret_cast<const float(*)[16]>(v + 16 * u));
+                    }
+                }
+                for (; ch < nchunks; ++ch) {
                     float v[16];
                     tmem_load16(tbase + ch * 16, v);
                     store_chunk(ch, v);

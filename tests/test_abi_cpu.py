@@ -98,7 +98,7 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     if S:
         quarters = -(-4 // S) if S <= 4 else 1
         red = quarters * (S - 1) * 32 * b_rows * 4
-    assert p["smem_bytes"] == p["stages"] * (128 + b_rows) * 128 + red + 16384
+    assert p["smem_bytes"] == p["stages"] * (128 + b_rows) * 128 + red + 25600
     cover = np.zeros((tiles, KT), dtype=np.int32)
     by_tile = collections.defaultdict(list)
     coords = {}
@@ -245,7 +245,7 @@ def test_scratch_and_stages():
     p = plan(16, 28672, 8192)
     assert p["tiles_sk"] > 0 and p["cluster_split"] == 0
     stage = 128 * 64 * 2 + p["block_t"] * 64 * 2  # swapped: B holds the token rows
-    assert p["smem_bytes"] == p["stages"] * stage + 16384
+    assert p["smem_bytes"] == p["stages"] * stage + 25600
     assert p["scratch_bytes"] >= 2 * p["grid"] * p["block_t"] * 128 * 4 + 4 * 4 * p["tiles_sk"]
     assert p["tmem_cols"] >= 2 * p["block_t"] and p["tmem_cols"] in (32, 64, 128, 256, 512)
 
