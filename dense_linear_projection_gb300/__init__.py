@@ -28,6 +28,7 @@ __all__ = [
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "TRACE_FIELDS",
     "PROJ_OVERLAP_NONE", "PROJ_OVERLAP_PROLOGUE", "PROJ_OVERLAP_WEIGHTS", "proj_run_noalloc",
+    "proj_packed_weight_bytes", "proj_pack_weights", "proj_run_packed", "proj_run_host_packed",
     "Projection",
 ]
 
@@ -42,6 +43,7 @@ EXPORTED_SYMBOLS = (
     "proj_plan_compute", "proj_plan_segments", "proj_plan_reduction_order", "proj_create", "proj_run", "proj_run_host", "proj_device_status",
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "proj_run_noalloc",
+    "proj_packed_weight_bytes", "proj_pack_weights", "proj_run_packed", "proj_run_host_packed",
 )
 
 
@@ -114,6 +116,10 @@ def lib() -> ctypes.CDLL:
     L.proj_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
     L.proj_set_overlap.argtypes = [vp, i32]
     L.proj_run_noalloc.argtypes = [i64, i64, i64, i32, i32, vp, vp, vp, vp, vp]
+    L.proj_packed_weight_bytes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+    L.proj_pack_weights.argtypes = [vp, vp, vp, vp]
+    L.proj_run_packed.argtypes = [vp, vp, vp, vp, vp, vp]
+    L.proj_run_host_packed.argtypes = [vp, vp, vp, vp, vp, vp]
     for name in EXPORTED_SYMBOLS:
         if name != "proj_status_string":
             getattr(L, name).restype = st
@@ -214,6 +220,26 @@ def proj_run_noalloc(M: int, N: int, K: int, w_layout: int, y_dtype: int, X, W, 
                                   _ptr(Y), _stream(stream)), "proj_run_noalloc")
 
 
+def proj_packed_weight_bytes(h: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().proj_packed_weight_bytes(h, ctypes.byref(out)), "proj_packed_weight_bytes")
+    return int(out.value)
+
+
+def proj_pack_weights(h: int, W, W_packed, stream=None) -> None:
+    _check(lib().proj_pack_weights(h, _ptr(W), _ptr(W_packed), _stream(stream)), "proj_pack_weights")
+
+
+def proj_run_packed(h: int, X, W_packed, bias, Y, stream=None) -> None:
+    _check(lib().proj_run_packed(h, _ptr(X), _ptr(W_packed), _ptr(bias), _ptr(Y), _stream(stream)),
+           "proj_run_packed")
+
+
+def proj_run_host_packed(h: int, X_host, W_packed, bias, Y_host, stream=None) -> None:
+    _check(lib().proj_run_host_packed(h, _ptr(X_host), _ptr(W_packed), _ptr(bias), _ptr(Y_host),
+                                      _stream(stream)), "proj_run_host_packed")
+
+
 def proj_device_status(h: int, stream=None) -> int:
     """Raw status (PROJ_OK or an error code); does not raise."""
     return int(lib().proj_device_status(h, _stream(stream)))
@@ -279,15 +305,27 @@ class Projection:
     def plan(self) -> dict:
         return proj_plan_info(self.handle)
 
-    def __call__(self, X, W, bias=None, out=None, stream=None):
+    def __call__(self, X, W, bias=None, out=None, stream=None, packed: bool = False):
+        """Y = X·Wᵀ (+ bias); ``packed=True`` takes weights from :meth:`pack`."""
         import torch
         if out is None:
             dt = torch.float32 if self.y_dtype == PROJ_F32 else torch.bfloat16
             out = torch.empty((self.M, self.N), dtype=dt, device=X.device)
         if stream is None:
             stream = torch.cuda.current_stream(X.device)
-        proj_run(self.handle, X, W, bias, out, stream)
+        (proj_run_packed if packed else proj_run)(self.handle, X, W, bias, out, stream)
         return out
+
+    def pack(self, W, stream=None):
+        """Repack weights into this handle's tile-contiguous layout (a preparation
+        step); returns a new bf16 CUDA tensor to pass with ``packed=True``."""
+        import torch
+        n = proj_packed_weight_bytes(self.handle)
+        P = torch.empty(max(n // 2, 8), dtype=torch.bfloat16, device=W.device)
+        if stream is None:
+            stream = torch.cuda.current_stream(W.device)
+        proj_pack_weights(self.handle, W, P, stream)
+        return P
 
     def status(self, stream=None) -> int:
         return proj_device_status(self.handle, stream)

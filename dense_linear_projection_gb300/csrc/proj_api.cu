@@ -29,8 +29,10 @@ struct proj_plan_s {
     // Tensor maps cached by base pointer (rebuilt when X or W moves).
     const void *map_x_ptr = nullptr;
     const void *map_w_ptr = nullptr;
+    const void *map_wp_ptr = nullptr;  // packed weights
     CUtensorMap map_x;  // CUtensorMap carries its own 64-byte alignment
     CUtensorMap map_w;
+    CUtensorMap map_wp;
     unsigned long long *trace = nullptr;  // caller's phase-trace buffer, if any
     int overlap = PROJ_OVERLAP_PROLOGUE;    // programmatic dependent launch mode
     int prefetch_stages = kMaxStages;       // PROJ_OVERLAP_WEIGHTS: W stages before the wait
@@ -315,8 +317,67 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     return PROJ_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Rows of the packed weight layout (see proj_pack_weights), or -1 if they do
+// not fit the 31-bit TMA coordinates.
+int64_t packed_rows(const proj_plan_desc_t &plan) {
+    const int64_t rows = plan.tiles_n * plan.k_blocks * plan.block_n;
+    return rows < (int64_t(1) << 31) ? rows : -1;
+}
+
+proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packed, const void *bias,
+                       void *Y, void *stream);
+
+}  // namespace
+
+extern "C" {
+
 proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void *bias, void *Y,
                        void *stream) {
+    return run_impl(h, X, W, false, bias, Y, stream);
+}
+
+proj_status_t proj_run_packed(proj_handle_t h, const void *X, const void *W_packed, const void *bias,
+                              void *Y, void *stream) {
+    return run_impl(h, X, W_packed, true, bias, Y, stream);
+}
+
+proj_status_t proj_packed_weight_bytes(proj_handle_t h, size_t *bytes) {
+    if (!h || !bytes) return PROJ_ERR_INVALID_ARG;
+    *bytes = 0;
+    if (h->plan.kernel != PROJ_KERNEL_TC) return PROJ_OK;
+    const int64_t rows = packed_rows(h->plan);
+    if (rows < 0) return PROJ_ERR_UNSUPPORTED;
+    *bytes = static_cast<size_t>(rows) * 128;
+    return PROJ_OK;
+}
+
+proj_status_t proj_pack_weights(proj_handle_t h, const void *W, void *W_packed, void *stream) {
+    if (!h) return PROJ_ERR_INVALID_ARG;
+    const proj_plan_desc_t &plan = h->plan;
+    if (plan.kernel != PROJ_KERNEL_TC) return PROJ_OK;
+    if (!W || !W_packed) return PROJ_ERR_INVALID_ARG;
+    if (!aligned16(W) || !aligned16(W_packed)) return PROJ_ERR_MISALIGNED;
+    const int64_t rows = packed_rows(plan);
+    if (rows < 0) return PROJ_ERR_UNSUPPORTED;
+    const int64_t chunks = rows * 8;  // 16-byte chunks
+    const int64_t want = (chunks + 255) / 256;
+    const int blocks = static_cast<int>(want < int64_t(h->sm_count) * 16 ? want : int64_t(h->sm_count) * 16);
+    dev::proj_pack_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
+        static_cast<const uint16_t *>(W), static_cast<uint16_t *>(W_packed), h->N, h->K,
+        h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, chunks);
+    return check_launch();
+}
+
+}  // extern "C"
+
+namespace {
+
+proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packed, const void *bias,
+                       void *Y, void *stream) {
     if (!h) return PROJ_ERR_INVALID_ARG;
     if ((bias != nullptr) != (h->has_bias != 0)) return PROJ_ERR_INVALID_ARG;
     const proj_plan_desc_t &plan = h->plan;
@@ -342,7 +403,17 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
         }
         h->map_x_ptr = X;
     }
-    if (W != h->map_w_ptr) {
+    if (packed) {
+        if (W != h->map_wp_ptr) {
+            const int64_t rows = packed_rows(plan);
+            if (rows < 0) return PROJ_ERR_UNSUPPORTED;
+            if (!encode_2d(&h->map_wp, W, 64, static_cast<uint64_t>(rows), 128, kBlockK, plan.block_n)) {
+                h->map_wp_ptr = nullptr;
+                return PROJ_ERR_CUDA;
+            }
+            h->map_wp_ptr = W;
+        }
+    } else if (W != h->map_w_ptr) {
         const bool ok = h->w_layout == PROJ_W_NK
                             ? encode_2d(&h->map_w, W, h->K, h->N, h->K * 2, kBlockK, plan.block_n)
                             : encode_2d(&h->map_w, W, h->N, h->K, h->N * 2, 64, kBlockK);
@@ -353,6 +424,12 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
         h->map_w_ptr = W;
     }
     KernelParams kp = h->params;
+    if (packed) {
+        // Packed weights are K-major blocks whatever the stored layout.
+        kp.w_packed = 1;
+        kp.w_kn = 0;
+        kp.idesc = idesc_of(plan, PROJ_W_NK);
+    }
     kp.bias = static_cast<const uint16_t *>(bias);
     kp.Y = Y;
     kp.y_vec = y_vec_of(Y, h->N, h->y_dtype);
@@ -364,15 +441,38 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
     kp.w_prefetch =
         h->overlap == PROJ_OVERLAP_WEIGHTS && plan.grid >= h->sm_count ? h->prefetch_stages : 0;
     TcLaunch l(plan, s, h->overlap != PROJ_OVERLAP_NONE);
-    if (cudaLaunchKernelEx(&l.cfg, dev::proj_tc_kernel, kp, h->map_w, h->map_x) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&l.cfg, dev::proj_tc_kernel, kp, packed ? h->map_wp : h->map_w, h->map_x) !=
+        cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }
     return PROJ_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+namespace {
+proj_status_t run_host_impl(proj_handle_t h, const void *X_host, const void *W, bool packed,
+                            const void *bias, void *Y_host, void *stream);
+}  // namespace
+
 proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W, const void *bias,
                             void *Y_host, void *stream) {
+    return run_host_impl(h, X_host, W, false, bias, Y_host, stream);
+}
+
+proj_status_t proj_run_host_packed(proj_handle_t h, const void *X_host, const void *W_packed,
+                                   const void *bias, void *Y_host, void *stream) {
+    return run_host_impl(h, X_host, W_packed, true, bias, Y_host, stream);
+}
+
+}  // extern "C"
+
+namespace {
+proj_status_t run_host_impl(proj_handle_t h, const void *X_host, const void *W, bool packed,
+                            const void *bias, void *Y_host, void *stream) {
     if (!h) return PROJ_ERR_INVALID_ARG;
     if (h->plan.kernel == PROJ_KERNEL_NONE) return PROJ_OK;
     if (!Y_host || (!X_host && h->K > 0)) return PROJ_ERR_INVALID_ARG;
@@ -393,12 +493,15 @@ proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W, 
     cudaStream_t s = as_stream(stream);
     if (xb && cudaMemcpyAsync(h->stage_x, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return PROJ_ERR_CUDA;
-    proj_status_t st = proj_run(h, h->stage_x, W, bias, h->stage_y, stream);
+    proj_status_t st = run_impl(h, h->stage_x, W, packed, bias, h->stage_y, stream);
     if (st != PROJ_OK) return st;
     if (cudaMemcpyAsync(Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return PROJ_ERR_CUDA;
     return PROJ_OK;
 }
+}  // namespace
+
+extern "C" {
 
 proj_status_t proj_device_status(proj_handle_t h, void *stream) {
     if (!h) return PROJ_ERR_INVALID_ARG;

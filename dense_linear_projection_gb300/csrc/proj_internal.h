@@ -105,6 +105,7 @@ struct KernelParams {
     int32_t tmem_cols;
     uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128, N=b_rows)
     int32_t w_kn;          // W stored [K,N] (MN-major A operand)
+    int32_t w_packed;      // W pre-packed: block (tile, k-block) at row (tn·k_blocks + kb)·block_n
     int32_t y_f32;         // store fp32 (else bf16)
     int32_t y_vec;         // Y rows start 16-byte aligned (N·size % 16 == 0, aligned base)
     int64_t wait_limit_ns; // bounded device waits give up after this long

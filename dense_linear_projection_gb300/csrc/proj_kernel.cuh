@@ -494,7 +494,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // [N,K] weights; for [K,N] weights, block_n/64 boxes of 64 N-rows
             // x 64 K, 8 KiB apart (the MN-major operand layout).
             auto load_w = [&](uint32_t dst, uint32_t full, int32_t tn, int32_t kb) {
-                if (!p.w_kn) {
+                if (p.w_packed) {
+                    // Pre-packed: the stage is one contiguous block of block_n
+                    // rows x 128 bytes (a 2-D map of 64-wide rows).
+                    tma_load_2d(dst, &tmap_w, full, 0, (tn * p.k_blocks + kb) * p.block_n, pol_w);
+                } else if (!p.w_kn) {
                     tma_load_2d(dst, &tmap_w, full, kb * kBlockK, tn * p.block_n, pol_w);
                 } else {
                     for (int32_t j = 0; j < p.block_n / 64; ++j)
@@ -1071,6 +1075,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+    }
+}
+
+// Weight packing (preparation, not part of a run): packed block (tn, kb) holds
+// rows tn·block_n + r, r < block_n, and K positions kb·64 + c, c < 64, K
+// contiguous; positions past N or K are zero.  One thread writes 16 bytes (8
+// values).  [N,K] weights: consecutive threads take consecutive K chunks of a
+// row (contiguous reads); [K,N] weights: consecutive threads take consecutive
+// rows of one K chunk (contiguous reads along N).
+__global__ void proj_pack_kernel(const uint16_t *W, uint16_t *P, int64_t N, int64_t K, int w_kn,
+                                 int32_t block_n, int64_t k_blocks, int64_t chunks) {
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < chunks;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int64_t blk, r, c8;
+        if (!w_kn) {
+            c8 = e & 7;
+            const int64_t row = e >> 3;
+            blk = row / block_n;
+            r = row - blk * block_n;
+        } else {
+            const int64_t per_blk = static_cast<int64_t>(block_n) * 8;
+            blk = e / per_blk;
+            const int64_t rem = e - blk * per_blk;
+            c8 = rem / block_n;
+            r = rem - c8 * block_n;
+        }
+        const int64_t tn = blk / k_blocks;
+        const int64_t kb = blk - tn * k_blocks;
+        const int64_t n = tn * block_n + r;
+        const int64_t k0 = kb * 64 + c8 * 8;
+        uint4 out = make_uint4(0u, 0u, 0u, 0u);
+        if (n < N && k0 < K) {  // K % 8 == 0: the 8 values are all in range
+            if (!w_kn) {
+                out = *reinterpret_cast<const uint4 *>(W + n * K + k0);
+            } else {
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    w[j] = static_cast<uint32_t>(W[(k0 + 2 * j) * N + n]) |
+                           (static_cast<uint32_t>(W[(k0 + 2 * j + 1) * N + n]) << 16);
+                out = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+        *reinterpret_cast<uint4 *>(P + ((blk * block_n + r) * 64 + c8 * 8)) = out;
     }
 }
 

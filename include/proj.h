@@ -219,6 +219,39 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
                        void *Y, void *stream);
 
 /*
+ * Pre-packed weights, a preparation step outside the timed call.  The
+ * worklog's contract let preparation pack fixed weights (section "Preparation
+ * is not secretly computing the answer"), and its C2 experiments kept each
+ * output tile's weights next to each other in memory (section "Sometimes
+ * moving the same numbers around was enough").
+ *
+ * The handle's packed layout is one block per (weight tile t, k-block b), in
+ * the order t·k_blocks + b.  Each block holds block_n rows × 64 K values in
+ * bf16, K contiguous (128 bytes a row).  Rows at or past N and K positions at
+ * or past K are zero.  Every pipeline stage of a packed run then reads one
+ * contiguous block of block_n × 128 bytes, and [K,N] weights become K-major.
+ * The layout follows the plan's block_n, so packed weights are used with the
+ * handle that packed them (or one with the same plan).
+ *
+ * proj_packed_weight_bytes: the packed size, tiles_n · k_blocks · block_n ·
+ *   128 bytes (0 for plans without the tensor-core kernel).
+ *   PROJ_ERR_UNSUPPORTED if the packed rows would not fit 31-bit coordinates.
+ * proj_pack_weights: W (device, the handle's layout) → W_packed (device,
+ *   proj_packed_weight_bytes bytes, 16-byte aligned, caller-owned), enqueued
+ *   on `stream`.  W must not overlap W_packed.
+ * proj_run_packed: proj_run with packed weights; same arguments otherwise.
+ * PROJ_ERR_INVALID_ARG for NULL handles or pointers, PROJ_ERR_MISALIGNED for
+ * unaligned pointers, PROJ_ERR_CUDA if a launch fails.
+ */
+proj_status_t proj_packed_weight_bytes(proj_handle_t h, size_t *bytes);
+proj_status_t proj_pack_weights(proj_handle_t h, const void *W, void *W_packed, void *stream);
+proj_status_t proj_run_packed(proj_handle_t h, const void *X, const void *W_packed,
+                              const void *bias, void *Y, void *stream);
+/* proj_run_host with packed weights (W_packed on the device). */
+proj_status_t proj_run_host_packed(proj_handle_t h, const void *X_host, const void *W_packed,
+                                   const void *bias, void *Y_host, void *stream);
+
+/*
  * Same projection with HOST activations: copies X_host ([M,K] bf16) to a
  * device staging buffer, runs, and copies Y back to Y_host, all on `stream`.
  * W and bias stay device pointers (weights are resident, as after a
