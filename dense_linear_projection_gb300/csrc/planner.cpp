@@ -171,14 +171,17 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // (weight-streaming) plans, 80 % for the tensor-bound token-major plans,
     // whose split partial tiles are large.
     //
-    // Cluster split: fewer (swapped, narrow) tiles than SMs, each split along
-    // K over the S CTAs of one thread-block cluster whose partial sums meet in
-    // distributed shared memory (no global scratch, no atomics).  Used when
-    // the clusters keep at least cluster_fill_pct (60) % of the SMs busy:
-    // measured on GB300 for 16 tiles of 16 tokens x 128 rows x K = 8192,
-    // clusters of 6 on 96 SMs beat stream-K over all 152 (13.6 vs 14.3 us).
+    // Cluster split: far fewer (swapped, narrow) tiles than SMs, each split
+    // along K over the S CTAs of one thread-block cluster whose partial sums
+    // meet in distributed shared memory (no global scratch, no atomics).
+    // Stream-K over every SM wins while a split tile has about three
+    // contributors or fewer (3·tiles >= SMs); below that its fixups cost more
+    // than the idle SMs of a cluster split.  Measured on GB300 with packed
+    // weights, K = 8192, 16 tokens: 64 tiles, stream-K 25.2 us vs clusters of
+    // 2 26.2 us; 16 tiles, clusters of 6 on 96 SMs 12.6 us vs stream-K 13.4 us.
+    // The clusters must keep at least cluster_fill_pct (60) % of the SMs busy.
     int32_t S = 0;
-    if (swap && opt.max_cluster >= 2 && tiles < sms && b_rows <= 64) {
+    if (swap && opt.max_cluster >= 2 && 3 * tiles < sms && b_rows <= 64) {
         int64_t s_try = sms / tiles;
         if (s_try > opt.max_cluster) s_try = opt.max_cluster;
         if (s_try > out->k_blocks) s_try = out->k_blocks;

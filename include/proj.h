@@ -111,8 +111,9 @@ typedef struct proj_device_desc {
  * section "My first useful win: split up the sum"; CTA c takes units
  * [⌊c·U/G⌋, ⌊(c+1)·U/G⌋), the integer partition of section "Why the later
  * TMA/WGMMA kernel was a new experiment" that splits 128 tiles 42/43/43).
- * Cluster split instead (cluster_split = S ≥ 2): when fewer narrow swapped
- * tiles than SMs exist and S CTAs per tile keep at least 60 % of the SMs busy,
+ * Cluster split instead (cluster_split = S ≥ 2): when there are fewer than a
+ * third as many narrow swapped tiles as SMs (stream-K would give a tile more
+ * than three contributors) and S CTAs per tile keep at least 60 % of the SMs busy,
  * each tile gets its own cluster of S CTAs, grid = tiles_sk · S, and the
  * partial sums meet in distributed shared memory; no partial-sum scratch and
  * no counters.

@@ -149,25 +149,25 @@ def test_plans_of_the_workloads(M, N, K, layout):
 
 
 def test_cluster_split_plans():
-    # Decode shapes with fewer 128-row weight tiles than SMs: 64 tiles in
-    # clusters of 2 (128 CTAs), 16 tiles in clusters of 8 (128 CTAs).
-    for (N, S) in ((8192, 2), (2048, 8)):
+    # 16 tiles of the 2048-row decode weight: clusters of 8 (128 CTAs).
+    p = plan(16, 2048, 8192)
+    assert (p["cluster_split"], p["grid"], p["tiles_sk"], p["tiles_dp"]) == (8, 128, 16, 0)
+    assert dlp.proj_plan_reduction_order(p, 3) == [(3 * 8 + r, -1) for r in range(8)]
+    # 64 tiles of the 8192-row decode weight: stream-K over every SM (a split
+    # tile has about 2.4 contributors), as for the 28672-row FFN weight.
+    for N in (8192, 28672):
         p = plan(16, N, 8192)
-        assert (p["cluster_split"], p["grid"], p["tiles_sk"], p["tiles_dp"]) == (S, 128, 128 // S, 0)
-        assert dlp.proj_plan_reduction_order(p, 3) == [(3 * S + r, -1) for r in range(S)]
-    # Enough tiles for every SM (the 28672-row FFN weight): no clusters.
-    assert plan(16, 28672, 8192)["cluster_split"] == 0
-    # 77 or more tiles leave no room for two CTAs each: stream-K; 76 tiles
-    # take clusters of 2 on every SM; 45 tiles clusters of 3 (135 SMs).
-    p = plan(16, 100 * 128, 8192)
-    assert p["cluster_split"] == 0 and p["tiles_sk"] == 100
-    assert plan(16, 77 * 128, 8192)["cluster_split"] == 0
-    assert plan(16, 76 * 128, 8192)["cluster_split"] == 2
+        assert p["cluster_split"] == 0 and p["grid"] == 152
+    # Clusters only below a third of the SMs in tiles: 50 tiles (3·50 < 152)
+    # take clusters of 3 on 150 SMs; 51 tiles stream-K; 45 tiles clusters of 3.
+    assert plan(16, 50 * 128, 8192)["cluster_split"] == 3
+    assert plan(16, 51 * 128, 8192)["cluster_split"] == 0
     assert plan(16, 45 * 128, 8192)["cluster_split"] == 3
-    # Below 60 % of the SMs (8 SMs, 3 tiles: clusters of 2 on 6 SMs = 75 %,
-    # 5 tiles of one CTA each on 5 SMs: no split possible).
-    assert plan(16, 3 * 128, 8192, sm_count=8, smem_optin_bytes=232448)["cluster_split"] == 2
-    assert plan(16, 5 * 128, 8192, sm_count=8, smem_optin_bytes=232448)["cluster_split"] == 0
+    # Below 60 % of the SMs (12 SMs, 3 tiles: clusters of 4 on 12 SMs; 8 SMs
+    # and 2 tiles: clusters of 4 on 8 SMs; 5 SMs, 1 tile: clusters of 5).
+    assert plan(16, 3 * 128, 8192, sm_count=12, smem_optin_bytes=232448)["cluster_split"] == 4
+    assert plan(16, 2 * 128, 8192, sm_count=8, smem_optin_bytes=232448)["cluster_split"] == 4
+    assert plan(16, 128, 8192, sm_count=5, smem_optin_bytes=232448)["cluster_split"] == 5
     # S is capped by the k-blocks there are to share (5 SMs, 1 tile, 4 k-blocks).
     p = plan(16, 128, 256, sm_count=5, smem_optin_bytes=232448)
     assert p["k_blocks"] == 4 and p["cluster_split"] == 4 and p["grid"] == 4

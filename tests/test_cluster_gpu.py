@@ -25,7 +25,7 @@ CLUSTER_SHAPES = [
     (16, 3304, 1032, synth.W_KN, True, "bf16", 5),   # [K,N] weights, 26 tiles x 5
     (16, 4000, 2056, synth.W_NK, True, "bf16", 4),   # 32 tiles x 4, ragged K block
     (12, 5300, 1032, synth.W_NK, False, "f32", 3),   # 42 tiles x 3
-    (16, 8192, 8192, synth.W_NK, True, "bf16", 2),   # the decode projection: 64 tiles x 2
+    (16, 6144, 8192, synth.W_NK, True, "bf16", 3),   # 48 tiles x 3 (x 2 where 48 clusters of 3 do not fit)
     (100, 1024, 8192, synth.W_NK, True, "bf16", 8),  # two 64-token tiles x 8 weight tiles
 ]
 
@@ -86,13 +86,16 @@ def test_every_cluster_size(S, M, N, K, layout, bias, yd, monkeypatch):
 
 
 def test_handle_keeps_only_clusters_that_fit():
-    # One CTA per SM: the 64 clusters of 2 of the 8192-row decode projection
-    # fit at once, and the handle keeps them.  Whatever split size a handle
-    # ends with, all of its clusters fit the device together.
+    # The 8192-row decode projection (64 tiles) runs stream-K on every SM; the
+    # 2048-row one (16 tiles) keeps a cluster split whose clusters all fit at
+    # once.  Whatever split size a handle ends with, its clusters fit together.
     import torch
     import dense_linear_projection_gb300 as dlp
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     proj = dlp.Projection(16, 8192, 8192, dlp.PROJ_W_NK, dlp.PROJ_BF16, has_bias=True)
-    assert proj.plan["cluster_split"] == 2 and proj.plan["grid"] == 128
+    assert proj.plan["cluster_split"] == 0 and proj.plan["grid"] == sms
+    p = dlp.Projection(16, 2048, 8192, dlp.PROJ_W_NK, dlp.PROJ_F32).plan
+    assert p["cluster_split"] >= 2 and p["grid"] == 16 * p["cluster_split"]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     for N in (2048, 2500, 3304, 4000, 5300):
         p = dlp.Projection(16, N, 8192, dlp.PROJ_W_NK, dlp.PROJ_BF16).plan
@@ -120,7 +123,7 @@ def test_cluster_split_graph_replay_follows_fresh_inputs():
     # Replays of a captured cluster launch: each replay reads the X it is given.
     import torch
     import dense_linear_projection_gb300 as dlp
-    w = synth.Workload("t", 16, 8192, 8192, synth.W_NK, True, "bf16", 62)
+    w = synth.Workload("t", 16, 2048, 8192, synth.W_NK, True, "bf16", 62)
     inp = synth.make_inputs(w)
     proj, Y, (X, W, b) = gu.run(w, inp)
     assert proj.plan["cluster_split"] >= 2

@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("M,N,K,layout,bias,yd", [
-    (16, 8192, 8192, synth.W_NK, True, "bf16"),   # decode shape: tiles split over clusters
-    (16, 2048, 8192, synth.W_NK, False, "f32"),   # many contributors per split tile
+    (16, 8192, 8192, synth.W_NK, True, "bf16"),   # decode shape: stream-K over every SM
+    (16, 2048, 8192, synth.W_NK, False, "f32"),   # 16 tiles split over clusters
     (16, 28672, 1024, synth.W_NK, True, "bf16"),  # 224 tiles: split-K through the scratch
     (3, 520, 1032, synth.W_KN, True, "bf16"),     # [K,N] weights, ragged edges
     (256, 19456, 256, synth.W_NK, False, "bf16"), # 152 whole tiles, one wave: no split scratch
