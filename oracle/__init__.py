@@ -64,6 +64,12 @@ def _lib():
         lib.oracle_project_cells.argtypes = [i64, i64, i64, vp, vp, ctypes.c_int, vp,
                                              i64, vp, vp, vp]
         lib.oracle_project_cells.restype = None
+        lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.oracle_split_hilo.argtypes = [i64, vp, vp, vp]
+        lib.oracle_split_hilo.restype = None
+        lib.oracle_project_f32w.argtypes = [i64, i64, i64, vp, vp, ctypes.c_int, vp, vp]
+        lib.oracle_project_f32w.restype = None
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _LIB = lib
@@ -130,6 +136,50 @@ def project_cells(X, W, w_layout: int, bias, ms, ns) -> np.ndarray:
                                     ms.size, ms.ctypes.data, ns.ctypes.data,
                                     out.ctypes.data)
     return out
+
+
+def f32_to_bf16(values) -> np.ndarray:
+    """bf16 bit patterns of fp32 values, through the oracle's own rounding (RNE)."""
+    lib = _lib()
+    flat = np.asarray(values, dtype=np.float32).ravel()
+    return np.array([lib.oracle_f32_to_bf16(float(v)) for v in flat],
+                    dtype=np.uint16).reshape(np.shape(values))
+
+
+def split_hilo(W) -> tuple:
+    """The router's high and low bf16 parts of fp32 weights (any shape):
+    H = roundBF16(W), L = roundBF16(W − FP32(H)), as uint16 bit patterns."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    H = np.empty(W.shape, dtype=np.uint16)
+    L = np.empty(W.shape, dtype=np.uint16)
+    if W.size:
+        _lib().oracle_split_hilo(W.size, W.ctypes.data, H.ctypes.data, L.ctypes.data)
+    return H, L
+
+
+def project_f32w(X, W, w_layout: int = W_NK, bias=None) -> np.ndarray:
+    """fp64 ``Y = X·Wᵀ (+ bias)`` with fp32 weights ``W`` (the router's reference)."""
+    X = _u16(X)
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    M, K = X.shape
+    if w_layout == W_NK:
+        N, K2 = W.shape
+    else:
+        K2, N = W.shape
+    if K2 != K:
+        raise ValueError(f"K mismatch: X has {K}, W has {K2}")
+    b = None if bias is None else _u16(bias)
+    Y = np.empty((M, N), dtype=np.float64)
+    if M and N:
+        _lib().oracle_project_f32w(M, N, K, X.ctypes.data, W.ctypes.data, int(w_layout),
+                                   None if b is None else b.ctypes.data, Y.ctypes.data)
+    return Y
+
+
+def project_hilo(X, W, w_layout: int = W_NK, bias=None) -> np.ndarray:
+    """The router method itself in fp64: X·Hᵀ + X·Lᵀ (+ bias)."""
+    H, L = split_hilo(W)
+    return project(X, H, w_layout, bias) + project(X, L, w_layout, None)
 
 
 def max_threads() -> int:

@@ -81,6 +81,66 @@ void oracle_project_cells(int64_t M, int64_t N, int64_t K, const uint16_t *X,
         out[i] = cell(N, K, X, W, w_layout, bias, ms[i], ns[i]);
 }
 
+/* ------------------------------------------------------------------------
+ * FP32 router weights ("How I made Muse's GPU projections 1.32× faster in the
+ * Open Kernel Challenge", section "Why the high-plus-low router scheme
+ * helped"): the weight is fp32, and the method keeps a bf16 high part and a
+ * bf16 low part of it:
+ *
+ *     H = roundBF16(W),  R = W − FP32(H),  L = roundBF16(R),  X·Wᵀ ≈ X·Hᵀ + X·Lᵀ.
+ *
+ * roundBF16 is round to nearest, ties to even (section "What a floating-point
+ * number is approximating": bf16 keeps 7 of fp32's 23 fraction bits).  The
+ * residual R is an fp32 subtraction, as the section writes it.
+ * ------------------------------------------------------------------------ */
+
+/* fp32 → bf16 bits, round to nearest, ties to even.  A NaN stays a (quiet)
+ * NaN.  Rounding adds just under half of the dropped 16 bits' range, plus one
+ * more when the kept part is odd, then drops them: ties go to even. */
+uint16_t oracle_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    const uint32_t keep_odd = (u >> 16) & 1u;
+    u += 0x7FFFu + keep_odd;
+    return (uint16_t)(u >> 16);
+}
+
+/* H and L for `count` fp32 weights (any layout: element by element). */
+void oracle_split_hilo(int64_t count, const float *W, uint16_t *H, uint16_t *L) {
+    for (int64_t i = 0; i < count; ++i) {
+        const uint16_t h = oracle_f32_to_bf16(W[i]);
+        const float h32 = (float)oracle_bf16_to_double(h);
+        const float r = W[i] - h32;
+        H[i] = h;
+        L[i] = oracle_f32_to_bf16(r);
+    }
+}
+
+/* The router's reference: the exact product with the fp32 weight, in fp64
+ * (each bf16 × fp32 product has at most 8 + 24 significant bits: exact). */
+static double cell_f32w(int64_t N, int64_t K, const uint16_t *X, const float *W,
+                        int w_layout, const uint16_t *bias, int64_t m, int64_t n) {
+    double acc = 0.0;
+    for (int64_t kk = 0; kk < K; ++kk) {
+        const double w = (double)(w_layout == 0 ? W[n * K + kk] : W[kk * N + n]);
+        acc += oracle_bf16_to_double(X[m * K + kk]) * w;
+    }
+    if (bias)
+        acc += oracle_bf16_to_double(bias[n]);
+    return acc;
+}
+
+void oracle_project_f32w(int64_t M, int64_t N, int64_t K, const uint16_t *X,
+                         const float *W, int w_layout, const uint16_t *bias,
+                         double *Y) {
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            Y[m * N + n] = cell_f32w(N, K, X, W, w_layout, bias, m, n);
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -1,8 +1,9 @@
 """The oracle's pins catch plausible mistakes.
 
 Each case plants one mistake in a copy of oracle.c (on the CPU), builds it, and
-runs the pin suite (test_oracle.py) against it in a subprocess: the suite must
-fail.  The real oracle passing the same suite is test_oracle.py itself.
+runs the pin suites (test_oracle.py, test_oracle_router.py) against it in a
+subprocess: they must fail.  The real oracle passing the same suites is those
+files themselves.
 """
 import os
 import subprocess
@@ -30,6 +31,16 @@ MUTANTS = {
     "bias_dropped": ("if (bias)\n", "if (0)\n"),
     "decode_shift": ("(uint32_t)b << 16", "(uint32_t)b << 15"),
     "output_transposed": ("Y[m * N + n] = cell", "Y[n * M + m] = cell"),
+    # fp32 router weights: rounding, the high/low split, the fp32-weight product.
+    "rne_truncates": ("u += 0x7FFFu + keep_odd;", "u += 0u * keep_odd;"),
+    "rne_ties_away": ("u += 0x7FFFu + keep_odd;", "u += 0x8000u + 0u * keep_odd;"),
+    "low_from_weight": ("const float r = W[i] - h32;", "const float r = W[i] + 0.0f * h32;"),
+    "low_dropped": ("L[i] = oracle_f32_to_bf16(r);", "L[i] = 0;"),
+    "f32w_rounded_to_bf16": (
+        "const double w = (double)(w_layout == 0 ? W[n * K + kk] : W[kk * N + n]);",
+        "const double w = oracle_bf16_to_double(oracle_f32_to_bf16("
+        "w_layout == 0 ? W[n * K + kk] : W[kk * N + n]));"),
+    "f32w_layout_ignored": ("(w_layout == 0 ? W[n * K + kk] : W[kk * N + n])", "(W[n * K + kk])"),
 }
 
 
@@ -46,6 +57,7 @@ def test_pins_fail_on_mutant(name):
                         "-o", so, c], check=True)
         env = dict(os.environ, ORACLE_LIB=so)
         r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-                            os.path.join(HERE, "test_oracle.py")],
+                            os.path.join(HERE, "test_oracle.py"),
+                            os.path.join(HERE, "test_oracle_router.py")],
                            cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
         assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
