@@ -210,6 +210,15 @@ def visible_gpu_id(local_rank: int) -> str:
 
 
 # ---------------------------------------------------------------- CPU oracle
+def _oracle_project(w, X, W, bias):
+    """The oracle's product for workload ``w``: bf16 weights, or the exact
+    fp32-weight product for router weights."""
+    import oracle
+    if w.w_dtype == "f32":
+        return oracle.project_f32w(X, W, w.w_layout, bias)
+    return oracle.project(X, W, w.w_layout, bias)
+
+
 def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None) -> dict:
     """Time the fp64 oracle on the host cores on a bounded sample of the
     workload: all M token rows against the first n_cols output columns (or the
@@ -229,7 +238,7 @@ def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None) -> dict:
     probe = min(w.N, 64)
     Wp, bp = cols_slice(probe)
     t0 = time.perf_counter()
-    oracle.project(X[: min(w.M, 256)], Wp, w.w_layout, bp)
+    _oracle_project(w, X[: min(w.M, 256)], Wp, bp)
     dt = max(time.perf_counter() - t0, 1e-6)
     per_col = dt / probe * (w.M / min(w.M, 256))
     n_cols = int(max(1, min(w.N, target_s / per_col)))
@@ -239,7 +248,7 @@ def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None) -> dict:
     Ws, bs = cols_slice(n_cols)
     t0 = time.perf_counter()
     for _ in range(reps):
-        r = oracle.project(X, Ws, w.w_layout, bs)
+        r = _oracle_project(w, X, Ws, bs)
     elapsed = time.perf_counter() - t0
     wbytes = 2.0 * n_cols * w.K * reps
     sample = (f"all {w.M} token rows x {n_cols} of {w.N} output columns"
@@ -275,8 +284,12 @@ def run_gpu_arm(args) -> dict:
     def dev_bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
 
-    X, W0 = dev_bf16(inp["X"]), dev_bf16(inp["W"])
+    X = dev_bf16(inp["X"])
+    fp32_w = w.w_dtype == "f32"  # router weights: packed runs only (high/low split)
+    W0 = torch.from_numpy(np.ascontiguousarray(inp["W"])).to(device) if fp32_w else dev_bf16(inp["W"])
     bias = dev_bf16(inp["bias"]) if w.has_bias else None
+    if fp32_w and not args.packed:
+        raise SystemExit("fp32 router weights run only packed (the split is the packing)")
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     n_copies = max(2, math.ceil(2 * l2 / w.weight_bytes) + 1)
     Ws = [W0] + [W0.clone() for _ in range(n_copies - 1)]
@@ -290,7 +303,7 @@ def run_gpu_arm(args) -> dict:
                "weights": dlp.PROJ_OVERLAP_WEIGHTS}[args.overlap]
     proj = dlp.Projection(w.M, w.N, w.K, w.w_layout,
                           dlp.PROJ_F32 if w.y_dtype == "f32" else dlp.PROJ_BF16, w.has_bias,
-                          overlap=overlap)
+                          overlap=overlap, w_dtype=dlp.PROJ_F32 if fp32_w else dlp.PROJ_BF16)
     stream = torch.cuda.Stream(device)
     # Weights packed once per copy into the handle's tile-contiguous layout:
     # the preparation step, outside every timed region.
@@ -392,14 +405,18 @@ def run_gpu_arm(args) -> dict:
     # ---- Informational: the same projection through cuBLAS (torch), never the target.
     library = None
     if args.library:
-        Yl = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+        # bf16 weights: bf16 GEMM, bf16 output; fp32 router weights: fp32 GEMM
+        # of X cast to fp32 (torch keeps TF32 off for matmul by default).
+        Xl = X.float() if fp32_w else X
+        bl = None if bias is None else (bias.float() if fp32_w else bias)
+        Yl = torch.empty((w.M, w.N), dtype=torch.float32 if fp32_w else torch.bfloat16, device=device)
 
         def lib_call(Wc):
             Wm = Wc.t() if w.w_layout == 0 else Wc
-            if bias is not None:
-                torch.addmm(bias, X, Wm, out=Yl)
+            if bl is not None:
+                torch.addmm(bl, Xl, Wm, out=Yl)
             else:
-                torch.mm(X, Wm, out=Yl)
+                torch.mm(Xl, Wm, out=Yl)
 
         with torch.cuda.stream(stream):
             lib_call(W0)
@@ -419,7 +436,8 @@ def run_gpu_arm(args) -> dict:
             b_.record(stream)
         torch.cuda.synchronize()
         t_lib = a.elapsed_time(b_) / 1e3 / l_steps
-        library = {"impl": "torch.addmm / torch.mm (cuBLAS), bf16 output", "steps": l_steps,
+        library = {"impl": ("torch.mm (cuBLAS fp32 GEMM, X cast to fp32), fp32 output" if fp32_w
+                            else "torch.addmm / torch.mm (cuBLAS), bf16 output"), "steps": l_steps,
                    "us_per_call": t_lib * 1e6, "value": w.weight_bytes / t_lib / 1e9, "unit": "GB/s",
                    "note": "informational; same inputs, W rotation and CUDA-graph replay"}
         del Yl, gl
@@ -495,7 +513,7 @@ def run_gpu_arm(args) -> dict:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16 (fp32 weights as high/low bf16 parts)" if fp32_w else "bf16",
         "data": "synthetic (seeded SplitMix64/Box-Muller normals, bf16)",
         "config": {
             "workload": w.name, "M": w.M, "N": w.N, "K": w.K,
@@ -547,17 +565,17 @@ def run_reference_arm(args) -> dict:
     probe = min(w.N, 32)
     Wp = W[:probe] if w.w_layout == 0 else np.ascontiguousarray(W[:, :probe])
     t0 = time.perf_counter()
-    oracle.project(X, Wp, w.w_layout, None if b is None else b[:probe])
+    _oracle_project(w, X, Wp, None if b is None else b[:probe])
     per_col = max(time.perf_counter() - t0, 1e-6) / probe
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
     n_cols = int(max(1, min(w.N, budget / per_col)))
     Ws = W[:n_cols] if w.w_layout == 0 else np.ascontiguousarray(W[:, :n_cols])
     bs = None if b is None else b[:n_cols]
     for _ in range(args.warmup):
-        oracle.project(X, Ws, w.w_layout, bs)
+        _oracle_project(w, X, Ws, bs)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.project(X, Ws, w.w_layout, bs)
+        _oracle_project(w, X, Ws, bs)
     elapsed = time.perf_counter() - t0
     value = 2.0 * n_cols * w.K * args.steps / elapsed / 1e9
     sample = f"each step: all {w.M} token rows x {n_cols} of {w.N} output columns"
@@ -592,7 +610,8 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    help="decode_f32out | decode_bias | ffn_up_sweep | qkv_kn_bias | prefill")
+                    help="decode_f32out | decode_bias | ffn_up_sweep | qkv_kn_bias | prefill"
+                         " | router_f32w")
     ap.add_argument("--m", type=int, default=None, help="token rows (overrides the workload's M)")
     ap.add_argument("--soak", type=float, default=1.0,
                     help="seconds of untimed load before timing (clock sampling)")

@@ -292,11 +292,12 @@ class Projection:
 
     def __init__(self, M: int, N: int, K: int, w_layout: int = PROJ_W_NK,
                  y_dtype: int = PROJ_BF16, has_bias: bool = False, stream=None,
-                 overlap: Optional[int] = None):
+                 overlap: Optional[int] = None, w_dtype: int = PROJ_BF16):
         import torch  # noqa: F401  (PyTorch provides memory and streams only)
         self.M, self.N, self.K = M, N, K
         self.w_layout, self.y_dtype, self.has_bias = w_layout, y_dtype, bool(has_bias)
-        self.handle = proj_create(M, N, K, w_layout, PROJ_BF16, PROJ_BF16, y_dtype, has_bias,
+        self.w_dtype = w_dtype
+        self.handle = proj_create(M, N, K, w_layout, PROJ_BF16, w_dtype, y_dtype, has_bias,
                                   PROJ_BF16, stream)
         if overlap is not None:
             proj_set_overlap(self.handle, overlap)
@@ -318,7 +319,9 @@ class Projection:
 
     def pack(self, W, stream=None):
         """Repack weights into this handle's tile-contiguous layout (a preparation
-        step); returns a new bf16 CUDA tensor to pass with ``packed=True``."""
+        step; fp32 weights of a ``w_dtype=PROJ_F32`` handle are split into high
+        and low bf16 parts here); returns a new bf16 CUDA tensor to pass with
+        ``packed=True``."""
         import torch
         n = proj_packed_weight_bytes(self.handle)
         P = torch.empty(max(n // 2, 8), dtype=torch.bfloat16, device=W.device)

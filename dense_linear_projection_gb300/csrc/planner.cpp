@@ -178,8 +178,11 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // contributors or fewer (3·tiles >= SMs); below that its fixups cost more
     // than the idle SMs of a cluster split.  Measured on GB300 with packed
     // weights, K = 8192, 16 tokens: 64 tiles, stream-K 25.2 us vs clusters of
-    // 2 26.2 us; 16 tiles, clusters of 6 on 96 SMs 12.6 us vs stream-K 13.4 us.
-    // The clusters must keep at least cluster_fill_pct (60) % of the SMs busy.
+    // 2 26.2 us; 16 tiles, clusters of 6 on 96 SMs 12.6 us vs stream-K 13.4 us;
+    // the 2 tiles of a 256-row router weight, clusters of 8 on 16 SMs 14.6 us vs
+    // 16.3 us for stream-K at its best grid.  S goes up to 16 (a non-portable
+    // cluster size); the clusters must keep cluster_fill_pct (10) % of the SMs
+    // busy.
     int32_t S = 0;
     if (swap && opt.max_cluster >= 2 && 3 * tiles < sms && b_rows <= 64) {
         int64_t s_try = sms / tiles;

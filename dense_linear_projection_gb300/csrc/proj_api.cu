@@ -37,6 +37,10 @@ struct proj_plan_s {
     int overlap = PROJ_OVERLAP_PROLOGUE;    // programmatic dependent launch mode
     int prefetch_stages = kMaxStages;       // PROJ_OVERLAP_WEIGHTS: W stages before the wait
     int sm_count = 0;
+    // fp32 router weights: planned and run as [H | L] along K (2·kt k-blocks);
+    // they exist only in packed form (the split happens in proj_pack_weights).
+    int hilo = 0;
+    int64_t kt = 0;  // k-blocks of K
     // Device staging for proj_run_host (allocated on first use).
     void *stage_x = nullptr;
     void *stage_y = nullptr;
@@ -112,8 +116,12 @@ int64_t partial_bytes_of(const proj_plan_desc_t &plan) {
 // The kernel may use up to the device's opt-in shared memory.  The attribute
 // belongs to the kernel, not to a handle: every launch fits under it.
 bool set_kernel_smem_limit(int smem_optin) {
+    // Also allow clusters above the portable 8 CTAs (GB300 runs 16); the
+    // occupancy query in plan_for_device decides whether a size fits.
     if (cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_optin) != cudaSuccess) {
+                             smem_optin) != cudaSuccess ||
+        cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -207,10 +215,13 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     if (w_layout != PROJ_W_NK && w_layout != PROJ_W_KN) return PROJ_ERR_INVALID_ARG;
     if (has_bias != 0 && has_bias != 1) return PROJ_ERR_INVALID_ARG;
     if (y_dtype != PROJ_BF16 && y_dtype != PROJ_F32) return PROJ_ERR_INVALID_ARG;
-    if (x_dtype != PROJ_BF16 || w_dtype != PROJ_BF16) return PROJ_ERR_UNSUPPORTED;
+    if (x_dtype != PROJ_BF16 || (w_dtype != PROJ_BF16 && w_dtype != PROJ_F32)) return PROJ_ERR_UNSUPPORTED;
+    const bool hilo = w_dtype == PROJ_F32;
     if (has_bias && bias_dtype != PROJ_BF16) return PROJ_ERR_UNSUPPORTED;
     if (K % 8 != 0) return PROJ_ERR_MISALIGNED;
-    if (w_layout == PROJ_W_KN && N % 8 != 0) return PROJ_ERR_MISALIGNED;
+    // [K,N] bf16 weights are loaded by TMA along N; fp32 weights are only read
+    // by the pack kernel, element by element.
+    if (w_layout == PROJ_W_KN && N % 8 != 0 && !hilo) return PROJ_ERR_MISALIGNED;
 
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return PROJ_ERR_CUDA;
@@ -232,7 +243,10 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int f = std::atoi(e);
         if (f >= 1 && f <= 100) opt.cluster_fill_pct = f;
     }
-    proj_status_t st = plan_for_device(M, N, K, w_layout, y_dtype, has_bias, dd, opt, &plan);
+    // fp32 weights: the reduction runs over [H | L], twice the k-blocks of K.
+    const int64_t kt = (K + kBlockK - 1) / kBlockK;
+    const int64_t k_plan = hilo ? 2 * kt * kBlockK : K;
+    proj_status_t st = plan_for_device(M, N, k_plan, w_layout, y_dtype, has_bias, dd, opt, &plan);
     if (st != PROJ_OK) return st;
     if (const char *e = std::getenv("PROJ_FORCE_GRID")) {  // tuning only: fewer CTAs, all-split plans
         const int g = std::atoi(e);
@@ -271,6 +285,8 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     if (!h) return PROJ_ERR_OUT_OF_MEMORY;
     h->device = device;
     h->sm_count = prop.multiProcessorCount;
+    h->hilo = hilo ? 1 : 0;
+    h->kt = kt;
     h->M = M;
     h->N = N;
     h->K = K;
@@ -299,6 +315,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         kp.idesc = idesc_of(plan, w_layout);
         kp.w_kn = w_layout == PROJ_W_KN;
         kp.y_f32 = y_dtype == PROJ_F32;
+        kp.x_kb_mod = hilo ? static_cast<int32_t>(kt) : 0;
         kp.wait_limit_ns = kDefaultWaitLimitNs;
         kp.partials = reinterpret_cast<float *>(sc);
         kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);
@@ -366,9 +383,14 @@ proj_status_t proj_pack_weights(proj_handle_t h, const void *W, void *W_packed, 
     const int64_t chunks = rows * 8;  // 16-byte chunks
     const int64_t want = (chunks + 255) / 256;
     const int blocks = static_cast<int>(want < int64_t(h->sm_count) * 16 ? want : int64_t(h->sm_count) * 16);
-    dev::proj_pack_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
-        static_cast<const uint16_t *>(W), static_cast<uint16_t *>(W_packed), h->N, h->K,
-        h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, chunks);
+    if (h->hilo)
+        dev::proj_pack_hilo_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
+            static_cast<const float *>(W), static_cast<uint16_t *>(W_packed), h->N, h->K,
+            h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, h->kt, chunks);
+    else
+        dev::proj_pack_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
+            static_cast<const uint16_t *>(W), static_cast<uint16_t *>(W_packed), h->N, h->K,
+            h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, chunks);
     return check_launch();
 }
 
@@ -379,6 +401,7 @@ namespace {
 proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packed, const void *bias,
                        void *Y, void *stream) {
     if (!h) return PROJ_ERR_INVALID_ARG;
+    if (h->hilo && !packed && h->plan.kernel == PROJ_KERNEL_TC) return PROJ_ERR_UNSUPPORTED;
     if ((bias != nullptr) != (h->has_bias != 0)) return PROJ_ERR_INVALID_ARG;
     const proj_plan_desc_t &plan = h->plan;
     if (plan.kernel == PROJ_KERNEL_NONE) return PROJ_OK;

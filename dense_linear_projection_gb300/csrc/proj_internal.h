@@ -20,8 +20,8 @@ constexpr int32_t kMmaK = 16;          // K per tcgen05.mma (kind::f16)
 constexpr int32_t kMaxTokenTile = 256; // tcgen05 MMA N limit for cta_group::1
 constexpr int32_t kMaxStages = 12;
 constexpr int32_t kInflightTarget = 160 * 1024;  // stage bytes per SM when streaming W from HBM
-constexpr int32_t kMaxClusterSplit = 8;           // portable thread-block cluster size
-constexpr int32_t kClusterFillPct = 60;           // SMs a cluster split must keep busy (%)
+constexpr int32_t kMaxClusterSplit = 16;          // thread-block cluster size (16: non-portable)
+constexpr int32_t kClusterFillPct = 10;           // SMs a cluster split must keep busy (%)
 constexpr int32_t kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int32_t kEpilogueThreads = 128;
 constexpr int32_t kSmemReserve = 25600; // 1024-byte alignment slack + barriers + epilogue staging
@@ -106,6 +106,7 @@ struct KernelParams {
     uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128, N=b_rows)
     int32_t w_kn;          // W stored [K,N] (MN-major A operand)
     int32_t w_packed;      // W pre-packed: block (tile, k-block) at row (tn·k_blocks + kb)·block_n
+    int32_t x_kb_mod;      // > 0: fp32 router weights as [H | L]; X k-block = kb mod x_kb_mod
     int32_t y_f32;         // store fp32 (else bf16)
     int32_t y_vec;         // Y rows start 16-byte aligned (N·size % 16 == 0, aligned base)
     int64_t wait_limit_ns; // bounded device waits give up after this long

@@ -562,7 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         load_w(st_base + w_off, full, tn, kb);
                     }
                     dep_wait();
-                    tma_load_2d(st_base + x_off, &tmap_x, full, kb * kBlockK, tm * p.block_t, pol_x);
+                    // fp32 router weights run as [H | L] along K: the second
+                    // half multiplies the same X k-blocks again.
+                    const int32_t xkb = (p.x_kb_mod > 0 && kb >= p.x_kb_mod) ? kb - p.x_kb_mod : kb;
+                    tma_load_2d(st_base + x_off, &tmap_x, full, xkb * kBlockK, tm * p.block_t, pol_x);
                     if (issued == 0 && pre == 0) trace_stamp(p, kTraceFirstLoad);
                     ++issued;
                     if (++stage == stages) {
@@ -1119,6 +1122,63 @@ __global__ void proj_pack_kernel(const uint16_t *W, uint16_t *P, int64_t N, int6
             }
         }
         *reinterpret_cast<uint4 *>(P + ((blk * block_n + r) * 64 + c8 * 8)) = out;
+    }
+}
+
+// fp32 router weights ("How I made Muse's GPU projections 1.32× faster in the
+// Open Kernel Challenge", section "Why the high-plus-low router scheme
+// helped"): H = roundBF16(W), R = W − FP32(H) (an fp32 subtraction), L =
+// roundBF16(R), packed as [H | L] along K: packed k-block kb' < kt holds H's
+// k-block kb', kb' >= kt holds L's k-block kb' − kt (kt = k-blocks of K), in
+// the block layout of proj_pack_kernel.  One thread writes 16 bytes.
+__global__ void proj_pack_hilo_kernel(const float *W, uint16_t *P, int64_t N, int64_t K, int w_kn,
+                                      int32_t block_n, int64_t k_blocks, int64_t kt, int64_t chunks) {
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < chunks;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        int64_t blk, r, c8;
+        if (!w_kn) {
+            c8 = e & 7;
+            const int64_t row = e >> 3;
+            blk = row / block_n;
+            r = row - blk * block_n;
+        } else {
+            const int64_t per_blk = static_cast<int64_t>(block_n) * 8;
+            blk = e / per_blk;
+            const int64_t rem = e - blk * per_blk;
+            c8 = rem / block_n;
+            r = rem - c8 * block_n;
+        }
+        const int64_t tn = blk / k_blocks;
+        const int64_t kbp = blk - tn * k_blocks;
+        const bool low = kbp >= kt;
+        const int64_t n = tn * block_n + r;
+        const int64_t k0 = (low ? kbp - kt : kbp) * 64 + c8 * 8;
+        uint32_t w4[4] = {0u, 0u, 0u, 0u};
+        if (n < N && k0 < K) {  // K % 8 == 0: the 8 values are all in range
+            float v[8];
+            if (!w_kn) {
+                const float4 a = *reinterpret_cast<const float4 *>(W + n * K + k0);
+                const float4 b = *reinterpret_cast<const float4 *>(W + n * K + k0 + 4);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) v[j] = W[(k0 + j) * N + n];
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint16_t h2[2];
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    const float w = v[2 * j + t];
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+                    const __nv_bfloat16 part = low ? __float2bfloat16_rn(__fsub_rn(w, __bfloat162float(hi))) : hi;
+                    h2[t] = *reinterpret_cast<const uint16_t *>(&part);
+                }
+                w4[j] = static_cast<uint32_t>(h2[0]) | (static_cast<uint32_t>(h2[1]) << 16);
+            }
+        }
+        *reinterpret_cast<uint4 *>(P + ((blk * block_n + r) * 64 + c8 * 8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
     }
 }
 

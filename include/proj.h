@@ -38,7 +38,8 @@
  *
  * Alignment (TMA global strides and addresses must be 16-byte multiples):
  *   X and W base addresses 16-byte aligned; K % 8 == 0 (X rows and [N,K]
- *   weight rows are whole 16-byte multiples); for PROJ_W_KN also N % 8 == 0.
+ *   weight rows are whole 16-byte multiples); for PROJ_W_KN bf16 weights also
+ *   N % 8 == 0 (fp32 router weights are read only by proj_pack_weights).
  *   Violations return PROJ_ERR_MISALIGNED and launch nothing.
  *
  * Errors: every call returns a proj_status_t; nothing aborts or throws across
@@ -113,7 +114,7 @@ typedef struct proj_device_desc {
  * TMA/WGMMA kernel was a new experiment" that splits 128 tiles 42/43/43).
  * Cluster split instead (cluster_split = S ≥ 2): when there are fewer than a
  * third as many narrow swapped tiles as SMs (stream-K would give a tile more
- * than three contributors) and S CTAs per tile keep at least 60 % of the SMs busy,
+ * than three contributors) and S CTAs per tile (S ≤ 16) keep at least 10 % of the SMs busy,
  * each tile gets its own cluster of S CTAs, grid = tiles_sk · S, and the
  * partial sums meet in distributed shared memory; no partial-sum scratch and
  * no counters.
@@ -197,7 +198,15 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
 /*
  * Create a handle for one problem shape on the current CUDA device.
  *   M, N, K ≥ 0 (a zero M or N plans nothing; K == 0 plans Y = bias or 0).
- *   x_dtype, w_dtype, bias_dtype: PROJ_BF16 only (else PROJ_ERR_UNSUPPORTED).
+ *   x_dtype, bias_dtype: PROJ_BF16 only (else PROJ_ERR_UNSUPPORTED).
+ *   w_dtype: PROJ_BF16, or PROJ_F32 for fp32 router weights, computed as the
+ *     worklog's high/low bf16 split (section "Why the high-plus-low router
+ *     scheme helped"): H = roundBF16(W), L = roundBF16(W − FP32(H)),
+ *     Y = X·Hᵀ + X·Lᵀ summed in one fp32 accumulator.  The split happens
+ *     when the weights are packed: such a handle runs only through
+ *     proj_pack_weights (fp32 W in) and proj_run_packed / proj_run_host_packed;
+ *     proj_run and proj_run_host return PROJ_ERR_UNSUPPORTED.  Its plan
+ *     covers [H | L] along K: k_blocks = 2·ceil(K / 64).
  *   y_dtype: PROJ_BF16 or PROJ_F32.   has_bias: 0 or 1.
  *   stream: cudaStream_t used to clear the new scratch; create synchronises it
  *   before returning, so the handle may be used on any stream afterwards.
@@ -237,9 +246,11 @@ proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void
  * proj_packed_weight_bytes: the packed size, tiles_n · k_blocks · block_n ·
  *   128 bytes (0 for plans without the tensor-core kernel).
  *   PROJ_ERR_UNSUPPORTED if the packed rows would not fit 31-bit coordinates.
- * proj_pack_weights: W (device, the handle's layout) → W_packed (device,
- *   proj_packed_weight_bytes bytes, 16-byte aligned, caller-owned), enqueued
- *   on `stream`.  W must not overlap W_packed.
+ * proj_pack_weights: W (device, the handle's layout and w_dtype: bf16, or
+ *   fp32 for a PROJ_F32 handle, which stores the H blocks of a tile followed
+ *   by its L blocks) → W_packed (device, proj_packed_weight_bytes bytes,
+ *   16-byte aligned, caller-owned), enqueued on `stream`.  W must not overlap
+ *   W_packed.
  * proj_run_packed: proj_run with packed weights; same arguments otherwise.
  * PROJ_ERR_INVALID_ARG for NULL handles or pointers, PROJ_ERR_MISALIGNED for
  * unaligned pointers, PROJ_ERR_CUDA if a launch fails.

@@ -156,6 +156,9 @@ def _lib():
         lib.synth_normal_bf16.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int64,
                                           ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]
         lib.synth_normal_bf16.restype = None
+        lib.synth_normal_f32.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.c_int64,
+                                         ctypes.c_int64, ctypes.c_double, ctypes.c_void_p]
+        lib.synth_normal_f32.restype = None
         lib.synth_stream_seed.argtypes = [ctypes.c_uint64, ctypes.c_int]
         lib.synth_stream_seed.restype = ctypes.c_uint64
         _LIB = lib
@@ -169,6 +172,16 @@ def normal_bf16(seed: int, tensor: int, count: int, std: float,
     if count:
         _lib().synth_normal_bf16(int(seed), int(tensor), int(first), int(count),
                                  float(std), out.ctypes.data)
+    return out
+
+
+def normal_f32(seed: int, tensor: int, count: int, std: float, first: int = 0) -> np.ndarray:
+    """``count`` fp32 values of N(0, std²) from one tensor stream (C): the same
+    normals as :func:`normal_bf16`, rounded to fp32 instead of bf16."""
+    out = np.empty(count, dtype=np.float32)
+    if count:
+        _lib().synth_normal_f32(int(seed), int(tensor), int(first), int(count),
+                                float(std), out.ctypes.data)
     return out
 
 
@@ -194,6 +207,7 @@ class Workload:
     seed: int = 0
     x_std: float = 1.0
     bias_std: float = 0.02
+    w_dtype: str = "bf16"  # "bf16", or "f32" (router weights: the high/low bf16 split)
 
     @property
     def w_std(self) -> float:
@@ -202,17 +216,18 @@ class Workload:
 
     def with_m(self, M: int) -> "Workload":
         return Workload(self.name, M, self.N, self.K, self.w_layout, self.has_bias,
-                        self.y_dtype, self.seed, self.x_std, self.bias_std)
+                        self.y_dtype, self.seed, self.x_std, self.bias_std, self.w_dtype)
 
     # ---- byte / flop accounting (the pages' roofline model: F = 2MNK) ----
     @property
     def weight_bytes(self) -> int:
-        return 2 * self.N * self.K
+        # fp32 router weights stream as two bf16 parts: 4 bytes a weight either way.
+        return (4 if self.w_dtype == "f32" else 2) * self.N * self.K
 
     @property
     def algorithmic_bytes(self) -> int:
         yb = 4 if self.y_dtype == "f32" else 2
-        return (2 * self.N * self.K + 2 * self.M * self.K
+        return (self.weight_bytes + 2 * self.M * self.K
                 + (2 * self.N if self.has_bias else 0) + yb * self.M * self.N)
 
     @property
@@ -227,6 +242,9 @@ WORKLOADS = {
     "ffn_up_sweep": Workload("ffn_up_sweep", 16, 28672, 8192, W_NK, False, "bf16", 2),
     "qkv_kn_bias": Workload("qkv_kn_bias", 256, 12288, 4096, W_KN, True, "bf16", 3),
     "prefill": Workload("prefill", 4096, 8192, 8192, W_NK, False, "bf16", 4),
+    # The worklog's fp32-weight router (N = 256, K = 8192) through the high/low
+    # bf16 split, fp32 output; a §8(f) extension, not one of the five configs.
+    "router_f32w": Workload("router_f32w", 16, 256, 8192, W_NK, False, "f32", 5, w_dtype="f32"),
 }
 FFN_SWEEP_M = (1, 2, 4, 8, 16, 32, 64)
 
@@ -239,11 +257,12 @@ def workload(name: str, M: Optional[int] = None) -> Workload:
 def make_inputs(w: Workload) -> dict:
     """Draw X ``[M,K]``, W in storage order and (optionally) the bias.
 
-    All arrays are uint16 bf16 bit patterns; W is ``[N,K]`` for ``W_NK`` and
-    ``[K,N]`` for ``W_KN``.
+    All arrays are uint16 bf16 bit patterns, except W of an fp32-weight
+    workload (float32); W is ``[N,K]`` for ``W_NK`` and ``[K,N]`` for ``W_KN``.
     """
     X = normal_bf16(w.seed, STREAM_X, w.M * w.K, w.x_std).reshape(w.M, w.K)
-    Wf = normal_bf16(w.seed, STREAM_W, w.N * w.K, w.w_std)
+    gen = normal_f32 if w.w_dtype == "f32" else normal_bf16
+    Wf = gen(w.seed, STREAM_W, w.N * w.K, w.w_std)
     Wm = Wf.reshape(w.N, w.K) if w.w_layout == W_NK else Wf.reshape(w.K, w.N)
     b = normal_bf16(w.seed, STREAM_BIAS, w.N, w.bias_std) if w.has_bias else None
     return {"X": X, "W": Wm, "bias": b}

@@ -39,20 +39,31 @@ static inline uint16_t synth_bf16_rne(double v) {
     return (uint16_t)(((uint64_t)u + 0x7FFFu + lsb) >> 16);
 }
 
+/* The j-th standard normal of stream s (Box–Muller on the pair j & ~1). */
+static inline double synth_normal_at(uint64_t s, uint64_t j) {
+    const double two_pi = 6.283185307179586476925286766559;
+    uint64_t pair = j & ~1ULL;
+    double u1 = synth_uniform(s, pair);
+    double u2 = synth_uniform(s, pair + 1ULL);
+    double r = sqrt(-2.0 * log(u1));
+    double th = two_pi * u2;
+    return (j & 1ULL) ? r * sin(th) : r * cos(th);
+}
+
 /* out[i] = bf16(std · normal_j) for j = first + i, i < count. */
 void synth_normal_bf16(uint64_t seed, int tensor, int64_t first, int64_t count,
                        double std, uint16_t *out) {
     const uint64_t s = synth_stream_seed(seed, tensor);
-    const double two_pi = 6.283185307179586476925286766559;
 #pragma omp parallel for schedule(static)
-    for (int64_t i = 0; i < count; ++i) {
-        uint64_t j = (uint64_t)(first + i);
-        uint64_t pair = j & ~1ULL;
-        double u1 = synth_uniform(s, pair);
-        double u2 = synth_uniform(s, pair + 1ULL);
-        double r = sqrt(-2.0 * log(u1));
-        double th = two_pi * u2;
-        double z = (j & 1ULL) ? r * sin(th) : r * cos(th);
-        out[i] = synth_bf16_rne(z * std);
-    }
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = synth_bf16_rne(synth_normal_at(s, (uint64_t)(first + i)) * std);
+}
+
+/* out[i] = fp32(std · normal_j) (round to nearest): fp32 weights. */
+void synth_normal_f32(uint64_t seed, int tensor, int64_t first, int64_t count,
+                      double std, float *out) {
+    const uint64_t s = synth_stream_seed(seed, tensor);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = (float)(synth_normal_at(s, (uint64_t)(first + i)) * std);
 }

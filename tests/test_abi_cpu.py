@@ -73,10 +73,11 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     assert p["tiles_dp"] + p["tiles_sk"] == tiles
     S = p["cluster_split"]
     if S:
-        # Cluster split: every tile its own cluster of S CTAs, at least 60 %
-        # of the SMs busy, narrow swapped tiles, partials in shared memory.
-        assert 2 <= S <= 8 and S <= KT and p["swap_ab"] == 1 and p["block_t"] <= 64
-        assert p["tiles_dp"] == 0 and G == tiles * S and 10 * G >= 6 * sms
+        # Cluster split: every tile its own cluster of S CTAs (S <= 16), at
+        # least 10 % of the SMs busy, fewer than a third as many tiles as SMs,
+        # narrow swapped tiles, partials in shared memory.
+        assert 2 <= S <= 16 and S <= KT and p["swap_ab"] == 1 and p["block_t"] <= 64
+        assert p["tiles_dp"] == 0 and G == tiles * S and 10 * G >= sms and 3 * tiles < sms
         assert p["scratch_bytes"] == 256
     if p["tiles_sk"]:
         assert p["tiles_dp"] % G == 0
@@ -149,10 +150,15 @@ def test_plans_of_the_workloads(M, N, K, layout):
 
 
 def test_cluster_split_plans():
-    # 16 tiles of the 2048-row decode weight: clusters of 8 (128 CTAs).
+    # 16 tiles of the 2048-row decode weight: clusters of 9 (144 CTAs; a
+    # device lowers S until all 16 clusters fit at once).
     p = plan(16, 2048, 8192)
-    assert (p["cluster_split"], p["grid"], p["tiles_sk"], p["tiles_dp"]) == (8, 128, 16, 0)
-    assert dlp.proj_plan_reduction_order(p, 3) == [(3 * 8 + r, -1) for r in range(8)]
+    assert (p["cluster_split"], p["grid"], p["tiles_sk"], p["tiles_dp"]) == (9, 144, 16, 0)
+    assert dlp.proj_plan_reduction_order(p, 3) == [(3 * 9 + r, -1) for r in range(9)]
+    # The 2 tiles of the router weight (N = 256, [H | L]: 2·8192 K): clusters
+    # of 16, the largest size.
+    p = plan(16, 256, 2 * 8192)
+    assert (p["cluster_split"], p["grid"]) == (16, 32)
     # 64 tiles of the 8192-row decode weight: stream-K over every SM (a split
     # tile has about 2.4 contributors), as for the 28672-row FFN weight.
     for N in (8192, 28672):
@@ -163,17 +169,20 @@ def test_cluster_split_plans():
     assert plan(16, 50 * 128, 8192)["cluster_split"] == 3
     assert plan(16, 51 * 128, 8192)["cluster_split"] == 0
     assert plan(16, 45 * 128, 8192)["cluster_split"] == 3
-    # Below 60 % of the SMs (12 SMs, 3 tiles: clusters of 4 on 12 SMs; 8 SMs
-    # and 2 tiles: clusters of 4 on 8 SMs; 5 SMs, 1 tile: clusters of 5).
+    # Small devices (12 SMs, 3 tiles: clusters of 4; 8 SMs and 2 tiles:
+    # clusters of 4; 5 SMs, 1 tile: clusters of 5).
     assert plan(16, 3 * 128, 8192, sm_count=12, smem_optin_bytes=232448)["cluster_split"] == 4
     assert plan(16, 2 * 128, 8192, sm_count=8, smem_optin_bytes=232448)["cluster_split"] == 4
     assert plan(16, 128, 8192, sm_count=5, smem_optin_bytes=232448)["cluster_split"] == 5
+    # Fewer than 10 % of the SMs busy: 1 tile with 4 or 8 k-blocks on 152 SMs.
+    assert plan(16, 128, 256)["cluster_split"] == 0
+    assert plan(16, 128, 512)["cluster_split"] == 0
     # S is capped by the k-blocks there are to share (5 SMs, 1 tile, 4 k-blocks).
     p = plan(16, 128, 256, sm_count=5, smem_optin_bytes=232448)
     assert p["k_blocks"] == 4 and p["cluster_split"] == 4 and p["grid"] == 4
     # Several token tiles (100 tokens in two 64-row tiles) are clustered too.
     p = plan(100, 1024, 8192)
-    assert (p["block_t"], p["tiles_m"], p["cluster_split"], p["grid"]) == (64, 2, 8, 128)
+    assert (p["block_t"], p["tiles_m"], p["cluster_split"], p["grid"]) == (64, 2, 9, 144)
     # Token-major tiles are never cluster-split.
     assert plan(256, 2048, 8192)["cluster_split"] == 0
 

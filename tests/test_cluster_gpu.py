@@ -2,7 +2,7 @@
 over the S CTAs of one thread-block cluster, partial sums added in shared
 memory in rank (= K) order.
 
-The planner's own choices (S = 2 .. 8 on 152 SMs; the handle lowers S where
+The planner's own choices (S = 2 .. 16 on 152 SMs; the handle lowers S where
 the device cannot hold every cluster at once) and every cluster size forced on
 a few tiles: K ranges that do not divide evenly by S, ragged N and K tails,
 both weight layouts and two token tiles.  Each is compared with the fp64
@@ -20,13 +20,14 @@ pytestmark = pytest.mark.gpu
 
 # (M, N, K, layout, bias, y_dtype, S the planner picks on 152 SMs)
 CLUSTER_SHAPES = [
-    (16, 2048, 8192, synth.W_NK, False, "f32", 8),   # 16 tiles x 8
+    (16, 2048, 8192, synth.W_NK, False, "f32", 9),   # 16 tiles x 9 (x 6 where 16 clusters of 9 do not fit)
     (9, 2500, 1032, synth.W_NK, True, "bf16", 7),    # 20 tiles x 7, ragged N, 17 k-blocks
     (16, 3304, 1032, synth.W_KN, True, "bf16", 5),   # [K,N] weights, 26 tiles x 5
     (16, 4000, 2056, synth.W_NK, True, "bf16", 4),   # 32 tiles x 4, ragged K block
     (12, 5300, 1032, synth.W_NK, False, "f32", 3),   # 42 tiles x 3
     (16, 6144, 8192, synth.W_NK, True, "bf16", 3),   # 48 tiles x 3 (x 2 where 48 clusters of 3 do not fit)
-    (100, 1024, 8192, synth.W_NK, True, "bf16", 8),  # two 64-token tiles x 8 weight tiles
+    (100, 1024, 8192, synth.W_NK, True, "bf16", 9),  # two 64-token tiles x 8 weight tiles
+    (16, 1024, 8192, synth.W_NK, False, "bf16", 16), # 8 tiles x 16: the largest clusters
 ]
 
 
@@ -62,11 +63,12 @@ def test_cluster_split_parity(shape, monkeypatch):
     gu.assert_within_tol(gu.y_to_f64(Y_sk), r, "stream-K")
 
 
-@pytest.mark.parametrize("S", [2, 3, 4, 5, 6, 7, 8])
-@pytest.mark.parametrize("M,N,K,layout,bias,yd", [
-    (16, 512, 1032, synth.W_NK, True, "bf16"),   # 4 tiles, 17 k-blocks
-    (100, 264, 520, synth.W_KN, True, "f32"),    # 2 token x 3 weight tiles, 9 k-blocks, ragged
-], ids=["NK_4tiles", "KN_6tiles"])
+@pytest.mark.parametrize("S,M,N,K,layout,bias,yd", [
+    (S, *shape) for S in (2, 3, 4, 5, 6, 7, 8, 9, 12, 16) for shape in (
+        (16, 512, 1032, synth.W_NK, True, "bf16"),   # 4 tiles, 17 k-blocks
+        (100, 264, 520, synth.W_KN, True, "f32"),    # 2 token x 3 weight tiles, 9 k-blocks, ragged
+    ) if S <= -(-shape[2] // 64)
+], ids=lambda v: str(v))
 def test_every_cluster_size(S, M, N, K, layout, bias, yd, monkeypatch):
     import torch
     import dense_linear_projection_gb300 as dlp

@@ -56,3 +56,16 @@ def test_workload_accounting():
     assert w["prefill"].algorithmic_bytes == 268_435_456
     assert w["decode_bias"].flops == 2 * 16 * 8192 * 8192
     assert w["qkv_kn_bias"].w_layout == synth.W_KN
+
+
+def test_fp32_weights_share_the_bf16_stream():
+    # fp32 weights are the same normals rounded to fp32 instead of bf16: their
+    # bf16 rounding is the bf16 stream itself, bit for bit.
+    a = synth.normal_f32(9, synth.STREAM_W, 4096, 0.01)
+    b = synth.normal_bf16(9, synth.STREAM_W, 4096, 0.01)
+    assert a.dtype == np.float32 and np.array_equal(synth.to_bf16_bits(a.astype(np.float64)), b)
+    w = synth.WORKLOADS["router_f32w"]
+    assert (w.N, w.K, w.w_dtype) == (256, 8192, "f32")
+    assert w.weight_bytes == 4 * 256 * 8192
+    assert w.algorithmic_bytes == 4 * 256 * 8192 + 2 * 16 * 8192 + 4 * 16 * 256
+    assert synth.make_inputs(w.with_m(2))["W"].dtype == np.float32
