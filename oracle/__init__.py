@@ -46,7 +46,7 @@ def build(force: bool = False) -> str:
     # -ffp-contract=off: each product and each sum is its own rounded fp64 op,
     # exactly as the loop is written (no fused multiply-add reassociation).
     cmd = ["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
-           "-o", tmp, _SRC]
+           "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -70,6 +70,10 @@ def _lib():
         lib.oracle_split_hilo.restype = None
         lib.oracle_project_f32w.argtypes = [i64, i64, i64, vp, vp, ctypes.c_int, vp, vp]
         lib.oracle_project_f32w.restype = None
+        lib.oracle_gelu.argtypes = [ctypes.c_double]
+        lib.oracle_gelu.restype = ctypes.c_double
+        lib.oracle_apply_activation.argtypes = [i64, ctypes.c_int, vp]
+        lib.oracle_apply_activation.restype = None
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _LIB = lib
@@ -180,6 +184,30 @@ def project_hilo(X, W, w_layout: int = W_NK, bias=None) -> np.ndarray:
     """The router method itself in fp64: X·Hᵀ + X·Lᵀ (+ bias)."""
     H, L = split_hilo(W)
     return project(X, H, w_layout, bias) + project(X, L, w_layout, None)
+
+
+ACT_NONE, ACT_GELU = 0, 1
+
+
+def gelu(x) -> np.ndarray:
+    """GELU(x) = x/2 · (1 + erf(x/√2)) of fp64 values, one by one."""
+    lib = _lib()
+    flat = np.asarray(x, dtype=np.float64).ravel()
+    return np.array([lib.oracle_gelu(float(v)) for v in flat]).reshape(np.shape(x))
+
+
+def project_fused(X, W, w_layout: int = W_NK, bias=None, act: int = ACT_NONE,
+                  residual=None) -> np.ndarray:
+    """The fused epilogue: act(X·Wᵀ + bias) + residual, all in fp64.  ``residual``
+    is [M,N] fp64 (the decoded residual input) or None."""
+    Y = np.ascontiguousarray(project(X, W, w_layout, bias))
+    if act not in (ACT_NONE, ACT_GELU):
+        raise ValueError("act must be ACT_NONE or ACT_GELU")
+    if Y.size:
+        _lib().oracle_apply_activation(Y.size, int(act), Y.ctypes.data)
+    if residual is not None:
+        Y = Y + np.asarray(residual, dtype=np.float64)
+    return Y
 
 
 def max_threads() -> int:

@@ -28,6 +28,7 @@
  * OpenMP spreads independent output cells over host threads; each cell's sum
  * is still the single sequential k loop.
  */
+#include <math.h>
 #include <stdint.h>
 #include <string.h>
 #ifdef _OPENMP
@@ -139,6 +140,25 @@ void oracle_project_f32w(int64_t M, int64_t N, int64_t K, const uint16_t *X,
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n)
             Y[m * N + n] = cell_f32w(N, K, X, W, w_layout, bias, m, n);
+}
+
+/* ------------------------------------------------------------------------
+ * Fused epilogues.  The worklog's second page fuses the FFN's activation into
+ * the projection's epilogue ("FFN intermediate written, re-read for GELU,
+ * written again" → written once), and a residual connection adds an earlier
+ * representation back to the projected one (first page, section
+ * "Normalization and residuals also cost time").  The pages do not write the
+ * activation out; this oracle takes GELU's definition, x·Φ(x) with Φ the
+ * standard normal CDF: GELU(x) = x/2 · (1 + erf(x/√2)).
+ * ------------------------------------------------------------------------ */
+double oracle_gelu(double x) {
+    return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
+}
+
+/* In place over `count` values: act 0 = identity, 1 = GELU. */
+void oracle_apply_activation(int64_t count, int act, double *v) {
+    if (act == 1)
+        for (int64_t i = 0; i < count; ++i) v[i] = oracle_gelu(v[i]);
 }
 
 int oracle_max_threads(void) {

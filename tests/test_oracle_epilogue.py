@@ -1,0 +1,59 @@
+"""Pins of the oracle's fused-epilogue functions: GELU and act(X·Wᵀ + b) + R.
+
+GELU is taken from its definition x·Φ(x) (the pages fuse "GELU" into the FFN
+projection's epilogue without writing it out).  It is pinned against the
+standard normal CDF of an independent library routine (scipy.special.ndtr),
+the identity GELU(x) − GELU(−x) = x (from Φ(x) + Φ(−x) = 1), and its limits.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+scipy_special = pytest.importorskip("scipy.special")
+
+
+def test_gelu_definition_against_normal_cdf():
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.standard_normal(2000) * 3.0, [0.0, 1.0, -1.0, np.sqrt(2.0), 0.5]])
+    want = x * scipy_special.ndtr(x)
+    got = oracle.gelu(x)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-15)
+    assert oracle.gelu([0.0])[0] == 0.0
+
+
+def test_gelu_odd_part_identity_and_limits():
+    x = np.linspace(-6.0, 6.0, 1201)
+    g_pos, g_neg = oracle.gelu(x), oracle.gelu(-x)
+    assert np.allclose(g_pos - g_neg, x, rtol=0, atol=1e-14)
+    assert abs(oracle.gelu([12.0])[0] - 12.0) < 1e-12
+    assert abs(oracle.gelu([-12.0])[0]) < 1e-12
+    # Monotone on [−0.75, ∞) (its minimum is near x = −0.7518).
+    g = oracle.gelu(np.linspace(-0.75, 6.0, 500))
+    assert np.all(np.diff(g) > 0)
+
+
+def _bits(a):
+    return synth.to_bf16_bits(np.asarray(a, dtype=np.float64))
+
+
+def test_fused_epilogue_order_and_residual():
+    # W = 0: Y = act(bias) + residual, whatever X is.
+    M, N, K = 3, 5, 8
+    X = _bits(np.ones((M, K)))
+    W = _bits(np.zeros((N, K)))
+    b = _bits([-2.0, -1.0, 0.0, 1.0, 2.0])
+    R = np.arange(M * N, dtype=np.float64).reshape(M, N) / 4.0
+    bd = oracle.bf16_to_double(b)
+    got = oracle.project_fused(X, W, oracle.W_NK, b, oracle.ACT_GELU, R)
+    assert np.array_equal(got, oracle.gelu(np.broadcast_to(bd, (M, N))) + R)
+    # The activation applies to the projection plus bias, before the residual:
+    # X·Wᵀ = 2 in every cell, bias 0.5: GELU(2.5) + R.
+    X2 = _bits(np.full((M, K), 0.25))
+    Wn = _bits(np.ones((N, K)))
+    got2 = oracle.project_fused(X2, Wn, oracle.W_NK, _bits(np.full(N, 0.5)), oracle.ACT_GELU, R)
+    assert np.allclose(got2, 2.5 * scipy_special.ndtr(2.5) + R, rtol=1e-14, atol=0)
+    # No activation, no residual: the plain projection.
+    assert np.array_equal(oracle.project_fused(X2, Wn, oracle.W_NK, None),
+                          oracle.project(X2, Wn, oracle.W_NK, None))

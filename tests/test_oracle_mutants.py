@@ -1,7 +1,8 @@
 """The oracle's pins catch plausible mistakes.
 
 Each case plants one mistake in a copy of oracle.c (on the CPU), builds it, and
-runs the pin suites (test_oracle.py, test_oracle_router.py) against it in a
+runs the pin suites (test_oracle.py, test_oracle_router.py,
+test_oracle_epilogue.py) against it in a
 subprocess: they must fail.  The real oracle passing the same suites is those
 files themselves.
 """
@@ -41,6 +42,14 @@ MUTANTS = {
         "const double w = oracle_bf16_to_double(oracle_f32_to_bf16("
         "w_layout == 0 ? W[n * K + kk] : W[kk * N + n]));"),
     "f32w_layout_ignored": ("(w_layout == 0 ? W[n * K + kk] : W[kk * N + n])", "(W[n * K + kk])"),
+    # Fused epilogues: GELU's definition and where it applies.
+    "gelu_no_half": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+                     "return 1.0 * x * (1.0 + erf(x / sqrt(2.0)));"),
+    "gelu_scale_two": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+                       "return 0.5 * x * (1.0 + erf(x / 2.0));"),
+    "gelu_sign": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
+                  "return 0.5 * x * (1.0 - erf(x / sqrt(2.0)));"),
+    "activation_ignored": ("if (act == 1)\n", "if (act == 7)\n"),
 }
 
 
@@ -54,10 +63,11 @@ def test_pins_fail_on_mutant(name):
         so = os.path.join(d, "mutant.so")
         open(c, "w").write(src.replace(old, new))
         subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared",
-                        "-o", so, c], check=True)
+                        "-o", so, c, "-lm"], check=True)
         env = dict(os.environ, ORACLE_LIB=so)
         r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
                             os.path.join(HERE, "test_oracle.py"),
-                            os.path.join(HERE, "test_oracle_router.py")],
+                            os.path.join(HERE, "test_oracle_router.py"),
+                            os.path.join(HERE, "test_oracle_epilogue.py")],
                            cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
         assert r.returncode != 0, f"pins did not catch mutant {name}:\n{r.stdout[-2000:]}"
