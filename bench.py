@@ -219,7 +219,7 @@ def _oracle_project(w, X, W, bias):
     return oracle.project(X, W, w.w_layout, bias)
 
 
-def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None) -> dict:
+def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None, act: str = "none", residual=None) -> dict:
     """Time the fp64 oracle on the host cores on a bounded sample of the
     workload: all M token rows against the first n_cols output columns (or the
     whole workload, repeated, if that is quick).  Returns weight GB/s.  With
@@ -256,6 +256,11 @@ def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None) -> dict:
     out = {"value": wbytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
            "sample": sample, "seconds": elapsed}
     if y_gpu is not None:
+        # The fused epilogue, if any, on the oracle's columns (fp64).
+        if act == "gelu":
+            r = oracle.gelu(r)
+        if residual is not None:
+            r = r + residual[:, :n_cols]
         # The tolerance of the parity tests: |u - r| <= 1e-3 + 5e-3·|r|.
         u = y_gpu[:, :n_cols]
         bad = int(np.count_nonzero(~(np.abs(u - r) <= 1e-3 + 5e-3 * np.abs(r))))
@@ -309,9 +314,13 @@ def run_gpu_arm(args) -> dict:
     # the preparation step, outside every timed region.
     Wrun = [proj.pack(Wc) for Wc in Ws] if args.packed else Ws
     torch.cuda.synchronize()
+    # Fused epilogue (optional): activation and a residual input R.
+    proj.set_activation(dlp.PROJ_ACT_GELU if args.activation == "gelu" else dlp.PROJ_ACT_NONE)
+    R = (torch.randn((w.M, w.N), device=device, generator=torch.Generator(device).manual_seed(w.seed))
+         .to(y_dt) if args.residual else None)
 
     def step(Wc, strm):
-        proj(X, Wc, bias, out=Y, stream=strm, packed=args.packed)
+        proj(X, Wc, bias, out=Y, stream=strm, packed=args.packed, residual=R)
 
     # Graphs of back-to-back steps, each step on the next W copy.
     def capture(nsteps, offset):
@@ -442,12 +451,15 @@ def run_gpu_arm(args) -> dict:
                    "note": "informational; same inputs, W rotation and CUDA-graph replay"}
         del Yl, gl
     peaks = load_peaks()
-    traffic, profile_path = profile_traffic(args.workload if args.m is None else
-                                            f"{args.workload}_m{args.m}")
-    hbm_bound = roofline_time_s(w.algorithmic_bytes, w.flops, peaks["hbm_gbs"] * 1e9,
+    fused = args.activation != "none" or args.residual
+    traffic, profile_path = (None, None) if fused else profile_traffic(
+        args.workload if args.m is None else f"{args.workload}_m{args.m}")
+    # A residual is one more [M,N] array read.
+    alg_bytes = w.algorithmic_bytes + (w.M * w.N * (4 if w.y_dtype == "f32" else 2) if args.residual else 0)
+    hbm_bound = roofline_time_s(alg_bytes, w.flops, peaks["hbm_gbs"] * 1e9,
                                 peaks["bf16_tflops"] * 1e12)
-    if w.algorithmic_bytes / (peaks["hbm_gbs"] * 1e9) >= w.flops / (peaks["bf16_tflops"] * 1e12):
-        roof = {"bound": "hbm", "achieved": w.algorithmic_bytes / t_step / 1e9,
+    if alg_bytes / (peaks["hbm_gbs"] * 1e9) >= w.flops / (peaks["bf16_tflops"] * 1e12):
+        roof = {"bound": "hbm", "achieved": alg_bytes / t_step / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
         peak_tf = peaks["bf16_tflops_sustained"] if agg["seconds"] > 1.0 else peaks["bf16_tflops"]
@@ -456,7 +468,7 @@ def run_gpu_arm(args) -> dict:
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = traffic
     roof["peak_source"] = ("of measured" if peaks["source"] == "measured" else "of fallback")
-    roof["bytes_per_launch"] = w.algorithmic_bytes
+    roof["bytes_per_launch"] = alg_bytes
     roof["flops_per_launch"] = w.flops
     roof["bound_us"] = hbm_bound * 1e6
     if profile_path:
@@ -464,7 +476,7 @@ def run_gpu_arm(args) -> dict:
 
     # ---- e2e: the user-facing call with host activations, every step.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not fused:  # the host-buffer call has no fused epilogue
         Xh = torch.from_numpy(np.ascontiguousarray(inp["X"]).view(np.int16)).view(
             torch.bfloat16).pin_memory()
         Yh = torch.empty((w.M, w.N), dtype=y_dt).pin_memory()
@@ -498,7 +510,8 @@ def run_gpu_arm(args) -> dict:
         step(Wrun[0], stream)  # the output of one plain call, to be safe
         torch.cuda.synchronize()
         y64 = Y.float().cpu().numpy().astype(np.float64)
-        cpu = cpu_oracle_timing(w, inp, args.cpu_seconds, y_gpu=y64)
+        cpu = cpu_oracle_timing(w, inp, args.cpu_seconds, y_gpu=y64, act=args.activation,
+                                residual=None if R is None else R.double().cpu().numpy())
         cpu.pop("seconds", None)
 
     plan = proj.plan
@@ -525,6 +538,8 @@ def run_gpu_arm(args) -> dict:
             "overlap": f"programmatic dependent launch, mode '{args.overlap}'",
             "weights": ("pre-packed tile-contiguous by proj_pack_weights, once per copy before "
                         "timing (the preparation step)" if args.packed else "as stored"),
+            "epilogue": ("act(X·Wᵀ + b) + R" if args.residual else "act(X·Wᵀ + b)")
+                        + f", act = {args.activation}",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "us_per_call": t_step * 1e6,
@@ -629,6 +644,10 @@ def parse_args(argv=None):
                     help="skip the informational cuBLAS timing")
     ap.add_argument("--no-packed", dest="packed", action="store_false",
                     help="run on the weights as stored instead of pre-packed ones")
+    ap.add_argument("--activation", choices=["none", "gelu"], default="none",
+                    help="fused activation on projection + bias (proj_set_activation)")
+    ap.add_argument("--residual", action="store_true",
+                    help="fused residual add: Y = act(X·Wᵀ + b) + R, R an [M,N] input")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -29,7 +29,7 @@ __all__ = [
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "TRACE_FIELDS",
     "PROJ_OVERLAP_NONE", "PROJ_OVERLAP_PROLOGUE", "PROJ_OVERLAP_WEIGHTS", "proj_run_noalloc",
     "proj_packed_weight_bytes", "proj_pack_weights", "proj_run_packed", "proj_run_host_packed",
-    "Projection",
+    "proj_set_activation", "proj_run_fused", "PROJ_ACT_NONE", "PROJ_ACT_GELU", "Projection",
 ]
 
 PROJ_OK, PROJ_ERR_INVALID_ARG, PROJ_ERR_UNSUPPORTED, PROJ_ERR_MISALIGNED = 0, 1, 2, 3
@@ -38,12 +38,14 @@ PROJ_BF16, PROJ_F32 = 0, 1
 PROJ_W_NK, PROJ_W_KN = 0, 1
 PROJ_KERNEL_NONE, PROJ_KERNEL_FILL, PROJ_KERNEL_TC = 0, 1, 2
 PROJ_OVERLAP_NONE, PROJ_OVERLAP_PROLOGUE, PROJ_OVERLAP_WEIGHTS = 0, 1, 2
+PROJ_ACT_NONE, PROJ_ACT_GELU = 0, 1
 
 EXPORTED_SYMBOLS = (
     "proj_plan_compute", "proj_plan_segments", "proj_plan_reduction_order", "proj_create", "proj_run", "proj_run_host", "proj_device_status",
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "proj_run_noalloc",
     "proj_packed_weight_bytes", "proj_pack_weights", "proj_run_packed", "proj_run_host_packed",
+    "proj_set_activation", "proj_run_fused",
 )
 
 
@@ -120,6 +122,8 @@ def lib() -> ctypes.CDLL:
     L.proj_pack_weights.argtypes = [vp, vp, vp, vp]
     L.proj_run_packed.argtypes = [vp, vp, vp, vp, vp, vp]
     L.proj_run_host_packed.argtypes = [vp, vp, vp, vp, vp, vp]
+    L.proj_set_activation.argtypes = [vp, i32]
+    L.proj_run_fused.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp]
     for name in EXPORTED_SYMBOLS:
         if name != "proj_status_string":
             getattr(L, name).restype = st
@@ -240,6 +244,15 @@ def proj_run_host_packed(h: int, X_host, W_packed, bias, Y_host, stream=None) ->
                                       _stream(stream)), "proj_run_host_packed")
 
 
+def proj_set_activation(h: int, act: int) -> None:
+    _check(lib().proj_set_activation(h, int(act)), "proj_set_activation")
+
+
+def proj_run_fused(h: int, X, W, packed: bool, bias, residual, Y, stream=None) -> None:
+    _check(lib().proj_run_fused(h, _ptr(X), _ptr(W), int(bool(packed)), _ptr(bias), _ptr(residual),
+                                _ptr(Y), _stream(stream)), "proj_run_fused")
+
+
 def proj_device_status(h: int, stream=None) -> int:
     """Raw status (PROJ_OK or an error code); does not raise."""
     return int(lib().proj_device_status(h, _stream(stream)))
@@ -306,16 +319,23 @@ class Projection:
     def plan(self) -> dict:
         return proj_plan_info(self.handle)
 
-    def __call__(self, X, W, bias=None, out=None, stream=None, packed: bool = False):
-        """Y = X·Wᵀ (+ bias); ``packed=True`` takes weights from :meth:`pack`."""
+    def __call__(self, X, W, bias=None, out=None, stream=None, packed: bool = False, residual=None):
+        """Y = act(X·Wᵀ + bias) + residual; ``packed=True`` takes weights from
+        :meth:`pack`; the activation is set by :meth:`set_activation`."""
         import torch
         if out is None:
             dt = torch.float32 if self.y_dtype == PROJ_F32 else torch.bfloat16
             out = torch.empty((self.M, self.N), dtype=dt, device=X.device)
         if stream is None:
             stream = torch.cuda.current_stream(X.device)
-        (proj_run_packed if packed else proj_run)(self.handle, X, W, bias, out, stream)
+        if residual is not None:
+            proj_run_fused(self.handle, X, W, packed, bias, residual, out, stream)
+        else:
+            (proj_run_packed if packed else proj_run)(self.handle, X, W, bias, out, stream)
         return out
+
+    def set_activation(self, act: int) -> None:
+        proj_set_activation(self.handle, act)
 
     def pack(self, W, stream=None):
         """Repack weights into this handle's tile-contiguous layout (a preparation

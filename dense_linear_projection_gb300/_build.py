@@ -16,8 +16,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["proj_api.cu", "planner.cpp"]
+SOURCES = ["proj_api.cu", "planner.cpp", "kernel_tc_lean.cu", "kernel_tc_fused.cu"]
 HEADERS = [os.path.join(CSRC, "proj_internal.h"), os.path.join(CSRC, "proj_kernel.cuh"),
+           os.path.join(CSRC, "proj_aux.cuh"), os.path.join(CSRC, "proj_launch.h"),
            os.path.join(INCLUDE, "proj.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -12,8 +12,9 @@
 #include <new>
 
 #include "proj.h"
+#include "proj_aux.cuh"
 #include "proj_internal.h"
-#include "proj_kernel.cuh"
+#include "proj_launch.h"
 
 using namespace projgb;
 
@@ -37,6 +38,7 @@ struct proj_plan_s {
     int overlap = PROJ_OVERLAP_PROLOGUE;    // programmatic dependent launch mode
     int prefetch_stages = kMaxStages;       // PROJ_OVERLAP_WEIGHTS: W stages before the wait
     int sm_count = 0;
+    int act = 0;  // fused activation (proj_set_activation)
     // fp32 router weights: planned and run as [H | L] along K (2·kt k-blocks);
     // they exist only in packed form (the split happens in proj_pack_weights).
     int hilo = 0;
@@ -118,10 +120,7 @@ int64_t partial_bytes_of(const proj_plan_desc_t &plan) {
 bool set_kernel_smem_limit(int smem_optin) {
     // Also allow clusters above the portable 8 CTAs (GB300 runs 16); the
     // occupancy query in plan_for_device decides whether a size fits.
-    if (cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem_optin) != cudaSuccess ||
-        cudaFuncSetAttribute(dev::proj_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess) {
+    if (tc_configure_lean(smem_optin) != cudaSuccess || tc_configure_fused(smem_optin) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -168,7 +167,7 @@ proj_status_t plan_for_device(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_
         if (st != PROJ_OK || plan->cluster_split < 2) return st;
         TcLaunch l(*plan, nullptr, false);
         int clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&clusters, dev::proj_tc_kernel, &l.cfg) == cudaSuccess &&
+        if (tc_max_active_clusters(&clusters, &l.cfg) == cudaSuccess &&
             static_cast<int64_t>(clusters) >= plan->tiles_sk)
             return PROJ_OK;
         cudaGetLastError();
@@ -346,7 +345,7 @@ int64_t packed_rows(const proj_plan_desc_t &plan) {
 }
 
 proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packed, const void *bias,
-                       void *Y, void *stream);
+                       const void *residual, void *Y, void *stream);
 
 }  // namespace
 
@@ -354,12 +353,12 @@ extern "C" {
 
 proj_status_t proj_run(proj_handle_t h, const void *X, const void *W, const void *bias, void *Y,
                        void *stream) {
-    return run_impl(h, X, W, false, bias, Y, stream);
+    return run_impl(h, X, W, false, bias, nullptr, Y, stream);
 }
 
 proj_status_t proj_run_packed(proj_handle_t h, const void *X, const void *W_packed, const void *bias,
                               void *Y, void *stream) {
-    return run_impl(h, X, W_packed, true, bias, Y, stream);
+    return run_impl(h, X, W_packed, true, bias, nullptr, Y, stream);
 }
 
 proj_status_t proj_packed_weight_bytes(proj_handle_t h, size_t *bytes) {
@@ -399,7 +398,7 @@ proj_status_t proj_pack_weights(proj_handle_t h, const void *W, void *W_packed, 
 namespace {
 
 proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packed, const void *bias,
-                       void *Y, void *stream) {
+                       const void *residual, void *Y, void *stream) {
     if (!h) return PROJ_ERR_INVALID_ARG;
     if (h->hilo && !packed && h->plan.kernel == PROJ_KERNEL_TC) return PROJ_ERR_UNSUPPORTED;
     if ((bias != nullptr) != (h->has_bias != 0)) return PROJ_ERR_INVALID_ARG;
@@ -408,12 +407,13 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     if (!Y) return PROJ_ERR_INVALID_ARG;
     const size_t y_align = h->y_dtype == PROJ_F32 ? 4 : 2;
     if (reinterpret_cast<uintptr_t>(Y) % y_align != 0) return PROJ_ERR_MISALIGNED;
+    if (residual && reinterpret_cast<uintptr_t>(residual) % y_align != 0) return PROJ_ERR_MISALIGNED;
     if (bias && reinterpret_cast<uintptr_t>(bias) % 2 != 0) return PROJ_ERR_MISALIGNED;
     cudaStream_t s = as_stream(stream);
 
     if (plan.kernel == PROJ_KERNEL_FILL) {
         dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(
-            h->M, h->N, static_cast<const uint16_t *>(bias), Y, h->y_dtype == PROJ_F32);
+            h->M, h->N, static_cast<const uint16_t *>(bias), Y, h->y_dtype == PROJ_F32, h->act, residual);
         return check_launch();
     }
 
@@ -455,7 +455,10 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     }
     kp.bias = static_cast<const uint16_t *>(bias);
     kp.Y = Y;
-    kp.y_vec = y_vec_of(Y, h->N, h->y_dtype);
+    kp.act = h->act;
+    kp.residual = residual;
+    // Vector stores read the residual the same way: both 16-byte aligned.
+    kp.y_vec = y_vec_of(Y, h->N, h->y_dtype) && (!residual || aligned16(residual));
     kp.trace = h->trace;
     // Weights stream early only when every SM has a CTA: the next kernel's
     // CTAs then start as the preceding kernel's leave, in its tail.  With SMs
@@ -464,7 +467,9 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     kp.w_prefetch =
         h->overlap == PROJ_OVERLAP_WEIGHTS && plan.grid >= h->sm_count ? h->prefetch_stages : 0;
     TcLaunch l(plan, s, h->overlap != PROJ_OVERLAP_NONE);
-    if (cudaLaunchKernelEx(&l.cfg, dev::proj_tc_kernel, kp, packed ? h->map_wp : h->map_w, h->map_x) !=
+    const bool fused = kp.act != 0 || kp.residual != nullptr;
+    const CUtensorMap &map_w = packed ? h->map_wp : h->map_w;
+    if ((fused ? tc_launch_fused(&l.cfg, kp, map_w, h->map_x) : tc_launch_lean(&l.cfg, kp, map_w, h->map_x)) !=
         cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
@@ -516,7 +521,7 @@ proj_status_t run_host_impl(proj_handle_t h, const void *X_host, const void *W, 
     cudaStream_t s = as_stream(stream);
     if (xb && cudaMemcpyAsync(h->stage_x, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return PROJ_ERR_CUDA;
-    proj_status_t st = run_impl(h, h->stage_x, W, packed, bias, h->stage_y, stream);
+    proj_status_t st = run_impl(h, h->stage_x, W, packed, bias, nullptr, h->stage_y, stream);
     if (st != PROJ_OK) return st;
     if (cudaMemcpyAsync(Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return PROJ_ERR_CUDA;
@@ -544,6 +549,19 @@ proj_status_t proj_device_status(proj_handle_t h, void *stream) {
                    static_cast<size_t>(plan.scratch_bytes - partial_bytes)) != cudaSuccess)
         return PROJ_ERR_CUDA;
     return what;
+}
+
+proj_status_t proj_set_activation(proj_handle_t h, proj_activation_t act) {
+    if (!h) return PROJ_ERR_INVALID_ARG;
+    if (act != PROJ_ACT_NONE && act != PROJ_ACT_GELU) return PROJ_ERR_INVALID_ARG;
+    h->act = act;
+    return PROJ_OK;
+}
+
+proj_status_t proj_run_fused(proj_handle_t h, const void *X, const void *W, int packed, const void *bias,
+                             const void *residual, void *Y, void *stream) {
+    if (packed != 0 && packed != 1) return PROJ_ERR_INVALID_ARG;
+    return run_impl(h, X, W, packed != 0, bias, residual, Y, stream);
 }
 
 proj_status_t proj_set_overlap(proj_handle_t h, proj_overlap_t mode) {
@@ -687,7 +705,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     if (st != PROJ_OK) return st;
     if (plan.kernel == PROJ_KERNEL_FILL) {
         dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(M, N, static_cast<const uint16_t *>(bias),
-                                                                 Y, y_dtype == PROJ_F32);
+                                                                 Y, y_dtype == PROJ_F32, 0, nullptr);
         return check_launch();
     }
     // The plan's scratch must fit the static array; larger problems are refused.
@@ -732,7 +750,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
     kp.trace = nullptr;
     TcLaunch l(plan, s, false);
-    if (cudaLaunchKernelEx(&l.cfg, dev::proj_tc_kernel, kp, map_w, map_x) != cudaSuccess) {
+    if (tc_launch_lean(&l.cfg, kp, map_w, map_x) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }

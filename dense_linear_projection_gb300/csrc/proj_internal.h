@@ -111,7 +111,9 @@ struct KernelParams {
     int32_t y_vec;         // Y rows start 16-byte aligned (N·size % 16 == 0, aligned base)
     int64_t wait_limit_ns; // bounded device waits give up after this long
     int32_t w_prefetch;    // stages of W streamed before the preceding kernel completes (0: none)
+    int32_t act;           // fused activation: 0 none, 1 GELU (on projection + bias)
     const uint16_t *bias;  // [N] bf16 or nullptr
+    const void *residual;  // [M,N] in Y's dtype, added after the activation, or nullptr (may alias Y)
     void *Y;
     float *partials;       // [2*grid][128 rows][b_rows] fp32 partial tiles
     uint32_t *counters;    // [4 * (tiles - tiles_dp)]: one per (split tile, row quarter)

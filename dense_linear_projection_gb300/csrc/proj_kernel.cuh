@@ -328,11 +328,96 @@ __device__ __forceinline__ void trace_stamp(const KernelParams &p, int slot) {
     if (p.trace) p.trace[static_cast<size_t>(blockIdx.x) * kTraceSlots + slot] = globaltimer_ns();
 }
 
+// Fused epilogue (the FFN activation written once; a residual added back):
+// y = act(projection + bias) + residual, in fp32, then one rounding to the
+// output type.  GELU is x/2 · (1 + erf(x/√2)).  The tensor-core kernel is
+// built twice: kFused = false leaves all of this out of the default path.
+__device__ __forceinline__ float gelu_f32(float v) {
+    return 0.5f * v * (1.0f + erff(v * 0.7071067811865476f));
+}
+
+// Out of line, four values a call (passed in registers): one copy of the code
+// instead of one per unrolled store site (the epilogue runs once per tile,
+// from a cold instruction cache), one call per four values.
+static __device__ __noinline__ float4 gelu4(float4 v) {
+    return make_float4(gelu_f32(v.x), gelu_f32(v.y), gelu_f32(v.z), gelu_f32(v.w));
+}
+
+// The activation over n values (n a multiple of 4), four per call.
+template <bool kFused, int n>
+__device__ __forceinline__ void apply_act_n(const KernelParams &p, float *v) {
+    if constexpr (kFused) {
+        if (p.act == 1) {
+#pragma unroll
+            for (int i = 0; i < n; i += 4) {
+                const float4 g = gelu4(make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                v[i] = g.x;
+                v[i + 1] = g.y;
+                v[i + 2] = g.z;
+                v[i + 3] = g.w;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ float residual_at(const KernelParams &p, size_t off) {
+    return p.y_f32 ? static_cast<const float *>(p.residual)[off]
+                   : __bfloat162float(static_cast<const __nv_bfloat16 *>(p.residual)[off]);
+}
+
+// 4 consecutive residual values (16-byte aligned fp32, or 8-byte aligned bf16).
+__device__ __forceinline__ float4 residual4(const KernelParams &p, size_t off) {
+    if (p.y_f32) return *reinterpret_cast<const float4 *>(static_cast<const float *>(p.residual) + off);
+    const uint2 u = *reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p.residual) + off);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// One output value (+ residual), rounded to Y's type.
+template <bool kFused>
 __device__ __forceinline__ void store_y(const KernelParams &p, size_t off, float y) {
+    if constexpr (kFused)
+        if (p.residual) y += residual_at(p, off);
     if (p.y_f32)
         static_cast<float *>(p.Y)[off] = y;
     else
         static_cast<__nv_bfloat16 *>(p.Y)[off] = __float2bfloat16_rn(y);
+}
+
+// 8 consecutive outputs at a 16-byte aligned offset (+ residual): one fp32
+// pair of float4 stores or one bf16 16-byte store.
+template <bool kFused>
+__device__ __forceinline__ void store_y8(const KernelParams &p, size_t off, float4 a, float4 b) {
+    if constexpr (kFused)
+        if (p.residual) {
+            a = add4(a, residual4(p, off));
+            b = add4(b, residual4(p, off + 4));
+        }
+    if (p.y_f32) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.Y) + off);
+        dst[0] = a;
+        dst[1] = b;
+    } else {
+        *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) + off) =
+            make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+    }
+}
+
+// 4 consecutive fp32 outputs at a 16-byte aligned offset (+ residual).
+template <bool kFused>
+__device__ __forceinline__ void store_y4_f32(const KernelParams &p, size_t off, float4 v) {
+    if constexpr (kFused)
+        if (p.residual) v = add4(v, residual4(p, off));
+    *reinterpret_cast<float4 *>(static_cast<float *>(p.Y) + off) = v;
 }
 
 // Acquire-release add at GPU scope: one lane publishes the partial sums its
@@ -385,6 +470,7 @@ static_assert(sizeof(SmemCtl) + 1023 <= kSmemReserve, "the reserve holds SmemCtl
 // ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_tc_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_x) {
@@ -684,8 +770,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
             const bool stamp_split = s.split && !split_traced && warp == 2 && lane == 0;
             if (s.split) split_traced = true;
-            // Store one chunk of 16 columns of this lane's row (+ bias).
-            // Store one chunk of 16 columns of this lane's row (+ bias).  Every
+            // Store one chunk of 16 columns of this lane's row (+ bias, the
+            // activation and the residual).  Every
             // lane of the warp calls it (the swapped path shuffles through
             // shared memory).
             auto store_chunk = [&](int32_t ch, const float (&y)[16]) {
@@ -698,31 +784,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t nw = n0 + q * 32;    // first weight row of the warp
                     if (p.y_vec && nw + 32 <= p.N && mb + 16 <= p.M) {
                         float *t = ctl->y_tile[q];
+                        float a16[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) t[i * kYTileStride + lane] = y[i] + bias_lane;
+                        for (int i = 0; i < 16; ++i) a16[i] = y[i] + bias_lane;
+                        apply_act_n<kFused, 16>(p, a16);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) t[i * kYTileStride + lane] = a16[i];
                         __syncwarp();
                         if (p.y_f32) {
 #pragma unroll
                             for (int pass = 0; pass < 4; ++pass) {
                                 const int32_t mi = pass * 4 + lane / 8, nc = (lane % 8) * 4;
-                                const float4 v = *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc);
-                                *reinterpret_cast<float4 *>(static_cast<float *>(p.Y) +
-                                                            static_cast<size_t>(mb + mi) * p.N + nw + nc) = v;
+                                store_y4_f32<kFused>(p, static_cast<size_t>(mb + mi) * p.N + nw + nc,
+                                             *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc));
                             }
                         } else {
 #pragma unroll
                             for (int pass = 0; pass < 2; ++pass) {
                                 const int32_t mi = pass * 8 + lane / 4, nc = (lane % 4) * 8;
-                                const float4 a = *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc);
-                                const float4 b = *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc + 4);
-                                __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y);
-                                __nv_bfloat162 h1 = __floats2bfloat162_rn(a.z, a.w);
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y);
-                                __nv_bfloat162 h3 = __floats2bfloat162_rn(b.z, b.w);
-                                *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) +
-                                                           static_cast<size_t>(mb + mi) * p.N + nw + nc) =
-                                    make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
-                                               *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+                                store_y8<kFused>(p, static_cast<size_t>(mb + mi) * p.N + nw + nc,
+                                         *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc),
+                                         *reinterpret_cast<const float4 *>(t + mi * kYTileStride + nc + 4));
                             }
                         }
                         __syncwarp();  // the tile is reused by the next chunk
@@ -730,10 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (!lane_ok) return;
                     const int32_t n = lane_row;
+                    float a16[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) a16[i] = y[i] + bias_lane;
+                    apply_act_n<kFused, 16>(p, a16);
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int32_t m = mb + i;
-                        if (m < p.M) store_y(p, static_cast<size_t>(m) * p.N + n, y[i] + bias_lane);
+                        if (m < p.M) store_y<kFused>(p, static_cast<size_t>(m) * p.N + n, a16[i]);
                     }
                 } else {
                     if (!lane_ok) return;
@@ -742,36 +828,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float v[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = y[i] + (p.bias != nullptr ? bias_s[ch * 16 + i] : 0.f);
+                    apply_act_n<kFused, 16>(p, v);
                     const size_t off = static_cast<size_t>(m) * p.N + nb;
                     if (p.y_vec && nb + 16 <= p.N) {
                         // 16 consecutive outputs of one row: vector stores.
-                        if (p.y_f32) {
-                            float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.Y) + off);
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-                        } else {
-                            uint32_t w[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
-                                w[i] = *reinterpret_cast<uint32_t *>(&h);
-                            }
-                            uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) + off);
-                            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                        }
+                        for (int i = 0; i < 2; ++i)
+                            store_y8<kFused>(p, off + 8 * i, make_float4(v[8 * i], v[8 * i + 1], v[8 * i + 2], v[8 * i + 3]),
+                                     make_float4(v[8 * i + 4], v[8 * i + 5], v[8 * i + 6], v[8 * i + 7]));
                     } else {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            if (nb + i < p.N) store_y(p, off + i, v[i]);
+                            if (nb + i < p.N) store_y<kFused>(p, off + i, v[i]);
                     }
                 }
             };
             // Token-major: store 32 columns [n0 + 16·ch, +32) of the warp's 32
-            // token rows (+ bias).  Each lane holds one row, so the block goes
-            // through shared memory and leaves as whole row segments (bf16: 8
-            // rows of 64 bytes per store instruction, fp32: 4 rows of 128),
+            // token rows (+ bias, activation, residual).  Each lane holds one
+            // row, so the block goes through shared memory and leaves as whole
+            // row segments (bf16: 8 rows of 64 bytes per store instruction,
+            // fp32: 4 rows of 128),
             // not 32 rows touched by every instruction.  Every lane calls it.
             auto store_cols32 = [&](int32_t ch, const float *y) {
                 const int32_t nb = n0 + ch * 16;
@@ -780,32 +856,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float b[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) b[i] = y[i] + (p.bias != nullptr ? bias_s[ch * 16 + i] : 0.f);
-                if (p.y_f32) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        *reinterpret_cast<float4 *>(t + lane * kYTileStride + 4 * j) =
-                            make_float4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
-                    __syncwarp();
-#pragma unroll
-                    for (int pass = 0; pass < 8; ++pass) {
-                        const int32_t r = pass * 4 + lane / 8, c = (lane % 8) * 4;
-                        if (mw + r < p.M)
-                            *reinterpret_cast<float4 *>(static_cast<float *>(p.Y) +
-                                                        static_cast<size_t>(mw + r) * p.N + nb + c) =
-                                *reinterpret_cast<const float4 *>(t + r * kYTileStride + c);
-                    }
-                } else {
+                apply_act_n<kFused, 32>(p, b);
+                bool with_residual = false;
+                if constexpr (kFused) with_residual = p.residual != nullptr;
+                if (!p.y_f32 && !with_residual) {
+                    // bf16 without a residual: stage the rounded values (64-byte
+                    // rows, stride 80 bytes: conflict-free 16-byte accesses).
                     uint8_t *tb = reinterpret_cast<uint8_t *>(t);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            __nv_bfloat162 h = __floats2bfloat162_rn(b[8 * j + 2 * k], b[8 * j + 2 * k + 1]);
-                            w4[k] = *reinterpret_cast<uint32_t *>(&h);
-                        }
-                        *reinterpret_cast<uint4 *>(tb + lane * 80 + 16 * j) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                    }
+                    for (int j = 0; j < 4; ++j)
+                        *reinterpret_cast<uint4 *>(tb + lane * 80 + 16 * j) =
+                            make_uint4(pack_bf16x2(b[8 * j], b[8 * j + 1]), pack_bf16x2(b[8 * j + 2], b[8 * j + 3]),
+                                       pack_bf16x2(b[8 * j + 4], b[8 * j + 5]), pack_bf16x2(b[8 * j + 6], b[8 * j + 7]));
                     __syncwarp();
 #pragma unroll
                     for (int pass = 0; pass < 4; ++pass) {
@@ -814,6 +876,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) +
                                                        static_cast<size_t>(mw + r) * p.N + nb + c) =
                                 *reinterpret_cast<const uint4 *>(tb + r * 80 + c * 2);
+                    }
+                    __syncwarp();  // the staging area is reused by the next block
+                    return;
+                }
+                // fp32 staging otherwise: a residual is added before the one
+                // rounding.  The block's residual values are all loaded before
+                // they are used (one memory round trip per block, not one per
+                // store).
+                if (p.y_f32) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4 *>(t + lane * kYTileStride + 4 * j) =
+                            make_float4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+                    float4 res[8];
+                    if constexpr (kFused) {
+#pragma unroll
+                        for (int pass = 0; pass < 8; ++pass) {
+                            const int32_t r = pass * 4 + lane / 8, c = (lane % 8) * 4;
+                            res[pass] = (with_residual && mw + r < p.M)
+                                            ? residual4(p, static_cast<size_t>(mw + r) * p.N + nb + c)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int pass = 0; pass < 8; ++pass) {
+                        const int32_t r = pass * 4 + lane / 8, c = (lane % 8) * 4;
+                        float4 v = *reinterpret_cast<const float4 *>(t + r * kYTileStride + c);
+                        if constexpr (kFused) v = add4(v, res[pass]);
+                        if (mw + r < p.M)
+                            *reinterpret_cast<float4 *>(static_cast<float *>(p.Y) +
+                                                        static_cast<size_t>(mw + r) * p.N + nb + c) = v;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<float4 *>(t + lane * kYTileStride + 4 * j) =
+                            make_float4(b[4 * j], b[4 * j + 1], b[4 * j + 2], b[4 * j + 3]);
+                    uint4 res[4];
+                    if constexpr (kFused) {
+#pragma unroll
+                        for (int pass = 0; pass < 4; ++pass) {
+                            const int32_t r = pass * 8 + lane / 4, c = (lane % 4) * 8;
+                            res[pass] = (with_residual && mw + r < p.M)
+                                            ? *reinterpret_cast<const uint4 *>(
+                                                  static_cast<const __nv_bfloat16 *>(p.residual) +
+                                                  static_cast<size_t>(mw + r) * p.N + nb + c)
+                                            : make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int pass = 0; pass < 4; ++pass) {
+                        const int32_t r = pass * 8 + lane / 4, c = (lane % 4) * 8;
+                        float4 a = *reinterpret_cast<const float4 *>(t + r * kYTileStride + c);
+                        float4 bb = *reinterpret_cast<const float4 *>(t + r * kYTileStride + c + 4);
+                        if constexpr (kFused) {
+                            const uint4 u = res[pass];
+                            a = add4(a, make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                                                    __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)));
+                            bb = add4(bb, make_float4(__uint_as_float(u.z << 16), __uint_as_float(u.z & 0xFFFF0000u),
+                                                      __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xFFFF0000u)));
+                        }
+                        if (mw + r < p.M)
+                            *reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.Y) +
+                                                       static_cast<size_t>(mw + r) * p.N + nb + c) =
+                                make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(bb.x, bb.y),
+                                           pack_bf16x2(bb.z, bb.w));
                     }
                 }
                 __syncwarp();  // the staging area is reused by the next block
@@ -1078,137 +1208,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
-    }
-}
-
-// Weight packing (preparation, not part of a run): packed block (tn, kb) holds
-// rows tn·block_n + r, r < block_n, and K positions kb·64 + c, c < 64, K
-// contiguous; positions past N or K are zero.  One thread writes 16 bytes (8
-// values).  [N,K] weights: consecutive threads take consecutive K chunks of a
-// row (contiguous reads); [K,N] weights: consecutive threads take consecutive
-// rows of one K chunk (contiguous reads along N).
-__global__ void proj_pack_kernel(const uint16_t *W, uint16_t *P, int64_t N, int64_t K, int w_kn,
-                                 int32_t block_n, int64_t k_blocks, int64_t chunks) {
-    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < chunks;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        int64_t blk, r, c8;
-        if (!w_kn) {
-            c8 = e & 7;
-            const int64_t row = e >> 3;
-            blk = row / block_n;
-            r = row - blk * block_n;
-        } else {
-            const int64_t per_blk = static_cast<int64_t>(block_n) * 8;
-            blk = e / per_blk;
-            const int64_t rem = e - blk * per_blk;
-            c8 = rem / block_n;
-            r = rem - c8 * block_n;
-        }
-        const int64_t tn = blk / k_blocks;
-        const int64_t kb = blk - tn * k_blocks;
-        const int64_t n = tn * block_n + r;
-        const int64_t k0 = kb * 64 + c8 * 8;
-        uint4 out = make_uint4(0u, 0u, 0u, 0u);
-        if (n < N && k0 < K) {  // K % 8 == 0: the 8 values are all in range
-            if (!w_kn) {
-                out = *reinterpret_cast<const uint4 *>(W + n * K + k0);
-            } else {
-                uint32_t w[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    w[j] = static_cast<uint32_t>(W[(k0 + 2 * j) * N + n]) |
-                           (static_cast<uint32_t>(W[(k0 + 2 * j + 1) * N + n]) << 16);
-                out = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
-        *reinterpret_cast<uint4 *>(P + ((blk * block_n + r) * 64 + c8 * 8)) = out;
-    }
-}
-
-// fp32 router weights ("How I made Muse's GPU projections 1.32× faster in the
-// Open Kernel Challenge", section "Why the high-plus-low router scheme
-// helped"): H = roundBF16(W), R = W − FP32(H) (an fp32 subtraction), L =
-// roundBF16(R), packed as [H | L] along K: packed k-block kb' < kt holds H's
-// k-block kb', kb' >= kt holds L's k-block kb' − kt (kt = k-blocks of K), in
-// the block layout of proj_pack_kernel.  One thread writes 16 bytes.
-__global__ void proj_pack_hilo_kernel(const float *W, uint16_t *P, int64_t N, int64_t K, int w_kn,
-                                      int32_t block_n, int64_t k_blocks, int64_t kt, int64_t chunks) {
-    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < chunks;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        int64_t blk, r, c8;
-        if (!w_kn) {
-            c8 = e & 7;
-            const int64_t row = e >> 3;
-            blk = row / block_n;
-            r = row - blk * block_n;
-        } else {
-            const int64_t per_blk = static_cast<int64_t>(block_n) * 8;
-            blk = e / per_blk;
-            const int64_t rem = e - blk * per_blk;
-            c8 = rem / block_n;
-            r = rem - c8 * block_n;
-        }
-        const int64_t tn = blk / k_blocks;
-        const int64_t kbp = blk - tn * k_blocks;
-        const bool low = kbp >= kt;
-        const int64_t n = tn * block_n + r;
-        const int64_t k0 = (low ? kbp - kt : kbp) * 64 + c8 * 8;
-        uint32_t w4[4] = {0u, 0u, 0u, 0u};
-        if (n < N && k0 < K) {  // K % 8 == 0: the 8 values are all in range
-            float v[8];
-            if (!w_kn) {
-                const float4 a = *reinterpret_cast<const float4 *>(W + n * K + k0);
-                const float4 b = *reinterpret_cast<const float4 *>(W + n * K + k0 + 4);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = W[(k0 + j) * N + n];
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint16_t h2[2];
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const float w = v[2 * j + t];
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-                    const __nv_bfloat16 part = low ? __float2bfloat16_rn(__fsub_rn(w, __bfloat162float(hi))) : hi;
-                    h2[t] = *reinterpret_cast<const uint16_t *>(&part);
-                }
-                w4[j] = static_cast<uint32_t>(h2[0]) | (static_cast<uint32_t>(h2[1]) << 16);
-            }
-        }
-        *reinterpret_cast<uint4 *>(P + ((blk * block_n + r) * 64 + c8 * 8)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-    }
-}
-
-// K == 0: every sum is empty, so Y = bias (or 0).
-__global__ void proj_fill_kernel(int64_t M, int64_t N, const uint16_t *bias, void *Y, int y_f32) {
-    const int64_t total = M * N;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t n = i % N;
-        const float y = bias ? bf16_bits_to_float(bias[n]) : 0.f;
-        if (y_f32)
-            static_cast<float *>(Y)[i] = y;
-        else
-            static_cast<__nv_bfloat16 *>(Y)[i] = __float2bfloat16_rn(y);
-    }
-}
-
-// Self-test of the bounded wait: a barrier nothing arrives on.
-__global__ void proj_selftest_wait_kernel(int64_t limit_ns, int *status) {
-    __shared__ uint64_t bar;
-    __shared__ int abort_flag;
-    if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&bar), 1);
-        abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const bool ok = wait_phase(smem_u32(&bar), 0, &abort_flag, status, kErrSelfTest, limit_ns);
-        if (ok) atomicOr(status, 1 << 30);  // would mean the wait completed: it must not
     }
 }
 

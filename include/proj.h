@@ -259,6 +259,33 @@ proj_status_t proj_packed_weight_bytes(proj_handle_t h, size_t *bytes);
 proj_status_t proj_pack_weights(proj_handle_t h, const void *W, void *W_packed, void *stream);
 proj_status_t proj_run_packed(proj_handle_t h, const void *X, const void *W_packed,
                               const void *bias, void *Y, void *stream);
+/*
+ * Fused epilogues.  The worklog's second page writes the FFN intermediate
+ * once by fusing its GELU into the projection's epilogue, and fuses the
+ * residual add that follows an output projection; the first page, section
+ * "Normalization and residuals also cost time", says why: the extra pass
+ * over the activations costs time of its own.
+ *
+ *   Y = act(X·Wᵀ + bias) + residual,
+ *
+ * computed in fp32 and rounded once to Y's type.  act is the handle's
+ * activation (proj_set_activation; PROJ_ACT_NONE by default): PROJ_ACT_GELU
+ * is GELU(x) = x/2 · (1 + erf(x/√2)).  residual is an [M,N] array in Y's
+ * type and layout, or NULL; it may be Y itself (each element is read before
+ * it is written).  proj_run_fused: packed = 1 takes packed weights (as
+ * proj_run_packed), 0 weights as stored; otherwise as proj_run.
+ * PROJ_ERR_INVALID_ARG for an unknown activation or packed flag;
+ * PROJ_ERR_MISALIGNED for a residual not aligned to Y's element size.
+ */
+typedef enum proj_activation {
+    PROJ_ACT_NONE = 0,
+    PROJ_ACT_GELU = 1
+} proj_activation_t;
+
+proj_status_t proj_set_activation(proj_handle_t h, proj_activation_t act);
+proj_status_t proj_run_fused(proj_handle_t h, const void *X, const void *W, int packed,
+                             const void *bias, const void *residual, void *Y, void *stream);
+
 /* proj_run_host with packed weights (W_packed on the device). */
 proj_status_t proj_run_host_packed(proj_handle_t h, const void *X_host, const void *W_packed,
                                    const void *bias, void *Y_host, void *stream);
