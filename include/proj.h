@@ -67,7 +67,7 @@ typedef struct proj_plan_s *proj_handle_t;
 typedef enum proj_status {
     PROJ_OK = 0,
     PROJ_ERR_INVALID_ARG = 1,    /* bad shape, NULL pointer, bias/has_bias mismatch */
-    PROJ_ERR_UNSUPPORTED = 2,    /* dtype or device this build does not handle */
+    PROJ_ERR_UNSUPPORTED = 2,    /* dtype or device this library does not handle */
     PROJ_ERR_MISALIGNED = 3,     /* a TMA alignment rule above is violated */
     PROJ_ERR_OUT_OF_MEMORY = 4,  /* scratch allocation failed */
     PROJ_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed */
@@ -213,6 +213,18 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
  * Allocates scratch with cudaMalloc (PROJ_ERR_OUT_OF_MEMORY on failure).
  * The device must be compute capability 10.3 (GB300); else PROJ_ERR_UNSUPPORTED.
  * On failure *out is set to NULL.
+ *
+ * Tuning overrides (environment, read once here; for experiments and tests,
+ * every plan they produce computes the same projection):
+ *   PROJ_FORCE_BLOCK_T=t     swapped orientation with token tile t (multiple of 16)
+ *   PROJ_FORCE_BLOCK_N=n     token-major orientation with weight tile n
+ *   PROJ_MAX_CLUSTER=s       largest cluster split (0 or 1: none)
+ *   PROJ_CLUSTER_FILL_PCT=f  SMs (%) a cluster split must keep busy
+ *   PROJ_FORCE_STAGES=k      fewer pipeline stages than planned
+ *   PROJ_FORCE_GRID=g        fewer CTAs for an all-split plan
+ *   PROJ_FORCE_WHOLE_TILES=1 no split tiles
+ *   PROJ_FORCE_RASTER_GROUP=r token tiles per raster group
+ *   PROJ_PREFETCH_STAGES=k   weight stages streamed early in PROJ_OVERLAP_WEIGHTS
  */
 proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
                           proj_wlayout_t w_layout, proj_dtype_t x_dtype,

@@ -3,7 +3,7 @@
 "How I made Muse's GPU projections 1.32× faster in the Open Kernel
 Challenge", section "Why the high-plus-low router scheme helped": H =
 roundBF16(W), L = roundBF16(W − FP32(H)), Y = X·Hᵀ + X·Lᵀ in fp32.  The
-output is judged against the exact fp32-weight product by the router contract
+output is compared with the exact fp32-weight product under the router contract
 of section "The actual error rule, including what L2 means" (values in
 tests/golden/router_hilo.txt): whole-output relative L2 within 0.01 %; each
 row within five times that, with its denominator its own norm or one tenth of
