@@ -74,6 +74,10 @@ def _lib():
         lib.oracle_gelu.restype = ctypes.c_double
         lib.oracle_apply_activation.argtypes = [i64, ctypes.c_int, vp]
         lib.oracle_apply_activation.restype = None
+        lib.oracle_silu.argtypes = [ctypes.c_double]
+        lib.oracle_silu.restype = ctypes.c_double
+        lib.oracle_swiglu.argtypes = [i64, vp, vp, vp]
+        lib.oracle_swiglu.restype = None
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         _LIB = lib
@@ -186,7 +190,7 @@ def project_hilo(X, W, w_layout: int = W_NK, bias=None) -> np.ndarray:
     return project(X, H, w_layout, bias) + project(X, L, w_layout, None)
 
 
-ACT_NONE, ACT_GELU = 0, 1
+ACT_NONE, ACT_GELU, ACT_SWIGLU = 0, 1, 2
 
 
 def gelu(x) -> np.ndarray:
@@ -205,6 +209,32 @@ def project_fused(X, W, w_layout: int = W_NK, bias=None, act: int = ACT_NONE,
         raise ValueError("act must be ACT_NONE or ACT_GELU")
     if Y.size:
         _lib().oracle_apply_activation(Y.size, int(act), Y.ctypes.data)
+    if residual is not None:
+        Y = Y + np.asarray(residual, dtype=np.float64)
+    return Y
+
+
+def silu(x) -> np.ndarray:
+    """SiLU(x) = x·σ(x) of fp64 values, one by one."""
+    lib = _lib()
+    flat = np.asarray(x, dtype=np.float64).ravel()
+    return np.array([lib.oracle_silu(float(v)) for v in flat]).reshape(np.shape(x))
+
+
+def project_swiglu(X, W, w_layout: int = W_NK, residual=None) -> np.ndarray:
+    """SwiGLU of the stacked projection: W holds the gate rows then the up rows
+    ([2F,K] for W_NK, [K,2F] for W_KN); Y[m,f] = SiLU(G[m,f])·U[m,f] (+ residual),
+    with G = X·W_gateᵀ and U = X·W_upᵀ in fp64."""
+    GU = np.ascontiguousarray(project(X, W, w_layout, None))
+    M, N2 = GU.shape
+    if N2 % 2:
+        raise ValueError("SwiGLU weights stack 2F rows")
+    F = N2 // 2
+    G = np.ascontiguousarray(GU[:, :F])
+    U = np.ascontiguousarray(GU[:, F:])
+    Y = np.empty((M, F), dtype=np.float64)
+    if Y.size:
+        _lib().oracle_swiglu(Y.size, G.ctypes.data, U.ctypes.data, Y.ctypes.data)
     if residual is not None:
         Y = Y + np.asarray(residual, dtype=np.float64)
     return Y

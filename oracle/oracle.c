@@ -155,6 +155,20 @@ double oracle_gelu(double x) {
     return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));
 }
 
+/* SwiGLU's gate nonlinearity (Shazeer, "GLU Variants Improve Transformer",
+ * 2020): SiLU(x) = x · σ(x) = x / (1 + e^(−x)).  The first page's
+ * expert pattern ("produces a gate vector and an up vector, transforms the
+ * gate with a nonlinear function, multiplies the two vectors elementwise")
+ * leaves the function unnamed; SwiGLU names it. */
+double oracle_silu(double x) {
+    return x / (1.0 + exp(-x));
+}
+
+/* SwiGLU of a gate and an up array: out[i] = SiLU(gate[i]) · up[i]. */
+void oracle_swiglu(int64_t count, const double *gate, const double *up, double *out) {
+    for (int64_t i = 0; i < count; ++i) out[i] = oracle_silu(gate[i]) * up[i];
+}
+
 /* In place over `count` values: act 0 = identity, 1 = GELU. */
 void oracle_apply_activation(int64_t count, int act, double *v) {
     if (act == 1)

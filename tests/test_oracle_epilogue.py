@@ -57,3 +57,36 @@ def test_fused_epilogue_order_and_residual():
     # No activation, no residual: the plain projection.
     assert np.array_equal(oracle.project_fused(X2, Wn, oracle.W_NK, None),
                           oracle.project(X2, Wn, oracle.W_NK, None))
+
+
+def test_silu_definition_against_logistic():
+    rng = np.random.default_rng(22)
+    x = np.concatenate([rng.standard_normal(2000) * 4.0, [0.0, 1.0, -1.0, 20.0, -20.0]])
+    assert np.allclose(oracle.silu(x), x * scipy_special.expit(x), rtol=1e-13, atol=1e-300)
+    # σ(x) + σ(−x) = 1, so SiLU(x) − SiLU(−x) = x.
+    assert np.allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=0, atol=1e-12)
+    assert oracle.silu([0.0])[0] == 0.0
+
+
+def test_swiglu_gates_the_up_projection():
+    # W = [W_gate; W_up]: Y = SiLU(X·W_gateᵀ) · (X·W_upᵀ).
+    rng = np.random.default_rng(23)
+    M, F, K = 3, 5, 16
+    Xf = rng.integers(-2, 3, size=(M, K)).astype(np.float64)
+    Wg = rng.integers(-2, 3, size=(F, K)).astype(np.float64)
+    Wu = rng.integers(-2, 3, size=(F, K)).astype(np.float64)
+    X, W = _bits(Xf), _bits(np.vstack([Wg, Wu]))
+    G, U = Xf @ Wg.T, Xf @ Wu.T
+    want = G * scipy_special.expit(G) * U
+    got = oracle.project_swiglu(X, W)
+    assert np.allclose(got, want, rtol=1e-13, atol=1e-13)
+    # The gate, not the up half, goes through the nonlinearity: swapping the
+    # halves changes the result.
+    assert not np.allclose(oracle.project_swiglu(X, _bits(np.vstack([Wu, Wg]))), want)
+    # [K,2F] storage gives the same result; a residual is added last.
+    R = np.arange(M * F, dtype=np.float64).reshape(M, F)
+    assert np.allclose(oracle.project_swiglu(X, np.ascontiguousarray(W.T), oracle.W_KN, R),
+                       want + R, rtol=1e-13, atol=1e-13)
+    # A zero up projection gives zero; a zero gate gives zero (SiLU(0) = 0).
+    assert not oracle.project_swiglu(X, _bits(np.vstack([Wg, 0 * Wu]))).any()
+    assert not oracle.project_swiglu(X, _bits(np.vstack([0 * Wg, Wu]))).any()

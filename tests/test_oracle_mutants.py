@@ -50,6 +50,9 @@ MUTANTS = {
     "gelu_sign": ("return 0.5 * x * (1.0 + erf(x / sqrt(2.0)));",
                   "return 0.5 * x * (1.0 - erf(x / sqrt(2.0)));"),
     "activation_ignored": ("if (act == 1)\n", "if (act == 7)\n"),
+    "silu_sign": ("return x / (1.0 + exp(-x));", "return x / (1.0 + exp(x));"),
+    "silu_no_x": ("return x / (1.0 + exp(-x));", "return 1.0 / (1.0 + exp(-x));"),
+    "swiglu_gates_up": ("out[i] = oracle_silu(gate[i]) * up[i];", "out[i] = gate[i] * oracle_silu(up[i]);"),
 }
 
 
