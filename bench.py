@@ -268,6 +268,25 @@ def cpu_oracle_timing(w, inp, target_s: float, y_gpu=None, act: str = "none", re
     return out
 
 
+def swiglu_output_check(w, inp, y_gpu, residual, features: int = 64) -> dict:
+    """The first ``features`` outputs of every token row against the oracle's
+    SwiGLU (their gate rows f and up rows F + f)."""
+    import numpy as np
+    import oracle
+    F = w.N // 2
+    nf = min(features, F)
+    W = inp["W"]
+    if w.w_layout == 0:
+        Wsub = np.ascontiguousarray(np.vstack([W[:nf], W[F:F + nf]]))
+    else:
+        Wsub = np.ascontiguousarray(np.hstack([W[:, :nf], W[:, F:F + nf]]))
+    r = oracle.project_swiglu(inp["X"], Wsub, w.w_layout,
+                              None if residual is None else residual[:, :nf])
+    u = y_gpu[:, :nf]
+    bad = int(np.count_nonzero(~(np.abs(u - r) <= 1e-3 + 5e-3 * np.abs(r))))
+    return {"cells": int(u.size), "out_of_tolerance": bad}
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu_arm(args) -> dict:
     import numpy as np
@@ -299,7 +318,11 @@ def run_gpu_arm(args) -> dict:
     n_copies = max(2, math.ceil(2 * l2 / w.weight_bytes) + 1)
     Ws = [W0] + [W0.clone() for _ in range(n_copies - 1)]
     y_dt = torch.float32 if w.y_dtype == "f32" else torch.bfloat16
-    Y = torch.empty((w.M, w.N), dtype=y_dt, device=device)
+    swiglu = args.activation == "swiglu"
+    if swiglu and (not args.packed or w.has_bias or fp32_w or w.N % 2):
+        raise SystemExit("swiglu runs packed, without bias, on bf16 weights with an even N")
+    n_out = w.N // 2 if swiglu else w.N
+    Y = torch.empty((w.M, n_out), dtype=y_dt, device=device)
     # Each step's kernel may start (set-up only) while the previous step
     # finishes; it touches global memory only after that step completes
     # (mode "prologue").  Mode "weights" also streams W early, which measured no
@@ -310,14 +333,16 @@ def run_gpu_arm(args) -> dict:
                           dlp.PROJ_F32 if w.y_dtype == "f32" else dlp.PROJ_BF16, w.has_bias,
                           overlap=overlap, w_dtype=dlp.PROJ_F32 if fp32_w else dlp.PROJ_BF16)
     stream = torch.cuda.Stream(device)
+    # Fused epilogue (optional): activation and a residual input R.  The
+    # activation is set before packing (SwiGLU interleaves gate and up rows).
+    proj.set_activation({"none": dlp.PROJ_ACT_NONE, "gelu": dlp.PROJ_ACT_GELU,
+                         "swiglu": dlp.PROJ_ACT_SWIGLU}[args.activation])
+    R = (torch.randn((w.M, n_out), device=device, generator=torch.Generator(device).manual_seed(w.seed))
+         .to(y_dt) if args.residual else None)
     # Weights packed once per copy into the handle's tile-contiguous layout:
     # the preparation step, outside every timed region.
     Wrun = [proj.pack(Wc) for Wc in Ws] if args.packed else Ws
     torch.cuda.synchronize()
-    # Fused epilogue (optional): activation and a residual input R.
-    proj.set_activation(dlp.PROJ_ACT_GELU if args.activation == "gelu" else dlp.PROJ_ACT_NONE)
-    R = (torch.randn((w.M, w.N), device=device, generator=torch.Generator(device).manual_seed(w.seed))
-         .to(y_dt) if args.residual else None)
 
     def step(Wc, strm):
         proj(X, Wc, bias, out=Y, stream=strm, packed=args.packed, residual=R)
@@ -454,8 +479,10 @@ def run_gpu_arm(args) -> dict:
     fused = args.activation != "none" or args.residual
     traffic, profile_path = (None, None) if fused else profile_traffic(
         args.workload if args.m is None else f"{args.workload}_m{args.m}")
-    # A residual is one more [M,N] array read.
-    alg_bytes = w.algorithmic_bytes + (w.M * w.N * (4 if w.y_dtype == "f32" else 2) if args.residual else 0)
+    # A residual is one more output-sized array read; SwiGLU writes N/2 columns.
+    ysz = 4 if w.y_dtype == "f32" else 2
+    alg_bytes = (w.algorithmic_bytes - (w.M * (w.N - n_out) * ysz)
+                 + (w.M * n_out * ysz if args.residual else 0))
     hbm_bound = roofline_time_s(alg_bytes, w.flops, peaks["hbm_gbs"] * 1e9,
                                 peaks["bf16_tflops"] * 1e12)
     if alg_bytes / (peaks["hbm_gbs"] * 1e9) >= w.flops / (peaks["bf16_tflops"] * 1e12):
@@ -510,8 +537,12 @@ def run_gpu_arm(args) -> dict:
         step(Wrun[0], stream)  # the output of one plain call, to be safe
         torch.cuda.synchronize()
         y64 = Y.float().cpu().numpy().astype(np.float64)
-        cpu = cpu_oracle_timing(w, inp, args.cpu_seconds, y_gpu=y64, act=args.activation,
+        cpu = cpu_oracle_timing(w, inp, args.cpu_seconds, y_gpu=None if swiglu else y64,
+                                act=args.activation,
                                 residual=None if R is None else R.double().cpu().numpy())
+        if swiglu:
+            cpu["timed_output_check"] = swiglu_output_check(w, inp, y64, None if R is None else
+                                                            R.double().cpu().numpy())
         cpu.pop("seconds", None)
 
     plan = proj.plan
@@ -644,8 +675,9 @@ def parse_args(argv=None):
                     help="skip the informational cuBLAS timing")
     ap.add_argument("--no-packed", dest="packed", action="store_false",
                     help="run on the weights as stored instead of pre-packed ones")
-    ap.add_argument("--activation", choices=["none", "gelu"], default="none",
-                    help="fused activation on projection + bias (proj_set_activation)")
+    ap.add_argument("--activation", choices=["none", "gelu", "swiglu"], default="none",
+                    help="fused activation on projection + bias (proj_set_activation); swiglu "
+                         "reads W as [gate rows; up rows] and writes N/2 columns")
     ap.add_argument("--residual", action="store_true",
                     help="fused residual add: Y = act(X·Wᵀ + b) + R, R an [M,N] input")
     args = ap.parse_args(argv)

@@ -29,7 +29,8 @@ __all__ = [
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "TRACE_FIELDS",
     "PROJ_OVERLAP_NONE", "PROJ_OVERLAP_PROLOGUE", "PROJ_OVERLAP_WEIGHTS", "proj_run_noalloc",
     "proj_packed_weight_bytes", "proj_pack_weights", "proj_run_packed", "proj_run_host_packed",
-    "proj_set_activation", "proj_run_fused", "PROJ_ACT_NONE", "PROJ_ACT_GELU", "Projection",
+    "proj_set_activation", "proj_run_fused", "PROJ_ACT_NONE", "PROJ_ACT_GELU", "PROJ_ACT_SWIGLU",
+    "Projection",
 ]
 
 PROJ_OK, PROJ_ERR_INVALID_ARG, PROJ_ERR_UNSUPPORTED, PROJ_ERR_MISALIGNED = 0, 1, 2, 3
@@ -38,7 +39,7 @@ PROJ_BF16, PROJ_F32 = 0, 1
 PROJ_W_NK, PROJ_W_KN = 0, 1
 PROJ_KERNEL_NONE, PROJ_KERNEL_FILL, PROJ_KERNEL_TC = 0, 1, 2
 PROJ_OVERLAP_NONE, PROJ_OVERLAP_PROLOGUE, PROJ_OVERLAP_WEIGHTS = 0, 1, 2
-PROJ_ACT_NONE, PROJ_ACT_GELU = 0, 1
+PROJ_ACT_NONE, PROJ_ACT_GELU, PROJ_ACT_SWIGLU = 0, 1, 2
 
 EXPORTED_SYMBOLS = (
     "proj_plan_compute", "proj_plan_segments", "proj_plan_reduction_order", "proj_create", "proj_run", "proj_run_host", "proj_device_status",
@@ -310,6 +311,7 @@ class Projection:
         self.M, self.N, self.K = M, N, K
         self.w_layout, self.y_dtype, self.has_bias = w_layout, y_dtype, bool(has_bias)
         self.w_dtype = w_dtype
+        self.act = PROJ_ACT_NONE
         self.handle = proj_create(M, N, K, w_layout, PROJ_BF16, w_dtype, y_dtype, has_bias,
                                   PROJ_BF16, stream)
         if overlap is not None:
@@ -325,7 +327,8 @@ class Projection:
         import torch
         if out is None:
             dt = torch.float32 if self.y_dtype == PROJ_F32 else torch.bfloat16
-            out = torch.empty((self.M, self.N), dtype=dt, device=X.device)
+            n_out = self.N // 2 if self.act == PROJ_ACT_SWIGLU else self.N
+            out = torch.empty((self.M, n_out), dtype=dt, device=X.device)
         if stream is None:
             stream = torch.cuda.current_stream(X.device)
         if residual is not None:
@@ -335,7 +338,10 @@ class Projection:
         return out
 
     def set_activation(self, act: int) -> None:
+        """PROJ_ACT_NONE, PROJ_ACT_GELU, or PROJ_ACT_SWIGLU (set it before
+        :meth:`pack`; the output then has N / 2 columns)."""
         proj_set_activation(self.handle, act)
+        self.act = act
 
     def pack(self, W, stream=None):
         """Repack weights into this handle's tile-contiguous layout (a preparation

@@ -389,7 +389,8 @@ proj_status_t proj_pack_weights(proj_handle_t h, const void *W, void *W_packed, 
     else
         dev::proj_pack_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
             static_cast<const uint16_t *>(W), static_cast<uint16_t *>(W_packed), h->N, h->K,
-            h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, chunks);
+            h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, chunks,
+            h->act == PROJ_ACT_SWIGLU ? (plan.swap_ab ? 1 : 2) : 0);
     return check_launch();
 }
 
@@ -411,11 +412,16 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     if (bias && reinterpret_cast<uintptr_t>(bias) % 2 != 0) return PROJ_ERR_MISALIGNED;
     cudaStream_t s = as_stream(stream);
 
+    const bool swiglu = h->act == PROJ_ACT_SWIGLU;
     if (plan.kernel == PROJ_KERNEL_FILL) {
+        // K = 0: every sum is empty.  SwiGLU of zeros is zero (no bias).
         dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(
-            h->M, h->N, static_cast<const uint16_t *>(bias), Y, h->y_dtype == PROJ_F32, h->act, residual);
+            h->M, swiglu ? h->N / 2 : h->N, static_cast<const uint16_t *>(bias), Y, h->y_dtype == PROJ_F32,
+            swiglu ? 0 : h->act, residual);
         return check_launch();
     }
+    // SwiGLU needs the interleaved packed weights.
+    if (swiglu && !packed) return PROJ_ERR_UNSUPPORTED;
 
     if (!X || !W) return PROJ_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W)) return PROJ_ERR_MISALIGNED;
@@ -457,8 +463,9 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     kp.Y = Y;
     kp.act = h->act;
     kp.residual = residual;
+    kp.ldy = static_cast<int32_t>(swiglu ? h->N / 2 : h->N);
     // Vector stores read the residual the same way: both 16-byte aligned.
-    kp.y_vec = y_vec_of(Y, h->N, h->y_dtype) && (!residual || aligned16(residual));
+    kp.y_vec = y_vec_of(Y, kp.ldy, h->y_dtype) && (!residual || aligned16(residual));
     kp.trace = h->trace;
     // Weights stream early only when every SM has a CTA: the next kernel's
     // CTAs then start as the preceding kernel's leave, in its tail.  With SMs
@@ -553,7 +560,9 @@ proj_status_t proj_device_status(proj_handle_t h, void *stream) {
 
 proj_status_t proj_set_activation(proj_handle_t h, proj_activation_t act) {
     if (!h) return PROJ_ERR_INVALID_ARG;
-    if (act != PROJ_ACT_NONE && act != PROJ_ACT_GELU) return PROJ_ERR_INVALID_ARG;
+    if (act != PROJ_ACT_NONE && act != PROJ_ACT_GELU && act != PROJ_ACT_SWIGLU) return PROJ_ERR_INVALID_ARG;
+    // SwiGLU: stacked gate and up rows (N even), no bias, bf16 weights.
+    if (act == PROJ_ACT_SWIGLU && (h->N % 2 != 0 || h->has_bias || h->hilo)) return PROJ_ERR_UNSUPPORTED;
     h->act = act;
     return PROJ_OK;
 }
@@ -744,6 +753,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.w_prefetch = 0;
     kp.bias = static_cast<const uint16_t *>(bias);
     kp.Y = Y;
+    kp.ldy = static_cast<int32_t>(N);
     kp.y_vec = y_vec_of(Y, N, y_dtype);
     kp.partials = reinterpret_cast<float *>(sc);
     kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);

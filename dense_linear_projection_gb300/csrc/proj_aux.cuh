@@ -14,8 +14,32 @@ namespace dev {
 // values).  [N,K] weights: consecutive threads take consecutive K chunks of a
 // row (contiguous reads); [K,N] weights: consecutive threads take consecutive
 // rows of one K chunk (contiguous reads along N).
+//
+// SwiGLU weights (interleave 1 or 2): W stacks F = N / 2 gate rows then F up
+// rows.  Packed row r of tile tn takes feature f, its gate row (f) or its up
+// row (F + f): interleave 1 (swapped tiles), r = 32·q + l with f = tn·(block_n
+// / 2) + 16·q + l mod 16, gate for l < 16; interleave 2 (token-major tiles),
+// r = 16·c + j with f = tn·(block_n / 2) + 8·c + j mod 8, gate for j < 8.  So a
+// warp quarter, or a 16-column chunk, holds both halves of its features.
+__device__ __forceinline__ int64_t packed_source_row(int64_t tn, int64_t r, int32_t block_n, int64_t N,
+                                                     int interleave) {
+    if (interleave == 0) return tn * block_n + r;
+    const int64_t F = N / 2;
+    int64_t f;
+    bool up;
+    if (interleave == 1) {
+        f = tn * (block_n / 2) + (r / 32) * 16 + (r % 16);
+        up = (r % 32) >= 16;
+    } else {
+        f = tn * (block_n / 2) + (r / 16) * 8 + (r % 8);
+        up = (r % 16) >= 8;
+    }
+    if (f >= F) return N;  // past the weights: zero
+    return up ? F + f : f;
+}
+
 __global__ void proj_pack_kernel(const uint16_t *W, uint16_t *P, int64_t N, int64_t K, int w_kn,
-                                 int32_t block_n, int64_t k_blocks, int64_t chunks) {
+                                 int32_t block_n, int64_t k_blocks, int64_t chunks, int interleave) {
     for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < chunks;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         int64_t blk, r, c8;
@@ -33,7 +57,7 @@ __global__ void proj_pack_kernel(const uint16_t *W, uint16_t *P, int64_t N, int6
         }
         const int64_t tn = blk / k_blocks;
         const int64_t kb = blk - tn * k_blocks;
-        const int64_t n = tn * block_n + r;
+        const int64_t n = packed_source_row(tn, r, block_n, N, interleave);
         const int64_t k0 = kb * 64 + c8 * 8;
         uint4 out = make_uint4(0u, 0u, 0u, 0u);
         if (n < N && k0 < K) {  // K % 8 == 0: the 8 values are all in range

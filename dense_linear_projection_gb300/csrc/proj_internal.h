@@ -111,7 +111,8 @@ struct KernelParams {
     int32_t y_vec;         // Y rows start 16-byte aligned (N·size % 16 == 0, aligned base)
     int64_t wait_limit_ns; // bounded device waits give up after this long
     int32_t w_prefetch;    // stages of W streamed before the preceding kernel completes (0: none)
-    int32_t act;           // fused activation: 0 none, 1 GELU (on projection + bias)
+    int32_t act;           // fused activation: 0 none, 1 GELU (on projection + bias), 2 SwiGLU
+    int32_t ldy;           // Y row stride in elements: N, or N / 2 for SwiGLU (gate and up rows stacked)
     const uint16_t *bias;  // [N] bf16 or nullptr
     const void *residual;  // [M,N] in Y's dtype, added after the activation, or nullptr (may alias Y)
     void *Y;

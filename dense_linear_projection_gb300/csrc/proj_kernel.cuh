@@ -343,6 +343,12 @@ static __device__ __noinline__ float4 gelu4(float4 v) {
     return make_float4(gelu_f32(v.x), gelu_f32(v.y), gelu_f32(v.z), gelu_f32(v.w));
 }
 
+// SwiGLU's gate: SiLU(g)·u for four (gate, up) pairs a call, out of line.
+static __device__ __noinline__ float4 swiglu4(float4 g, float4 u) {
+    return make_float4(g.x / (1.0f + expf(-g.x)) * u.x, g.y / (1.0f + expf(-g.y)) * u.y,
+                       g.z / (1.0f + expf(-g.z)) * u.z, g.w / (1.0f + expf(-g.w)) * u.w);
+}
+
 // The activation over n values (n a multiple of 4), four per call.
 template <bool kFused, int n>
 __device__ __forceinline__ void apply_act_n(const KernelParams &p, float *v) {
@@ -775,6 +781,87 @@ __global__ void __launch_bounds__(kThreads, 1)
             // lane of the warp calls it (the swapped path shuffles through
             // shared memory).
             auto store_chunk = [&](int32_t ch, const float (&y)[16]) {
+                if constexpr (kFused) {
+                    if (p.act == 2) {
+                        // SwiGLU.  Packing interleaved the stacked gate and up
+                        // rows: swapped tiles hold, in each 32-row quarter,
+                        // 16 gate rows (lanes 0-15) and the same 16 features'
+                        // up rows (lanes 16-31); token-major chunks hold 8
+                        // gate columns then the same 8 features' up columns.
+                        // Output feature f of this tile: n0 / 2 + ...; Y rows
+                        // are ldy = F apart.  There is no bias.
+                        const int32_t F = p.ldy;
+                        if (p.swap) {
+                            float up[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) up[i] = __shfl_xor_sync(0xFFFFFFFFu, y[i], 16);
+                            const int32_t f = n0 / 2 + q * 16 + lane;
+                            const int32_t fb = n0 / 2 + q * 16;  // the warp's first feature
+                            const int32_t mb = m0 + ch * 16;
+                            if (p.y_vec && fb + 16 <= F && mb + 16 <= p.M) {
+                                // 16 features (lanes 0-15) x 16 tokens through shared
+                                // memory, stored as 16-byte row segments.
+                                float *t = ctl->y_tile[q];
+                                if (lane < 16) {
+#pragma unroll
+                                    for (int i = 0; i < 16; i += 4) {
+                                        const float4 o = swiglu4(make_float4(y[i], y[i + 1], y[i + 2], y[i + 3]),
+                                                                 make_float4(up[i], up[i + 1], up[i + 2], up[i + 3]));
+                                        t[(i + 0) * kYTileStride + lane] = o.x;
+                                        t[(i + 1) * kYTileStride + lane] = o.y;
+                                        t[(i + 2) * kYTileStride + lane] = o.z;
+                                        t[(i + 3) * kYTileStride + lane] = o.w;
+                                    }
+                                }
+                                __syncwarp();
+                                if (p.y_f32) {
+#pragma unroll
+                                    for (int pass = 0; pass < 2; ++pass) {
+                                        const int32_t mi = pass * 8 + lane / 4, c = (lane % 4) * 4;
+                                        store_y4_f32<kFused>(p, static_cast<size_t>(mb + mi) * F + fb + c,
+                                                             *reinterpret_cast<const float4 *>(t + mi * kYTileStride + c));
+                                    }
+                                } else {
+                                    const int32_t mi = lane / 2, c = (lane % 2) * 8;
+                                    store_y8<kFused>(p, static_cast<size_t>(mb + mi) * F + fb + c,
+                                                     *reinterpret_cast<const float4 *>(t + mi * kYTileStride + c),
+                                                     *reinterpret_cast<const float4 *>(t + mi * kYTileStride + c + 4));
+                                }
+                                __syncwarp();  // the tile is reused by the next chunk
+                                return;
+                            }
+                            if (lane < 16 && f < F) {
+#pragma unroll
+                                for (int i = 0; i < 16; i += 4) {
+                                    const float4 o = swiglu4(make_float4(y[i], y[i + 1], y[i + 2], y[i + 3]),
+                                                             make_float4(up[i], up[i + 1], up[i + 2], up[i + 3]));
+                                    const float ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j) {
+                                        const int32_t m = m0 + ch * 16 + i + j;
+                                        if (m < p.M) store_y<kFused>(p, static_cast<size_t>(m) * F + f, ov[j]);
+                                    }
+                                }
+                            }
+                        } else {
+                            if (!lane_ok) return;
+                            const int32_t m = lane_row;
+                            const int32_t f0 = n0 / 2 + ch * 8;
+                            const float4 a = swiglu4(make_float4(y[0], y[1], y[2], y[3]), make_float4(y[8], y[9], y[10], y[11]));
+                            const float4 b = swiglu4(make_float4(y[4], y[5], y[6], y[7]), make_float4(y[12], y[13], y[14], y[15]));
+                            const size_t off = static_cast<size_t>(m) * F + f0;
+                            if (p.y_vec && f0 + 8 <= F) {
+                                store_y8<kFused>(p, off, a, b);
+                            } else {
+                                const float ov[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    if (f0 + j < F) store_y<kFused>(p, off + j, ov[j]);
+                            }
+                        }
+                        return;
+                    }
+                }
                 if (p.swap) {
                     // The warp holds 32 consecutive weight rows (lanes) x 16
                     // tokens (registers), but Y rows run along the weight rows:
@@ -961,7 +1048,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (; ch + 4 <= nchunks; ch += 4) {
                     float v[64];
                     tmem_load64(tbase + ch * 16, v);
-                    if (!p.swap && p.y_vec && n0 + (ch + 4) * 16 <= p.N) {
+                    bool cols32 = !p.swap && p.y_vec && n0 + (ch + 4) * 16 <= p.N;
+                    if constexpr (kFused) cols32 = cols32 && p.act != 2;  // SwiGLU stores per chunk
+                    if (cols32) {
                         store_cols32(ch, v);
                         store_cols32(ch + 2, v + 32);
                     } else {

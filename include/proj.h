@@ -286,12 +286,24 @@ proj_status_t proj_run_packed(proj_handle_t h, const void *X, const void *W_pack
  * type and layout, or NULL; it may be Y itself (each element is read before
  * it is written).  proj_run_fused: packed = 1 takes packed weights (as
  * proj_run_packed), 0 weights as stored; otherwise as proj_run.
+ *
+ * PROJ_ACT_SWIGLU (Shazeer, "GLU Variants Improve Transformer"; the first
+ * page's expert pattern of a gate vector through a nonlinearity times an up
+ * vector): W stacks the F = N / 2 gate rows, then the F up rows ([N,K], or
+ * [K,N] with gate columns first), and Y[m,f] = SiLU(G[m,f]) · U[m,f]
+ * (+ residual), Y and the residual [M, F], SiLU(x) = x / (1 + e^(−x)).  Set
+ * it before proj_pack_weights, which interleaves each tile's gate and up rows
+ * so they meet in one epilogue warp; such a handle runs only packed
+ * (proj_run_packed, or proj_run_fused with packed = 1).  proj_set_activation
+ * returns PROJ_ERR_UNSUPPORTED for SwiGLU on a handle with a bias, an odd N,
+ * or fp32 weights; an unpacked run returns PROJ_ERR_UNSUPPORTED.
  * PROJ_ERR_INVALID_ARG for an unknown activation or packed flag;
  * PROJ_ERR_MISALIGNED for a residual not aligned to Y's element size.
  */
 typedef enum proj_activation {
     PROJ_ACT_NONE = 0,
-    PROJ_ACT_GELU = 1
+    PROJ_ACT_GELU = 1,
+    PROJ_ACT_SWIGLU = 2
 } proj_activation_t;
 
 proj_status_t proj_set_activation(proj_handle_t h, proj_activation_t act);
