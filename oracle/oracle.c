@@ -157,9 +157,9 @@ double oracle_gelu(double x) {
 
 /* SwiGLU's gate nonlinearity (Shazeer, "GLU Variants Improve Transformer",
  * 2020): SiLU(x) = x · σ(x) = x / (1 + e^(−x)).  The first page's
- * expert pattern ("produces a gate vector and an up vector, transforms the
- * gate with a nonlinear function, multiplies the two vectors elementwise")
- * leaves the function unnamed; SwiGLU names it. */
+ * section on experts combines two projections of one input entry by entry,
+ * one of them passed through a nonlinearity it does not name; SwiGLU names
+ * it. */
 double oracle_silu(double x) {
     return x / (1.0 + exp(-x));
 }
