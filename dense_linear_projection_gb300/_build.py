@@ -16,7 +16,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["proj_api.cu", "planner.cpp", "kernel_tc_lean.cu", "kernel_tc_fused.cu"]
+SOURCES = ["proj_api.cu", "planner.cpp", "kernel_tc_lean.cu", "kernel_tc_fused.cu", "kernel_tc_pair.cu",
+           "kernel_tc_pair_fused.cu"]
 HEADERS = [os.path.join(CSRC, "proj_internal.h"), os.path.join(CSRC, "proj_kernel.cuh"),
            os.path.join(CSRC, "proj_aux.cuh"), os.path.join(CSRC, "proj_launch.h"),
            os.path.join(INCLUDE, "proj.h")]

@@ -132,9 +132,86 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
             }
         }
     }
+    const int32_t budget = dev->smem_optin_bytes - kSmemReserve;
+
+    // CTA pairs: a tile of 256 rows on the MMA's M side, computed by the two
+    // CTAs of a cluster with one cta_group::2 MMA per K step.  Each CTA
+    // stages half of the B operand (the MMA reads both halves), so a stage
+    // holds 16 KiB + b_rows/2 rows instead of 16 KiB + b_rows, and each CTA
+    // pulls half the weight (token-major) or token (swapped) rows from L2
+    // per FLOP.  Whole tiles only, dealt to pairs; the MMA's N side (b_rows)
+    // a multiple of 32 between 64 and 256.  Chosen for the tensor-bound
+    // swapped plans of 256-token tiles that keep at least half of the SMs
+    // busy (measured on GB300, 4096 x 8192 x 8192: 359 us on pairs with one
+    // accumulator vs 370 us on single CTAs).  Token-major pairs measured no
+    // faster on the 256 x 12288 x 4096 QKV shape (27.9 vs 27.7 us, whose
+    // time is its weight stream): they are taken only with option 2, which
+    // takes pairs wherever the tile allows them.
+    {
+        const bool forced = opt.cta_pair == 2;
+        const int64_t pairs_max = sms / 2;
+        bool pair_swapped = swap && bt % 32 == 0 && bt >= 64;
+        if (!forced)
+            pair_swapped = pair_swapped && bt == kMaxTokenTile && 2 * bt <= kPairTmemMax &&
+                           2 * ceil_div(M, bt) * ceil_div(N, 2 * kBlockA) >= pairs_max;
+        const bool pair_tm = forced && !swap && M > kBlockA && (force_block_n <= 0 || force_block_n % 32 == 0);
+        if (opt.cta_pair >= 1 && sms >= 2 && (pair_swapped || pair_tm)) {
+            int32_t pbt = bt, pbn = bn;
+            if (swap) {
+                pbn = 2 * kBlockA;
+            } else {
+                pbt = 2 * kBlockA;
+                if (force_block_n <= 0) {
+                    // As for single CTAs: per-pair time ~ waves x (block_n +
+                    // a fixed share); the widest block_n wins ties.
+                    const int64_t tiles_m = ceil_div(M, pbt);
+                    int64_t best_cost = -1;
+                    for (int32_t cand = kMaxTokenTile; cand >= 64; cand -= 32) {
+                        const int64_t waves = ceil_div(tiles_m * ceil_div(N, cand), pairs_max);
+                        const int64_t cost = waves * (cand + 32);
+                        if (best_cost < 0 || cost < best_cost) {
+                            best_cost = cost;
+                            pbn = cand;
+                        }
+                    }
+                }
+            }
+            const int32_t pb_rows = swap ? pbt : pbn;
+            const int32_t pstage = stage_bytes_for(pb_rows / 2);
+            int32_t pstages = budget / pstage;
+            if (pstages > kMaxStages) pstages = kMaxStages;
+            const int64_t ptiles = ceil_div(M, pbt) * ceil_div(N, pbn);
+            if (pstages >= 2 && (forced || 2 * ptiles >= pairs_max)) {
+                out->kernel = PROJ_KERNEL_TC;
+                out->cta_pair = 1;
+                out->swap_ab = swap ? 1 : 0;
+                out->block_t = pbt;
+                out->block_n = pbn;
+                // Two accumulator buffers when they fit the pair's tensor
+                // memory, else one (the epilogue then waits for the MMAs).
+                out->tmem_cols = 2 * pb_rows <= kPairTmemMax ? pow2_ceil(2 * pb_rows < 32 ? 32 : 2 * pb_rows)
+                                                             : pow2_ceil(pb_rows < 32 ? 32 : pb_rows);
+                out->tiles_m = ceil_div(M, pbt);
+                out->tiles_n = ceil_div(N, pbn);
+                int64_t g = 2048 / pbt;
+                if (g < 1) g = 1;
+                out->raster_group = static_cast<int32_t>(out->tiles_m < g ? out->tiles_m : g);
+                out->k_blocks = ceil_div(K, kBlockK);
+                const int64_t tiles = out->tiles_m * out->tiles_n;
+                out->grid = static_cast<int32_t>(2 * (tiles < pairs_max ? tiles : pairs_max));
+                out->tiles_dp = tiles;
+                out->tiles_sk = 0;
+                out->units_sk = 0;
+                out->stages = pstages;
+                out->smem_bytes = pstages * pstage + kSmemReserve;
+                out->scratch_bytes = 256;  // the status word
+                return PROJ_OK;
+            }
+        }
+    }
+
     const int32_t b_rows = swap ? bt : bn;
     const int32_t stage = stage_bytes_for(b_rows);
-    const int32_t budget = dev->smem_optin_bytes - kSmemReserve;
     int32_t stages = budget / stage;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return PROJ_ERR_UNSUPPORTED;
@@ -267,7 +344,7 @@ extern "C" proj_status_t proj_plan_segments(const proj_plan_desc_t *plan, int32_
     KernelParams kp{};
     params_from_plan(*plan, kp);
     WorkIter it;
-    it.init(kp, cta);
+    it.init(kp, plan->cta_pair ? cta / 2 : cta);  // both CTAs of a pair run the pair's tiles
     Segment s;
     int64_t n = 0;
     while (it.next(kp, s)) {
@@ -334,12 +411,12 @@ int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int
         "{\"kernel\": \"%s\", \"M\": %lld, \"N\": %lld, \"K\": %lld, \"w_layout\": \"%s\", "
         "\"y_dtype\": \"%s\", \"bias\": %s, \"block_n\": %d, \"block_t\": %d, \"block_k\": %d, "
         "\"stages\": %d, \"grid\": %d, \"threads\": %d, \"smem_bytes\": %d, "
-        "\"tmem_cols\": %d, \"raster_group\": %d, \"swap_ab\": %d, \"cluster_split\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
+        "\"tmem_cols\": %d, \"raster_group\": %d, \"swap_ab\": %d, \"cluster_split\": %d, \"cta_pair\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
         "\"tiles_dp\": %lld, \"tiles_sk\": %lld, \"units_sk\": %lld, \"scratch_bytes\": %lld}",
         kname, (long long)M, (long long)N, (long long)K, w_layout == PROJ_W_NK ? "NK" : "KN",
         y_dtype == PROJ_F32 ? "f32" : "bf16", has_bias ? "true" : "false", p.block_n,
         p.block_t, p.block_k, p.stages, p.grid, p.threads, p.smem_bytes, p.tmem_cols, p.raster_group,
-        p.swap_ab, p.cluster_split,
+        p.swap_ab, p.cluster_split, p.cta_pair,
         (long long)p.tiles_m, (long long)p.tiles_n, (long long)p.k_blocks,
         (long long)p.tiles_dp, (long long)p.tiles_sk, (long long)p.units_sk,
         (long long)p.scratch_bytes);

@@ -26,11 +26,21 @@ struct proj_plan_s {
     int has_bias = 0;
     proj_plan_desc_t plan{};
     KernelParams params{};
+    // Weights stored [K,N] load along N in 64-column boxes.  When the plan's
+    // CTA pairs hold weight halves of another width, runs on weights as
+    // stored (not packed) use this single-CTA plan instead.
+    bool has_plan_stored = false;
+    proj_plan_desc_t plan_stored{};
+    KernelParams params_stored{};
     void *scratch = nullptr;
-    // Tensor maps cached by base pointer (rebuilt when X or W moves).
+    int64_t scratch_bytes = 0;       // allocated
+    int64_t scratch_clear_from = 0;  // counters and status word: [clear_from, scratch_bytes)
+    // Tensor maps cached by base pointer and box rows (rebuilt when X or W
+    // moves or another plan runs).
     const void *map_x_ptr = nullptr;
     const void *map_w_ptr = nullptr;
     const void *map_wp_ptr = nullptr;  // packed weights
+    int32_t map_x_box = 0, map_w_box = 0;
     CUtensorMap map_x;  // CUtensorMap carries its own 64-byte alignment
     CUtensorMap map_w;
     CUtensorMap map_wp;
@@ -100,13 +110,21 @@ uint32_t make_idesc(int mma_m, int mma_n, bool a_mn_major, bool b_mn_major) {
     return d;
 }
 
-// Instruction descriptor of a plan: M = 128, N = B rows; [K,N] weights are
-// MN-major in whichever operand they occupy.
+// Instruction descriptor of a plan: M = 128 (256 for a CTA pair), N = B rows;
+// [K,N] weights are MN-major in whichever operand they occupy.
 uint32_t idesc_of(const proj_plan_desc_t &plan, int w_layout) {
     const bool kn = w_layout == PROJ_W_KN;
-    const int b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
-    return make_idesc(kBlockA, b_rows, plan.swap_ab && kn, !plan.swap_ab && kn);
+    return make_idesc(plan.cta_pair ? 2 * kBlockA : kBlockA, plan_b_rows(plan), plan.swap_ab && kn,
+                      !plan.swap_ab && kn);
 }
+
+// Rows of one TMA box of X and of W (a CTA of a pair loads half the tile's).
+int32_t x_box_rows(const proj_plan_desc_t &plan) { return plan.cta_pair ? plan.block_t / 2 : plan.block_t; }
+int32_t w_box_rows(const proj_plan_desc_t &plan) { return plan.cta_pair ? plan.block_n / 2 : plan.block_n; }
+
+// Whether a plan can load weights stored [K,N]: its weight rows per CTA are
+// whole 64-column boxes.
+bool loads_stored_kn(const proj_plan_desc_t &plan) { return w_box_rows(plan) % 64 == 0; }
 
 // Bytes of split-K partial tiles in the scratch (the rest is counters and
 // the status word).  Cluster-split plans reduce in shared memory: none.
@@ -120,7 +138,8 @@ int64_t partial_bytes_of(const proj_plan_desc_t &plan) {
 bool set_kernel_smem_limit(int smem_optin) {
     // Also allow clusters above the portable 8 CTAs (GB300 runs 16); the
     // occupancy query in plan_for_device decides whether a size fits.
-    if (tc_configure_lean(smem_optin) != cudaSuccess || tc_configure_fused(smem_optin) != cudaSuccess) {
+    if (tc_configure_lean(smem_optin) != cudaSuccess || tc_configure_fused(smem_optin) != cudaSuccess ||
+        tc_configure_pair(smem_optin) != cudaSuccess || tc_configure_pair_fused(smem_optin) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
@@ -128,7 +147,8 @@ bool set_kernel_smem_limit(int smem_optin) {
 }
 
 // Launch configuration of a tensor-core plan: the cluster shape of a
-// cluster-split plan and, unless off, programmatic dependent launch.
+// cluster-split or CTA-pair plan and, unless off, programmatic dependent
+// launch.
 struct TcLaunch {
     cudaLaunchConfig_t cfg{};
     cudaLaunchAttribute attr[2];
@@ -138,9 +158,9 @@ struct TcLaunch {
         cfg.dynamicSmemBytes = static_cast<size_t>(plan.smem_bytes);
         cfg.stream = s;
         unsigned n = 0;
-        if (plan.cluster_split > 1) {
+        if (plan.cluster_split > 1 || plan.cta_pair) {
             attr[n].id = cudaLaunchAttributeClusterDimension;
-            attr[n].val.clusterDim.x = static_cast<unsigned>(plan.cluster_split);
+            attr[n].val.clusterDim.x = static_cast<unsigned>(plan.cta_pair ? 2 : plan.cluster_split);
             attr[n].val.clusterDim.y = 1;
             attr[n].val.clusterDim.z = 1;
             ++n;
@@ -183,6 +203,15 @@ int y_vec_of(const void *Y, int64_t N, int y_dtype) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The kernel instance a plan runs on: CTA pairs or single CTAs, with or
+// without the fused epilogue.
+cudaError_t launch_tc(const proj_plan_desc_t &plan, const TcLaunch &l, bool fused, const KernelParams &kp,
+                      const CUtensorMap &map_w, const CUtensorMap &map_x) {
+    if (plan.cta_pair)
+        return fused ? tc_launch_pair_fused(&l.cfg, kp, map_w, map_x) : tc_launch_pair(&l.cfg, kp, map_w, map_x);
+    return fused ? tc_launch_fused(&l.cfg, kp, map_w, map_x) : tc_launch_lean(&l.cfg, kp, map_w, map_x);
+}
 
 proj_status_t check_launch() {
     return cudaGetLastError() == cudaSuccess ? PROJ_OK : PROJ_ERR_CUDA;
@@ -242,6 +271,10 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int f = std::atoi(e);
         if (f >= 1 && f <= 100) opt.cluster_fill_pct = f;
     }
+    if (const char *e = std::getenv("PROJ_CTA_PAIR")) {
+        const int c = std::atoi(e);
+        if (c >= 0 && c <= 2) opt.cta_pair = c;
+    }
     // fp32 weights: the reduction runs over [H | L], twice the k-blocks of K.
     const int64_t kt = (K + kBlockK - 1) / kBlockK;
     const int64_t k_plan = hilo ? 2 * kt * kBlockK : K;
@@ -250,7 +283,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     if (const char *e = std::getenv("PROJ_FORCE_GRID")) {  // tuning only: fewer CTAs, all-split plans
         const int g = std::atoi(e);
         if (g >= 1 && g < plan.grid && plan.kernel == PROJ_KERNEL_TC && plan.tiles_dp == 0 &&
-            plan.cluster_split < 2) {
+            plan.cluster_split < 2 && !plan.cta_pair) {
             plan.grid = g;
             const int64_t b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
             const int64_t counter_bytes = ((plan.tiles_sk * 4 * 4 + 255) / 256) * 256;
@@ -259,7 +292,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     }
     if (const char *e = std::getenv("PROJ_FORCE_WHOLE_TILES")) {  // tuning only
         if (std::atoi(e) == 1 && plan.kernel == PROJ_KERNEL_TC && plan.tiles_sk > 0 &&
-            plan.cluster_split < 2) {
+            plan.cluster_split < 2 && !plan.cta_pair) {
             plan.tiles_dp += plan.tiles_sk;
             plan.tiles_sk = 0;
             plan.units_sk = 0;
@@ -269,9 +302,8 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int st_force = std::atoi(e);
         if (st_force >= 2 && st_force < plan.stages && plan.kernel == PROJ_KERNEL_TC) {
             plan.stages = st_force;
-            const int32_t b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
-            plan.smem_bytes = st_force * stage_bytes_for(b_rows) +
-                              cluster_red_bytes(plan.cluster_split, b_rows) + kSmemReserve;
+            plan.smem_bytes = st_force * stage_bytes_for(plan_cta_b_rows(plan)) +
+                              cluster_red_bytes(plan.cluster_split, plan_b_rows(plan)) + kSmemReserve;
         }
     }
     if (const char *e = std::getenv("PROJ_FORCE_RASTER_GROUP")) {  // tuning only
@@ -298,29 +330,53 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         if (n >= 0 && n <= kMaxStages) h->prefetch_stages = n;
     }
 
+    if (plan.kernel == PROJ_KERNEL_TC && w_layout == PROJ_W_KN && !hilo && !loads_stored_kn(plan)) {
+        PlanOptions single = opt;
+        single.cta_pair = 0;
+        st = plan_for_device(M, N, k_plan, w_layout, y_dtype, has_bias, dd, single, &h->plan_stored);
+        if (st != PROJ_OK) {
+            delete h;
+            return st;
+        }
+        h->has_plan_stored = true;
+    }
+
     if (plan.kernel == PROJ_KERNEL_TC) {
-        if (cudaMalloc(&h->scratch, static_cast<size_t>(plan.scratch_bytes)) != cudaSuccess) {
+        // One scratch serves both plans: partial sums first, each plan's
+        // counters after its partials, the status word in the last 256 bytes.
+        int64_t scratch_bytes = plan.scratch_bytes;
+        if (h->has_plan_stored && h->plan_stored.scratch_bytes > scratch_bytes)
+            scratch_bytes = h->plan_stored.scratch_bytes;
+        if (cudaMalloc(&h->scratch, static_cast<size_t>(scratch_bytes)) != cudaSuccess) {
             cudaGetLastError();
             delete h;
             return PROJ_ERR_OUT_OF_MEMORY;
         }
-        const int64_t partial_bytes = partial_bytes_of(plan);
         uint8_t *sc = static_cast<uint8_t *>(h->scratch);
-        KernelParams &kp = h->params;
-        kp.M = static_cast<int32_t>(M);
-        kp.N = static_cast<int32_t>(N);
-        kp.K = static_cast<int32_t>(K);
-        params_from_plan(plan, kp);
-        kp.idesc = idesc_of(plan, w_layout);
-        kp.w_kn = w_layout == PROJ_W_KN;
-        kp.y_f32 = y_dtype == PROJ_F32;
-        kp.x_kb_mod = hilo ? static_cast<int32_t>(kt) : 0;
-        kp.wait_limit_ns = kDefaultWaitLimitNs;
-        kp.partials = reinterpret_cast<float *>(sc);
-        kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);
-        kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
+        auto init_params = [&](const proj_plan_desc_t &pl, KernelParams &kp) {
+            kp.M = static_cast<int32_t>(M);
+            kp.N = static_cast<int32_t>(N);
+            kp.K = static_cast<int32_t>(K);
+            params_from_plan(pl, kp);
+            kp.idesc = idesc_of(pl, w_layout);
+            kp.w_kn = w_layout == PROJ_W_KN;
+            kp.y_f32 = y_dtype == PROJ_F32;
+            kp.x_kb_mod = hilo ? static_cast<int32_t>(kt) : 0;
+            kp.wait_limit_ns = kDefaultWaitLimitNs;
+            kp.partials = reinterpret_cast<float *>(sc);
+            kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes_of(pl));
+            kp.status = reinterpret_cast<int *>(sc + scratch_bytes - 256);
+        };
+        init_params(plan, h->params);
+        int64_t partial_bytes = partial_bytes_of(plan);
+        if (h->has_plan_stored) {
+            init_params(h->plan_stored, h->params_stored);
+            if (partial_bytes_of(h->plan_stored) < partial_bytes) partial_bytes = partial_bytes_of(h->plan_stored);
+        }
+        h->scratch_bytes = scratch_bytes;
+        h->scratch_clear_from = partial_bytes;
         // Counters and the status word start at zero; partials need no clearing.
-        if (cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(plan.scratch_bytes - partial_bytes),
+        if (cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(scratch_bytes - partial_bytes),
                             as_stream(stream)) != cudaSuccess ||
             cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) {
             cudaGetLastError();
@@ -403,7 +459,8 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     if (!h) return PROJ_ERR_INVALID_ARG;
     if (h->hilo && !packed && h->plan.kernel == PROJ_KERNEL_TC) return PROJ_ERR_UNSUPPORTED;
     if ((bias != nullptr) != (h->has_bias != 0)) return PROJ_ERR_INVALID_ARG;
-    const proj_plan_desc_t &plan = h->plan;
+    const bool stored = !packed && h->has_plan_stored;  // weights as stored, plan of single CTAs
+    const proj_plan_desc_t &plan = stored ? h->plan_stored : h->plan;
     if (plan.kernel == PROJ_KERNEL_NONE) return PROJ_OK;
     if (!Y) return PROJ_ERR_INVALID_ARG;
     const size_t y_align = h->y_dtype == PROJ_F32 ? 4 : 2;
@@ -425,34 +482,36 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
 
     if (!X || !W) return PROJ_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W)) return PROJ_ERR_MISALIGNED;
-    if (X != h->map_x_ptr) {
-        if (!encode_2d(&h->map_x, X, h->K, h->M, h->K * 2, kBlockK, plan.block_t)) {
+    if (X != h->map_x_ptr || x_box_rows(plan) != h->map_x_box) {
+        if (!encode_2d(&h->map_x, X, h->K, h->M, h->K * 2, kBlockK, x_box_rows(plan))) {
             h->map_x_ptr = nullptr;
             return PROJ_ERR_CUDA;
         }
         h->map_x_ptr = X;
+        h->map_x_box = x_box_rows(plan);
     }
     if (packed) {
-        if (W != h->map_wp_ptr) {
+        if (W != h->map_wp_ptr) {  // packed runs always use h->plan: one box size
             const int64_t rows = packed_rows(plan);
             if (rows < 0) return PROJ_ERR_UNSUPPORTED;
-            if (!encode_2d(&h->map_wp, W, 64, static_cast<uint64_t>(rows), 128, kBlockK, plan.block_n)) {
+            if (!encode_2d(&h->map_wp, W, 64, static_cast<uint64_t>(rows), 128, kBlockK, w_box_rows(plan))) {
                 h->map_wp_ptr = nullptr;
                 return PROJ_ERR_CUDA;
             }
             h->map_wp_ptr = W;
         }
-    } else if (W != h->map_w_ptr) {
+    } else if (W != h->map_w_ptr || w_box_rows(plan) != h->map_w_box) {
         const bool ok = h->w_layout == PROJ_W_NK
-                            ? encode_2d(&h->map_w, W, h->K, h->N, h->K * 2, kBlockK, plan.block_n)
+                            ? encode_2d(&h->map_w, W, h->K, h->N, h->K * 2, kBlockK, w_box_rows(plan))
                             : encode_2d(&h->map_w, W, h->N, h->K, h->N * 2, 64, kBlockK);
         if (!ok) {
             h->map_w_ptr = nullptr;
             return PROJ_ERR_CUDA;
         }
         h->map_w_ptr = W;
+        h->map_w_box = w_box_rows(plan);
     }
-    KernelParams kp = h->params;
+    KernelParams kp = stored ? h->params_stored : h->params;
     if (packed) {
         // Packed weights are K-major blocks whatever the stored layout.
         kp.w_packed = 1;
@@ -471,13 +530,14 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     // CTAs then start as the preceding kernel's leave, in its tail.  With SMs
     // idle they would start at once and compete with its weight stream
     // (measured slower on GB300 for the cluster-split and 128-tile plans).
-    kp.w_prefetch =
-        h->overlap == PROJ_OVERLAP_WEIGHTS && plan.grid >= h->sm_count ? h->prefetch_stages : 0;
+    // (Not with CTA pairs, whose stages are armed by the leader for both.)
+    kp.w_prefetch = h->overlap == PROJ_OVERLAP_WEIGHTS && plan.grid >= h->sm_count && !plan.cta_pair
+                        ? h->prefetch_stages
+                        : 0;
     TcLaunch l(plan, s, h->overlap != PROJ_OVERLAP_NONE);
     const bool fused = kp.act != 0 || kp.residual != nullptr;
     const CUtensorMap &map_w = packed ? h->map_wp : h->map_w;
-    if ((fused ? tc_launch_fused(&l.cfg, kp, map_w, h->map_x) : tc_launch_lean(&l.cfg, kp, map_w, h->map_x)) !=
-        cudaSuccess) {
+    if (launch_tc(plan, l, fused, kp, map_w, h->map_x) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }
@@ -546,14 +606,13 @@ proj_status_t proj_device_status(proj_handle_t h, void *stream) {
     if (cudaMemcpy(&word, h->params.status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
         return PROJ_ERR_CUDA;
     if (word == 0) return PROJ_OK;
-    const proj_status_t what =
-        (word & (kErrSmemTooSmall | kErrLaunchShape)) ? PROJ_ERR_CUDA : PROJ_ERR_DEVICE_TIMEOUT;
+    const proj_status_t what = (word & (kErrSmemTooSmall | kErrLaunchShape | kErrPairTmem))
+                                   ? PROJ_ERR_CUDA
+                                   : PROJ_ERR_DEVICE_TIMEOUT;
     // Clear the word and the split-K counters (a run that gave up may have
     // left some mid-count) so the handle is usable again.
-    const proj_plan_desc_t &plan = h->plan;
-    const int64_t partial_bytes = partial_bytes_of(plan);
-    if (cudaMemset(static_cast<uint8_t *>(h->scratch) + partial_bytes, 0,
-                   static_cast<size_t>(plan.scratch_bytes - partial_bytes)) != cudaSuccess)
+    if (cudaMemset(static_cast<uint8_t *>(h->scratch) + h->scratch_clear_from, 0,
+                   static_cast<size_t>(h->scratch_bytes - h->scratch_clear_from)) != cudaSuccess)
         return PROJ_ERR_CUDA;
     return what;
 }
@@ -588,7 +647,9 @@ proj_status_t proj_set_trace(proj_handle_t h, void *device_buffer, size_t bytes)
         return PROJ_OK;
     }
     if (h->plan.kernel != PROJ_KERNEL_TC) return PROJ_ERR_UNSUPPORTED;
-    const size_t need = static_cast<size_t>(h->plan.grid) * kTraceSlots * sizeof(unsigned long long);
+    int32_t grid = h->plan.grid;
+    if (h->has_plan_stored && h->plan_stored.grid > grid) grid = h->plan_stored.grid;
+    const size_t need = static_cast<size_t>(grid) * kTraceSlots * sizeof(unsigned long long);
     if (bytes < need) return PROJ_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(device_buffer) % 8 != 0) return PROJ_ERR_MISALIGNED;
     h->trace = static_cast<unsigned long long *>(device_buffer);
@@ -712,6 +773,12 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     proj_plan_desc_t plan;
     proj_status_t st = plan_for_device(M, N, K, w_layout, y_dtype, bias != nullptr, dd, PlanOptions{}, &plan);
     if (st != PROJ_OK) return st;
+    if (plan.kernel == PROJ_KERNEL_TC && w_layout == PROJ_W_KN && !loads_stored_kn(plan)) {
+        PlanOptions single;
+        single.cta_pair = 0;
+        st = plan_for_device(M, N, K, w_layout, y_dtype, bias != nullptr, dd, single, &plan);
+        if (st != PROJ_OK) return st;
+    }
     if (plan.kernel == PROJ_KERNEL_FILL) {
         dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(M, N, static_cast<const uint16_t *>(bias),
                                                                  Y, y_dtype == PROJ_F32, 0, nullptr);
@@ -736,8 +803,8 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     }
 
     CUtensorMap map_x, map_w;
-    if (!encode_2d(&map_x, X, K, M, K * 2, kBlockK, plan.block_t)) return PROJ_ERR_CUDA;
-    const bool ok = w_layout == PROJ_W_NK ? encode_2d(&map_w, W, K, N, K * 2, kBlockK, plan.block_n)
+    if (!encode_2d(&map_x, X, K, M, K * 2, kBlockK, x_box_rows(plan))) return PROJ_ERR_CUDA;
+    const bool ok = w_layout == PROJ_W_NK ? encode_2d(&map_w, W, K, N, K * 2, kBlockK, w_box_rows(plan))
                                           : encode_2d(&map_w, W, N, K, N * 2, 64, kBlockK);
     if (!ok) return PROJ_ERR_CUDA;
 
@@ -760,7 +827,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
     kp.trace = nullptr;
     TcLaunch l(plan, s, false);
-    if (tc_launch_lean(&l.cfg, kp, map_w, map_x) != cudaSuccess) {
+    if (launch_tc(plan, l, false, kp, map_w, map_x) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }

@@ -22,6 +22,9 @@ constexpr int32_t kMaxStages = 12;
 constexpr int32_t kInflightTarget = 160 * 1024;  // stage bytes per SM when streaming W from HBM
 constexpr int32_t kMaxClusterSplit = 16;          // thread-block cluster size (16: non-portable)
 constexpr int32_t kClusterFillPct = 10;           // SMs a cluster split must keep busy (%)
+// CTA pairs: tensor-memory columns a pair may allocate in each of its SMs
+// (both CTAs allocate together and receive the same columns).
+constexpr int32_t kPairTmemMax = 512;
 constexpr int32_t kThreads = 192;      // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int32_t kEpilogueThreads = 128;
 constexpr int32_t kSmemReserve = 25600; // 1024-byte alignment slack + barriers + epilogue staging
@@ -56,6 +59,7 @@ constexpr int kErrWaitDrain = 1 << 3;
 constexpr int kErrSelfTest = 1 << 4;
 constexpr int kErrSmemTooSmall = 1 << 5;  // launch gave less shared memory than the ring needs
 constexpr int kErrLaunchShape = 1 << 6;   // cluster shape of the launch differs from the plan's
+constexpr int kErrPairTmem = 1 << 7;      // the two CTAs of a pair received different tensor memory
 
 int32_t token_tile_for(int64_t M);
 // Planner options.  force_block_t > 0 forces the swapped orientation with
@@ -70,13 +74,17 @@ struct PlanOptions {
     int32_t force_block_n = 0;
     int32_t max_cluster = kMaxClusterSplit;
     int32_t cluster_fill_pct = kClusterFillPct;
+    // CTA pairs (cta_group::2 MMAs, PROJ_CTA_PAIR): 0 never; 1 where they
+    // measure faster (swapped plans of 256-token tiles that keep half of the
+    // SMs busy); 2 wherever the tile allows (token-major tiles too).
+    int32_t cta_pair = 1;
 };
 // The planner behind proj_plan_compute (which uses the default options).
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
                            proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t *dev,
                            const PlanOptions &opt, proj_plan_desc_t *out);
 // Shared-memory bytes of one pipeline stage: A (128 rows x 64 K) plus B
-// (b_rows x 64 K), bf16.
+// (b_rows x 64 K), bf16.  A CTA of a pair holds half of the B rows.
 int32_t stage_bytes_for(int32_t b_rows);
 int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int w_layout,
                  int y_dtype, int has_bias, char *buf, size_t len);
@@ -94,16 +102,18 @@ struct KernelParams {
     int32_t raster_group;  // token tiles per raster group (tile order, see tile_coords)
     int32_t k_blocks;
     int32_t tiles_dp;      // whole tiles, dealt round-robin: CTA c gets c, c+G, ...
-    int32_t grid;
+    int32_t grid;          // work owners the tiles are dealt to: CTAs, or pairs of CTAs
     int64_t units_sk;      // split-K units after the whole tiles
     int32_t sk_pair;       // every CTA owns >= k_blocks units: a split tile has exactly 2 contributors
     int32_t sk_dense;      // units_sk >= grid: no CTA has an empty unit range
     int32_t cluster_split; // S >= 2: tile c / S split over the S CTAs of a cluster (DSMEM reduction)
+    int32_t cta_pair;      // 1: each tile on a cluster of 2 CTAs, one cta_group::2 MMA of 256 rows
+    int32_t acc_bufs;      // accumulator buffers in tensor memory (2: epilogue overlaps the next tile)
     int32_t stages;
     int32_t stage_bytes;
     int32_t red_bytes;     // cluster split: shared memory after the ring for peers' partial sums
     int32_t tmem_cols;
-    uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128, N=b_rows)
+    uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128 or 256, N=b_rows)
     int32_t w_kn;          // W stored [K,N] (MN-major A operand)
     int32_t w_packed;      // W pre-packed: block (tile, k-block) at row (tn·k_blocks + kb)·block_n
     int32_t x_kb_mod;      // > 0: fp32 router weights as [H | L]; X k-block = kb mod x_kb_mod
@@ -263,26 +273,35 @@ PROJ_HD int32_t cluster_red_bytes(int32_t S, int32_t b_rows) {
     return S > 1 ? cluster_quarters_per_reducer(S) * (S - 1) * 32 * b_rows * 4 : 0;
 }
 
+// B rows of the MMA (its N), and the B rows one CTA holds per stage (half of
+// them in a CTA pair).
+PROJ_HD int32_t plan_b_rows(const proj_plan_desc_t &plan) { return plan.swap_ab ? plan.block_t : plan.block_n; }
+PROJ_HD int32_t plan_cta_b_rows(const proj_plan_desc_t &plan) {
+    return plan.cta_pair ? plan_b_rows(plan) / 2 : plan_b_rows(plan);
+}
+
 inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.swap = plan.swap_ab;
     kp.block_t = plan.block_t;
     kp.block_n = plan.block_n;
-    kp.b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
+    kp.b_rows = plan_b_rows(plan);
     kp.tiles_m = static_cast<int32_t>(plan.tiles_m);
     kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
     kp.raster_group = plan.raster_group > 0 ? plan.raster_group : static_cast<int32_t>(plan.tiles_m);
     kp.k_blocks = static_cast<int32_t>(plan.k_blocks);
     kp.tiles_dp = static_cast<int32_t>(plan.tiles_dp);
-    kp.grid = plan.grid;
+    kp.cta_pair = plan.cta_pair;
+    kp.grid = plan.cta_pair ? plan.grid / 2 : plan.grid;  // pairs own tiles, not CTAs
     kp.units_sk = plan.units_sk;
     kp.sk_pair = plan.grid > 0 && plan.units_sk / plan.grid >= plan.k_blocks;
     kp.sk_dense = plan.units_sk >= plan.grid;
     kp.cluster_split = plan.cluster_split;
     if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;
     kp.stages = plan.stages;
-    kp.stage_bytes = stage_bytes_for(kp.b_rows);
+    kp.stage_bytes = stage_bytes_for(plan_cta_b_rows(plan));
     kp.red_bytes = cluster_red_bytes(plan.cluster_split, kp.b_rows);
     kp.tmem_cols = plan.tmem_cols;
+    kp.acc_bufs = plan.tmem_cols >= 2 * kp.b_rows ? 2 : 1;
 }
 
 }  // namespace projgb

@@ -164,6 +164,12 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t cluster_addr, float4 v) {
                  : "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ float4 ld_shared_f4(uint32_t saddr) {
     float4 v;
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -214,19 +220,48 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
+// CTA pairs: the same load, completing on an mbarrier that may sit in the
+// other CTA of the pair (`bar` is then a shared::cluster address from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *map, uint32_t bar, int32_t x,
+                                                 int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+// Tensor-memory allocation.  Every tcgen05 instruction of a kernel names the
+// same CTA group: cta_group::2 in the CTA-pair instance, where one warp of
+// each CTA of the pair takes part in the allocation and the release.
+template <bool kPair>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (kPair)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
 }
 
+template <bool kPair>
 __device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (kPair)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <bool kPair>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if constexpr (kPair)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before_sync() {
@@ -238,21 +273,50 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 }
 
 // D[tmem] (+)= A[smem] · B[smem]ᵀ, kind::f16 (bf16 operands, fp32 accumulate).
+// cta_group::2 (issued by the even CTA of a pair): M = 256, the A rows and
+// the accumulator rows split 128/128 between the two CTAs, B's rows split in
+// halves (the even CTA holds the first), each CTA's operands at the same
+// shared-memory offsets, so the descriptors of the issuing CTA serve both.
+template <bool kPair>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (kPair)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
 // Arrive once on `bar` when every tcgen05 op this thread issued so far completes.
+template <bool kPair>
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     bar)
-                 : "memory");
+    if constexpr (kPair)
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         bar)
+                     : "memory");
+    else
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         bar)
+                     : "memory");
+}
+
+// CTA pairs: the same arrival on the mbarrier at this shared-memory offset in
+// both CTAs of the pair (cluster ranks 0 and 1).
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            bar),
+        "h"(static_cast<uint16_t>(3))
+        : "memory");
 }
 
 // Load 16 consecutive fp32 columns of this thread's tensor-memory lane and wait
@@ -476,7 +540,7 @@ static_assert(sizeof(SmemCtl) + 1023 <= kSmemReserve, "the reserve holds SmemCtl
 // ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
-template <bool kFused>
+template <bool kFused, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_tc_kernel(const __grid_constant__ KernelParams p, const __grid_constant__ CUtensorMap tmap_w,
                    const __grid_constant__ CUtensorMap tmap_x) {
@@ -504,13 +568,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (threadIdx.x == 0) atomicOr(p.status, kErrLaunchShape);
             return;
         }
+        // A CTA-pair plan runs on the pair instance, in clusters of 2.
+        if ((p.cta_pair != 0) != kPair || (kPair && cluster_nctarank() != 2u)) {
+            if (threadIdx.x == 0) atomicOr(p.status, kErrLaunchShape);
+            return;
+        }
     }
     // The CTA's index in the plan: in a cluster split, cluster c's rank r is
     // CTA c·S + r (tile c, K range r), taken from the hardware's own numbering.
-    const int32_t cta = p.cluster_split > 1
+    // A CTA pair owns tiles as one: its index is the cluster's.
+    const int32_t cta = kPair ? static_cast<int32_t>(cluster_id_x())
+                        : p.cluster_split > 1
                             ? static_cast<int32_t>(cluster_id_x() * static_cast<uint32_t>(p.cluster_split) +
                                                    cluster_ctarank())
                             : static_cast<int32_t>(blockIdx.x);
+    // CTA pairs: rank 0 (the leader) issues the MMAs and owns the barriers
+    // they wait on; rank 1 loads its halves of the operands and runs the
+    // epilogue of its 128 accumulator rows.
+    const uint32_t pair_rank = kPair ? cluster_ctarank() : 0u;
+    const bool leader = pair_rank == 0u;
     uint8_t *smem = smem_raw + (base_addr - raw_addr);
     // [ring: stages x stage_bytes][peers' partial sums: red_bytes][SmemCtl]
     const uint32_t red_addr = base_addr + static_cast<uint32_t>(p.stages * p.stage_bytes);
@@ -533,7 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-            mbar_init(smem_u32(&ctl->acc_empty[b]), kEpilogueThreads / 32);
+            // Pairs: the leader's accumulator is free once both CTAs' epilogue
+            // warps have read their halves.
+            mbar_init(smem_u32(&ctl->acc_empty[b]), (kPair ? 2 : 1) * kEpilogueThreads / 32);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         if (p.cluster_split > 1)
@@ -547,8 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmap_x);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(p.tmem_cols));
-        tmem_relinquish();
+        tmem_alloc<kPair>(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(p.tmem_cols));
+        // A single CTA gives up its right to allocate at once (the next
+        // kernel's CTA on this SM may then allocate while this one runs).  A
+        // pair keeps it until its teardown, after both CTAs have allocated.
+        if constexpr (!kPair) tmem_relinquish<false>();
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -556,11 +637,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Cluster split: announce that this CTA's barriers exist.  A thread waits
     // for the whole cluster's announcement (cluster_waited) before its first
     // access to another CTA's shared memory, and at the latest at teardown.
-    const bool clustered = p.cluster_split > 1;
+    const bool clustered = kPair || p.cluster_split > 1;
     bool cluster_waited = false;
     if (clustered) cluster_arrive();
+    // CTA pairs: both CTAs' barriers and tensor memory exist before any role
+    // starts (the producer's first load completes on the leader's barrier,
+    // the leader's first commit arrives on the peer's).  Every thread waits
+    // here, each warp whole: a cluster-barrier wait from one lane while the
+    // rest of its warp is elsewhere did not return on GB300.
+    if constexpr (kPair) {
+        cluster_wait();
+        cluster_waited = true;
+    }
     const uint32_t tmem_base = ctl->tmem_base;
     const uint32_t half_cols = static_cast<uint32_t>(p.tmem_cols / 2);
+    // Accumulator buffer of the n-th tile and the parity of its use.
+    auto acc_buf = [&](int32_t n) { return p.acc_bufs == 2 ? n & 1 : 0; };
+    auto acc_use = [&](int32_t n) { return static_cast<uint32_t>(p.acc_bufs == 2 ? n >> 1 : n) & 1u; };
     if (threadIdx.x == 0) {
         // Only on-chip state has been touched so far; the next kernel may begin
         // its own set-up.  Global memory is touched only after griddep_wait().
@@ -582,6 +675,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = p.tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
             const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
+            // CTA pairs: this CTA's halves of the tile's weight and token rows.
+            const int32_t w_row_off = static_cast<int32_t>(pair_rank) * (p.block_n / 2);
+            const int32_t x_row_off = static_cast<int32_t>(pair_rank) * (p.block_t / 2);
+            const int32_t w_rows = kPair ? p.block_n / 2 : p.block_n;
+            // Loads complete on the leader's "full" barrier (the MMA issuer's).
+            auto full_bar = [&](int32_t st) {
+                const uint32_t a = smem_u32(&ctl->full[st]);
+                return (kPair && !leader) ? map_to_rank(a, 0u) : a;
+            };
+            auto load = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y,
+                            uint64_t pol) {
+                if constexpr (kPair)
+                    tma_load_2d_pair(dst, map, bar, x, y, pol);
+                else
+                    tma_load_2d(dst, map, bar, x, y, pol);
+            };
             // One k-block of a weight tile: a [block_n rows x 64 K] box for
             // [N,K] weights; for [K,N] weights, block_n/64 boxes of 64 N-rows
             // x 64 K, 8 KiB apart (the MN-major operand layout).
@@ -589,19 +698,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.w_packed) {
                     // Pre-packed: the stage is one contiguous block of block_n
                     // rows x 128 bytes (a 2-D map of 64-wide rows).
-                    tma_load_2d(dst, &tmap_w, full, 0, (tn * p.k_blocks + kb) * p.block_n, pol_w);
+                    load(dst, &tmap_w, full, 0, (tn * p.k_blocks + kb) * p.block_n + w_row_off, pol_w);
                 } else if (!p.w_kn) {
-                    tma_load_2d(dst, &tmap_w, full, kb * kBlockK, tn * p.block_n, pol_w);
+                    load(dst, &tmap_w, full, kb * kBlockK, tn * p.block_n + w_row_off, pol_w);
                 } else {
-                    for (int32_t j = 0; j < p.block_n / 64; ++j)
-                        tma_load_2d(dst + static_cast<uint32_t>(j) * 8192u, &tmap_w, full,
-                                    tn * p.block_n + 64 * j, kb * kBlockK, pol_w);
+                    for (int32_t j = 0; j < w_rows / 64; ++j)
+                        load(dst + static_cast<uint32_t>(j) * 8192u, &tmap_w, full,
+                             tn * p.block_n + w_row_off + 64 * j, kb * kBlockK, pol_w);
                 }
             };
             // Optional weight prefetch: fill the ring with W before the
             // preceding kernel has finished (W must not be written by it).
             int64_t pre = 0;
-            if (p.w_prefetch > 0) {
+            if (!kPair && p.w_prefetch > 0) {
                 const int32_t pre_max = min(p.w_prefetch, stages);
                 WorkIter it;
                 it.init(p, cta);
@@ -641,15 +750,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int32_t tm, tn;
                 tile_coords(p, s.tile, tm, tn);
                 for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
-                    const uint32_t full = smem_u32(&ctl->full[stage]);
+                    const uint32_t full = full_bar(stage);
                     const uint32_t st_base = base_addr + stage * stage_bytes;
                     if (issued >= pre) {
-                        if (!wait_phase(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.status,
-                                        kErrWaitProducer, p.wait_limit_ns)) {
+                        if (!wait_phase<kPair>(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_flag, p.status,
+                                               kErrWaitProducer, p.wait_limit_ns)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(full, stage_bytes);
+                        // The leader expects both CTAs' bytes of the stage.
+                        if (leader) mbar_arrive_expect_tx(full, (kPair ? 2u : 1u) * stage_bytes);
                         dep_wait();
                         load_w(st_base + w_off, full, tn, kb);
                     }
@@ -657,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // fp32 router weights run as [H | L] along K: the second
                     // half multiplies the same X k-blocks again.
                     const int32_t xkb = (p.x_kb_mod > 0 && kb >= p.x_kb_mod) ? kb - p.x_kb_mod : kb;
-                    tma_load_2d(st_base + x_off, &tmap_x, full, xkb * kBlockK, tm * p.block_t, pol_x);
+                    load(st_base + x_off, &tmap_x, full, xkb * kBlockK, tm * p.block_t + x_row_off, pol_x);
                     if (issued == 0 && pre == 0) trace_stamp(p, kTraceFirstLoad);
                     ++issued;
                     if (++stage == stages) {
@@ -671,7 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // (CTA pairs: the leader's, for both CTAs.)
+        if (lane == 0 && leader) {
             const bool a_mn = p.swap && p.w_kn;   // weights [K,N] as the A operand
             const bool b_mn = !p.swap && p.w_kn;  // weights [K,N] as the B operand
             int32_t stage = 0;
@@ -682,16 +793,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             Segment s;
             bool ok = true;
             while (ok && it.next(p, s)) {
-                const int32_t buf = seg_idx & 1;
-                const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
-                if (!wait_phase(smem_u32(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, p.status,
-                                kErrWaitMma, p.wait_limit_ns))
+                const int32_t buf = acc_buf(seg_idx);
+                const uint32_t use = acc_use(seg_idx);
+                if (!wait_phase<kPair>(smem_u32(&ctl->acc_empty[buf]), use ^ 1u, abort_flag, p.status,
+                                       kErrWaitMma, p.wait_limit_ns))
                     break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf) * half_cols;
                 for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
-                    if (!wait_phase(smem_u32(&ctl->full[stage]), phase, abort_flag, p.status,
-                                    kErrWaitMma, p.wait_limit_ns)) {
+                    if (!wait_phase<kPair>(smem_u32(&ctl->full[stage]), phase, abort_flag, p.status,
+                                           kErrWaitMma, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -711,16 +822,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t b_desc =
                             b_mn ? smem_desc_sw128(b_addr + kk * (kMmaK * 128), 8192, 1024)
                                  : smem_desc_sw128(b_addr + kk * (kMmaK * 2), 16, 1024);
-                        tc_mma(d_tmem, a_desc, b_desc, p.idesc, (kb > s.kb0 || kk > 0) ? 1u : 0u);
+                        tc_mma<kPair>(d_tmem, a_desc, b_desc, p.idesc, (kb > s.kb0 || kk > 0) ? 1u : 0u);
                     }
-                    tc_commit(smem_u32(&ctl->empty[stage]));  // stage free once these MMAs finish
+                    // The stage is free (in both CTAs of a pair) once these MMAs finish.
+                    if constexpr (kPair)
+                        tc_commit_pair(smem_u32(&ctl->empty[stage]));
+                    else
+                        tc_commit<false>(smem_u32(&ctl->empty[stage]));
                     if (++stage == stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&ctl->acc_full[buf]));  // accumulator ready
+                // The accumulator is ready (both CTAs' halves of it, for a pair).
+                if constexpr (kPair)
+                    tc_commit_pair(smem_u32(&ctl->acc_full[buf]));
+                else
+                    tc_commit<false>(smem_u32(&ctl->acc_full[buf]));
                 ++seg_idx;
             }
             trace_stamp(p, kTraceLastMma);
@@ -733,10 +852,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t U = p.units_sk;
         griddep_wait();  // partials, counters and Y may be in use by the preceding kernel
         if (warp == 2 && lane == 0) trace_stamp(p, kTraceEpiDepWait);
-        if (clustered) {
-            cluster_wait();  // every CTA of the cluster has initialised its barriers
+        if (clustered && !cluster_waited) {
+            cluster_wait();  // every CTA of the cluster has initialised its barriers (whole warps)
             cluster_waited = true;
         }
+        // CTA pairs: the MMAs write the accumulator at the leader's address in
+        // both CTAs' tensor memory.  Both CTAs allocate together and receive
+        // the same columns; a difference is recorded (and the leader's used).
+        uint32_t acc_base = tmem_base;
+        if (kPair && !leader) {
+            acc_base = ld_cluster_u32(map_to_rank(smem_u32(&ctl->tmem_base), 0u));
+            if (acc_base != tmem_base && warp == 2 && lane == 0) atomicOr(p.status, kErrPairTmem);
+        }
+        // Where this CTA's epilogue warps report an accumulator read.
+        const uint32_t acc_empty_bar0 =
+            kPair ? map_to_rank(smem_u32(&ctl->acc_empty[0]), 0u) : smem_u32(&ctl->acc_empty[0]);
         int32_t seg_idx = 0;
         bool split_traced = false;  // the split-epilogue stamps cover the first split tile
         float *bias_s = ctl->bias_tile[q];
@@ -744,20 +874,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         it.init(p, cta);
         Segment s;
         while (it.next(p, s)) {
-            const int32_t buf = seg_idx & 1;
-            const uint32_t use = static_cast<uint32_t>(seg_idx >> 1) & 1u;
+            const int32_t buf = acc_buf(seg_idx);
+            const uint32_t use = acc_use(seg_idx);
             int32_t tm, tn;
             tile_coords(p, s.tile, tm, tn);
             // Tensor-memory lane r holds one A row, columns hold B rows.
             // Swapped: lane = weight row n, columns = token rows m.
             // Otherwise: lane = token row m, columns = weight rows n.
-            const int32_t m0 = tm * p.block_t;
-            const int32_t n0 = tn * p.block_n;
+            // A CTA of a pair holds A rows 128·rank .. 128·rank + 127 of the
+            // pair's 256 and every B row (column).
+            int32_t m0 = tm * p.block_t;
+            int32_t n0 = tn * p.block_n;
+            if (kPair) {
+                if (p.swap)
+                    n0 += kBlockA * static_cast<int32_t>(pair_rank);
+                else
+                    m0 += kBlockA * static_cast<int32_t>(pair_rank);
+            }
             const int32_t lane_row = (p.swap ? n0 : m0) + r;
             const bool lane_ok = lane_row < (p.swap ? p.N : p.M);
             const int32_t ccount = p.swap ? min(p.block_t, p.M - m0) : min(p.block_n, p.N - n0);
             const int32_t nchunks = (ccount + 15) / 16;
-            const uint32_t tbase = tmem_base + lane_off + static_cast<uint32_t>(buf) * half_cols;
+            const uint32_t tbase = acc_base + lane_off + static_cast<uint32_t>(buf) * half_cols;
             // The bias is fetched before the accumulator wait, so that a DRAM
             // round trip under the weight stream's load overlaps the MMAs:
             // swapped, one value per lane (its weight row); token-major, the
@@ -769,8 +907,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bias_s[j] = n0 + j < p.N ? bf16_bits_to_float(p.bias[n0 + j]) : 0.f;
                 __syncwarp();
             }
-            if (!wait_phase(smem_u32(&ctl->acc_full[buf]), use, abort_flag, p.status,
-                            kErrWaitEpilogue, p.wait_limit_ns))
+            if (!wait_phase<kPair>(smem_u32(&ctl->acc_full[buf]), use, abort_flag, p.status,
+                                   kErrWaitEpilogue, p.wait_limit_ns))
                 break;
             tc_fence_after_sync();
             if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
@@ -1038,7 +1176,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto release_accumulator = [&]() {
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctl->acc_empty[buf]));
+                if (lane == 0) {
+                    const uint32_t bar = acc_empty_bar0 + static_cast<uint32_t>(buf) * 8u;
+                    if constexpr (kPair)
+                        mbar_arrive_remote(bar);  // the leader's barrier (release at cluster scope)
+                    else
+                        mbar_arrive(bar);
+                }
             };
 
             if (!s.split) {
@@ -1269,7 +1413,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (*abort_flag) {
         // Let every copy and MMA already in flight land before the CTA leaves.
-        if (warp == 0 && lane == 0) {
+        if (kPair && !leader && warp == 0 && lane == 0 && issued > 0) {
+            // The peer's loads complete on the leader's barriers: give them a
+            // fixed 100 µs (an in-bounds TMA copy lands in a few).
+            const uint64_t t0 = globaltimer_ns();
+            while (globaltimer_ns() - t0 < 100000ull) {
+            }
+        } else if (warp == 0 && lane == 0) {
             for (int32_t st = 0; st < stages; ++st) {
                 const int64_t times = issued > st ? (issued - 1 - st) / stages + 1 : 0;
                 if (times > 0) {
@@ -1279,8 +1429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (warp == 1 && lane == 0) {
-            tc_commit(smem_u32(&ctl->drain));
+        if (warp == 1 && lane == 0 && leader) {
+            tc_commit<kPair>(smem_u32(&ctl->drain));
             volatile int never = 0;
             wait_phase(smem_u32(&ctl->drain), 0, &never, p.status, kErrWaitDrain, p.wait_limit_ns);
         }
@@ -1296,7 +1446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+        if constexpr (kPair) tmem_relinquish<true>();
+        tmem_dealloc<kPair>(tmem_base, static_cast<uint32_t>(p.tmem_cols));
     }
 }
 

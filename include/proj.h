@@ -118,6 +118,11 @@ typedef struct proj_device_desc {
  * each tile gets its own cluster of S CTAs, grid = tiles_sk · S, and the
  * partial sums meet in distributed shared memory; no partial-sum scratch and
  * no counters.
+ * CTA pairs (cta_pair = 1): the tensor-bound shapes whose tiles are computed
+ * whole (several token tiles) run each tile on two CTAs of a cluster.  One
+ * MMA spans both CTAs' shared memory, so each CTA holds half of the B operand
+ * per stage: fewer bytes per stage, a deeper ring and half the weight (or
+ * token) rows per CTA from L2.
  */
 typedef struct proj_plan_desc {
     int32_t kernel;          /* proj_kernel_t */
@@ -138,6 +143,13 @@ typedef struct proj_plan_desc {
                                 thread-block cluster (CTA c: tile c / S, rank c % S, k-blocks
                                 [⌊r·k_blocks/S⌋, ⌊(r+1)·k_blocks/S⌋)), and the partial sums are
                                 added through distributed shared memory in rank order */
+    int32_t cta_pair;        /* 1: every tile is computed by a pair of CTAs (a cluster of 2) with
+                                one 256-row tensor-core MMA (tcgen05 cta_group::2).  The pair
+                                tile is 256 rows on the MMA's M side (block_n = 256 weight rows
+                                when swap_ab, else block_t = 256 tokens); each CTA loads half
+                                of the tile's weight rows and half of its token rows, and holds
+                                128 of the M rows' accumulators.  grid counts CTAs (2 per pair);
+                                tiles are dealt to pairs.  Whole tiles only (tiles_sk = 0) */
     int64_t tiles_m;         /* ceil(M / block_t) */
     int64_t tiles_n;         /* ceil(N / block_n) */
     int64_t k_blocks;        /* ceil(K / block_k) */
@@ -176,7 +188,7 @@ typedef struct proj_segment {
 /*
  * Host introspection of a PROJ_KERNEL_TC plan (pure host code, the same
  * decomposition code the kernel runs): the segments CTA `cta` executes, in
- * order.  Writes min(cap, total) segments to `out` and the total to *count.
+ * order (in a CTA-pair plan, CTAs 2p and 2p + 1 both run pair p's tiles).  Writes min(cap, total) segments to `out` and the total to *count.
  * A plan of another kernel kind yields zero segments.  PROJ_ERR_INVALID_ARG
  * for a NULL count/plan, a negative cap, or cta outside [0, grid).
  */
@@ -220,6 +232,7 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
  *   PROJ_FORCE_BLOCK_N=n     token-major orientation with weight tile n
  *   PROJ_MAX_CLUSTER=s       largest cluster split (0 or 1: none)
  *   PROJ_CLUSTER_FILL_PCT=f  SMs (%) a cluster split must keep busy
+ *   PROJ_CTA_PAIR=0|1        CTA pairs off, or on wherever the plan allows them
  *   PROJ_FORCE_STAGES=k      fewer pipeline stages than planned
  *   PROJ_FORCE_GRID=g        fewer CTAs for an all-split plan
  *   PROJ_FORCE_WHOLE_TILES=1 no split tiles

@@ -64,7 +64,16 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     G, KT = p["grid"], p["k_blocks"]
     tiles = p["tiles_m"] * p["tiles_n"]
     assert p["tiles_m"] == -(-M // p["block_t"]) and p["tiles_n"] == -(-N // p["block_n"])
-    if p["swap_ab"]:
+    pair = p["cta_pair"]
+    if pair:
+        # CTA pairs: 256 rows on the MMA's M side (two CTAs of 128), the N
+        # side a multiple of 32 in [64, 256] split in halves; whole tiles
+        # dealt to pairs, two CTAs each.
+        a, b = ("block_n", "block_t") if p["swap_ab"] else ("block_t", "block_n")
+        assert p[a] == 256 and p[b] % 32 == 0 and 64 <= p[b] <= 256
+        assert p["cluster_split"] == 0 and p["tiles_sk"] == 0 and p["scratch_bytes"] == 256
+        assert G % 2 == 0 and G == 2 * min(tiles, sms // 2)
+    elif p["swap_ab"]:
         assert p["block_n"] == 128 and p["block_t"] % 16 == 0
     else:
         assert p["block_t"] == 128 and p["block_n"] % 16 == 0 and 64 <= p["block_n"] <= 256
@@ -81,7 +90,7 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
         assert p["scratch_bytes"] == 256
     if p["tiles_sk"]:
         assert p["tiles_dp"] % G == 0
-    else:  # whole tiles only: the last wave is nearly full (95 % swapped, 80 % token-major)
+    elif not pair:  # whole tiles only: the last wave is nearly full (95 % swapped, 80 % token-major)
         waves = -(-tiles // G)
         pct = 95 if p["swap_ab"] else 80
         assert tiles % G == 0 or 100 * tiles >= pct * waves * G
@@ -89,7 +98,11 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     assert p["smem_bytes"] <= GB300["smem_optin_bytes"] and p["stages"] >= 2
     assert p["block_t"] % 16 == 0 and 16 <= p["block_t"] <= 256
     b_rows = p["block_t"] if p["swap_ab"] else p["block_n"]
-    assert p["tmem_cols"] >= 2 * b_rows
+    if pair:
+        # Two accumulator buffers (at most 512 columns a pair allocates per SM).
+        assert p["tmem_cols"] <= 512 and p["tmem_cols"] >= 2 * b_rows
+    else:
+        assert p["tmem_cols"] >= 2 * b_rows
     # The launch's shared memory covers the ring (A 128 rows + B rows, 64 K each),
     # its barriers, the epilogue's bias and output staging, 1024-byte alignment slack,
     # and in a cluster split the peers' partial sums: S - 1 partials of 32 rows
@@ -99,12 +112,15 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     if S:
         quarters = -(-4 // S) if S <= 4 else 1
         red = quarters * (S - 1) * 32 * b_rows * 4
-    assert p["smem_bytes"] == p["stages"] * (128 + b_rows) * 128 + red + 25600
+    # A CTA of a pair stages half of the B rows.
+    assert p["smem_bytes"] == p["stages"] * (128 + (b_rows // 2 if pair else b_rows)) * 128 + red + 25600
     cover = np.zeros((tiles, KT), dtype=np.int32)
     by_tile = collections.defaultdict(list)
     coords = {}
     slots = set()
-    for c in range(G):
+    for c in range(0, G, 2 if pair else 1):
+        if pair:  # both CTAs of a pair run the pair's tiles
+            assert dlp.proj_plan_segments(p, c) == dlp.proj_plan_segments(p, c + 1)
         for (tile, tm, tn, kb0, kb1, slot, split) in dlp.proj_plan_segments(p, c):
             assert 0 <= tm < p["tiles_m"] and 0 <= tn < p["tiles_n"] and 0 <= kb0 < kb1 <= KT
             assert coords.setdefault(tile, (tm, tn)) == (tm, tn)
@@ -263,15 +279,17 @@ def test_raster_groups():
     # Prefill: 16 token tiles of 256 rows in groups of 8 (2048 token rows);
     # within a group the token tile varies fastest, so the first wave covers
     # 8 token panels x 19 weight panels.
+    # The tiles are 256 weight rows wide (CTA pairs): 76 pairs cover 8 token
+    # panels x 10 weight panels.
     p = plan(4096, 8192, 8192)
-    assert p["raster_group"] == 8 and p["tiles_m"] == 16
+    assert p["raster_group"] == 8 and p["tiles_m"] == 16 and p["cta_pair"] == 1
     first_wave = set()
     for c in range(p["grid"]):
         tile, tm, tn = dlp.proj_plan_segments(p, c)[0][:3]
-        assert tile == c
+        assert tile == c // 2
         first_wave.add((tm, tn))
     assert {tm for tm, _ in first_wave} == set(range(8))
-    assert len({tn for _, tn in first_wave}) == 19
+    assert len({tn for _, tn in first_wave}) == 10
     assert plan(16, 8192, 8192)["raster_group"] == 1
 
 
@@ -281,13 +299,35 @@ def test_orientation_and_weight_tile_choice():
         assert plan(M, 8192, 8192)["swap_ab"] == 1
     # From 128 tokens: tokens on the M side, weight tile sized to fill waves.
     qkv = plan(256, 12288, 4096, 1)
-    assert qkv["swap_ab"] == 0 and qkv["block_t"] == 128
+    assert qkv["swap_ab"] == 0 and qkv["block_t"] == 128 and qkv["cta_pair"] == 0
     assert qkv["block_n"] == 192 and qkv["tiles_m"] * qkv["tiles_n"] == 128
     assert qkv["tiles_sk"] == 0  # one whole wave (84 % of the SMs) beats splitting
     # Many tiles either way (prefill): the swapped 256-token x 128-row tiles.
+    # Many tiles either way (prefill): swapped 256-token tiles, on CTA pairs of
+    # 2 x 128 weight rows.
     pre = plan(4096, 8192, 8192)
-    assert (pre["swap_ab"], pre["block_t"], pre["block_n"], pre["tiles_sk"]) == (1, 256, 128, 0)
-    # [K,N] weights load in 64-row boxes: the weight tile is a multiple of 64.
+    assert (pre["swap_ab"], pre["block_t"], pre["block_n"], pre["tiles_sk"]) == (1, 256, 256, 0)
+    assert pre["cta_pair"] == 1 and pre["tmem_cols"] == 512 and pre["grid"] == 152
+    # [K,N] weights load in 64-row boxes: the weight tile of a single-CTA plan
+    # is a multiple of 64.  A pair's tile is a multiple of 32 (the handle runs
+    # weights as stored on a single-CTA plan when the halves are not whole
+    # boxes; packed weights have no such limit).
     for N in (1000, 3000, 9000):  # few enough weight rows that swapped tiles leave SMs idle
         p = plan(300, N, 1024, 1)
-        assert p["swap_ab"] == 0 and p["block_n"] % 64 == 0
+        assert p["swap_ab"] == 0 and p["block_n"] % (32 if p["cta_pair"] else 64) == 0
+
+
+def test_cta_pair_choice():
+    # Pairs only for swapped 256-token tiles that keep half of the SMs busy.
+    assert plan(16, 8192, 8192)["cta_pair"] == 0           # decode: stream-K
+    assert plan(100, 1024, 8192)["cta_pair"] == 0          # two 64-token tiles: cluster split
+    assert plan(64, 28672, 8192)["cta_pair"] == 0          # weight streaming
+    assert plan(256, 12288, 4096, 1)["cta_pair"] == 0      # token-major: single CTAs
+    assert plan(1024, 4096, 4096)["cta_pair"] == 0         # token-major
+    p = plan(512, 20480, 256)
+    assert (p["cta_pair"], p["swap_ab"], p["block_t"], p["block_n"]) == (1, 1, 256, 256)
+    assert p["tiles_m"] * p["tiles_n"] == 160 and p["grid"] == 152
+    # Stages: 16 KiB of A (128 weight rows) plus half of the 256 token rows.
+    assert p["stages"] == 6 and p["smem_bytes"] == 6 * (16384 + 128 * 128) + 25600
+    # A small swapped problem: too few pair tiles for half of the SMs.
+    assert plan(256, 4096, 1024)["cta_pair"] == 0
