@@ -111,6 +111,10 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 bt = half;
             }
         }
+        // Half tiles (an option, off by default): 64 weight rows per swapped
+        // tile of at most 64 tokens (the MMA keeps M = 128; its rows 64-127
+        // are not used), twice the tiles of a narrow few-tile shape.
+        if (opt.half_tiles == 2 && bt <= 64) bn = kBlockA / 2;
     } else {
         bt = kBlockA;
         if (force_block_n > 0) {

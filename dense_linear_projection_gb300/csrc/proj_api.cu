@@ -275,6 +275,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int c = std::atoi(e);
         if (c >= 0 && c <= 2) opt.cta_pair = c;
     }
+    if (const char *e = std::getenv("PROJ_HALF_TILES")) opt.half_tiles = std::atoi(e) == 2 ? 2 : 0;
     // fp32 weights: the reduction runs over [H | L], twice the k-blocks of K.
     const int64_t kt = (K + kBlockK - 1) / kBlockK;
     const int64_t k_plan = hilo ? 2 * kt * kBlockK : K;

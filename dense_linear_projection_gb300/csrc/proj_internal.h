@@ -78,6 +78,11 @@ struct PlanOptions {
     // measure faster (swapped plans of 256-token tiles that keep half of the
     // SMs busy); 2 wherever the tile allows (token-major tiles too).
     int32_t cta_pair = 1;
+    // Half tiles (PROJ_HALF_TILES=2): swapped tiles of 64 weight rows, for
+    // any swapped plan of at most 64 tokens.  Off by default: on GB300 the
+    // 2048-row decode weight ran 15.9 us on 32 half tiles in clusters of 4
+    // (128 SMs) against 12.6 us on 16 full tiles in clusters of 6 (96 SMs).
+    int32_t half_tiles = 0;
 };
 // The planner behind proj_plan_compute (which uses the default options).
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
@@ -110,7 +115,9 @@ struct KernelParams {
     int32_t cta_pair;      // 1: each tile on a cluster of 2 CTAs, one cta_group::2 MMA of 256 rows
     int32_t acc_bufs;      // accumulator buffers in tensor memory (2: epilogue overlaps the next tile)
     int32_t stages;
-    int32_t stage_bytes;
+    int32_t stage_bytes;   // shared memory of one stage (A region of 128 rows + B rows)
+    int32_t stage_tx;      // bytes one CTA's loads bring into a stage (A rows loaded + B rows)
+    int32_t a_rows;        // A rows of a tile this CTA holds: 128, or 64 (half tiles: MMA rows 64-127 unused)
     int32_t red_bytes;     // cluster split: shared memory after the ring for peers' partial sums
     int32_t tmem_cols;
     uint32_t idesc;        // tcgen05 instruction descriptor (bf16 x bf16 -> f32, M=128 or 256, N=b_rows)
@@ -299,6 +306,10 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;
     kp.stages = plan.stages;
     kp.stage_bytes = stage_bytes_for(plan_cta_b_rows(plan));
+    // A rows per CTA: the weight rows of a swapped tile (64 for half tiles,
+    // 128 of a pair's 256), else 128 token rows.
+    kp.a_rows = plan.swap_ab ? (plan.cta_pair ? plan.block_n / 2 : plan.block_n) : kBlockA;
+    kp.stage_tx = (kp.a_rows + plan_cta_b_rows(plan)) * kBlockK * 2;
     kp.red_bytes = cluster_red_bytes(plan.cluster_split, kp.b_rows);
     kp.tmem_cols = plan.tmem_cols;
     kp.acc_bufs = plan.tmem_cols >= 2 * kp.b_rows ? 2 : 1;

@@ -675,6 +675,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = p.tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
             const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
+            // Bytes a stage's loads bring: less than the stage for half tiles
+            // (64 weight rows in the 128-row A region).
+            const uint32_t stage_tx = static_cast<uint32_t>(p.stage_tx);
             // CTA pairs: this CTA's halves of the tile's weight and token rows.
             const int32_t w_row_off = static_cast<int32_t>(pair_rank) * (p.block_n / 2);
             const int32_t x_row_off = static_cast<int32_t>(pair_rank) * (p.block_t / 2);
@@ -720,7 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tile_coords(p, s.tile, tm, tn);
                     for (int32_t kb = s.kb0; kb < s.kb1 && pre < pre_max; ++kb) {
                         const uint32_t full = smem_u32(&ctl->full[pre]);
-                        mbar_arrive_expect_tx(full, stage_bytes);  // W + X bytes of the stage
+                        mbar_arrive_expect_tx(full, stage_tx);  // W + X bytes of the stage
                         load_w(base_addr + static_cast<uint32_t>(pre) * stage_bytes + w_off, full, tn, kb);
                         ++pre;
                     }
@@ -759,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         // The leader expects both CTAs' bytes of the stage.
-                        if (leader) mbar_arrive_expect_tx(full, (kPair ? 2u : 1u) * stage_bytes);
+                        if (leader) mbar_arrive_expect_tx(full, (kPair ? 2u : 1u) * stage_tx);
                         dep_wait();
                         load_w(st_base + w_off, full, tn, kb);
                     }
@@ -892,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     m0 += kBlockA * static_cast<int32_t>(pair_rank);
             }
             const int32_t lane_row = (p.swap ? n0 : m0) + r;
-            const bool lane_ok = lane_row < (p.swap ? p.N : p.M);
+            const bool lane_ok = r < p.a_rows && lane_row < (p.swap ? p.N : p.M);
             const int32_t ccount = p.swap ? min(p.block_t, p.M - m0) : min(p.block_n, p.N - n0);
             const int32_t nchunks = (ccount + 15) / 16;
             const uint32_t tbase = acc_base + lane_off + static_cast<uint32_t>(buf) * half_cols;
@@ -912,6 +915,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after_sync();
             if (warp == 2 && lane == 0 && seg_idx == 0) trace_stamp(p, kTraceFirstAcc);
+            if (q * 32 >= p.a_rows) {
+                // Half tiles: this warp's accumulator rows come from the
+                // unused half of the A region.  Nothing to store or reduce.
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t bar = acc_empty_bar0 + static_cast<uint32_t>(buf) * 8u;
+                    if constexpr (kPair)
+                        mbar_arrive_remote(bar);
+                    else
+                        mbar_arrive(bar);
+                }
+                ++seg_idx;
+                continue;
+            }
             const bool stamp_split = s.split && !split_traced && warp == 2 && lane == 0;
             if (s.split) split_traced = true;
             // Store one chunk of 16 columns of this lane's row (+ bias, the

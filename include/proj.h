@@ -232,7 +232,8 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
  *   PROJ_FORCE_BLOCK_N=n     token-major orientation with weight tile n
  *   PROJ_MAX_CLUSTER=s       largest cluster split (0 or 1: none)
  *   PROJ_CLUSTER_FILL_PCT=f  SMs (%) a cluster split must keep busy
- *   PROJ_CTA_PAIR=0|1        CTA pairs off, or on wherever the plan allows them
+ *   PROJ_CTA_PAIR=0|2        CTA pairs off, or on wherever the tile allows them
+ *   PROJ_HALF_TILES=2        swapped tiles of 64 weight rows (at most 64 tokens)
  *   PROJ_FORCE_STAGES=k      fewer pipeline stages than planned
  *   PROJ_FORCE_GRID=g        fewer CTAs for an all-split plan
  *   PROJ_FORCE_WHOLE_TILES=1 no split tiles

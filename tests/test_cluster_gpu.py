@@ -69,15 +69,23 @@ def test_cluster_split_parity(shape, monkeypatch):
         (100, 264, 520, synth.W_KN, True, "f32"),    # 2 token x 3 weight tiles, 9 k-blocks, ragged
     ) if S <= -(-shape[2] // 64)
 ], ids=lambda v: str(v))
-def test_every_cluster_size(S, M, N, K, layout, bias, yd, monkeypatch):
+@pytest.mark.parametrize("half", ["0", "2"], ids=["full_tiles", "half_tiles"])
+def test_every_cluster_size(S, M, N, K, layout, bias, yd, half, monkeypatch):
+    # Full tiles take exactly S; half tiles (64 weight rows, twice the
+    # clusters) take S or, where that many clusters of S do not fit at once,
+    # a smaller split.
     import torch
     import dense_linear_projection_gb300 as dlp
     monkeypatch.setenv("PROJ_MAX_CLUSTER", str(S))
     monkeypatch.setenv("PROJ_CLUSTER_FILL_PCT", "1")  # a few tiles: any fill will do
+    monkeypatch.setenv("PROJ_HALF_TILES", half)
     w = synth.Workload("t", M, N, K, layout, bias, yd, seed=70 + S)
     inp = synth.make_inputs(w)
     proj, Y, (X, W, b) = gu.run(w, inp)
-    assert proj.plan["cluster_split"] == S
+    if half == "0":
+        assert proj.plan["cluster_split"] == S and proj.plan["block_n"] == 128
+    else:
+        assert 2 <= proj.plan["cluster_split"] <= S and proj.plan["block_n"] == 64
     again = proj(X, W, b).clone()
     torch.cuda.synchronize()
     assert proj.status() == dlp.PROJ_OK
