@@ -567,6 +567,47 @@ proj_status_t proj_run_host_packed(proj_handle_t h, const void *X_host, const vo
 }  // extern "C"
 
 namespace {
+
+// The device address of a host buffer the device can read and write (pinned
+// by cudaHostAlloc or registered by cudaHostRegister), or nullptr (pageable
+// memory, or a buffer the runtime does not know).
+void *host_device_pointer(const void *p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// One host <-> device copy: a copy kernel chained to its neighbours by
+// programmatic dependent launch when the host buffer is device-addressable
+// and both ends are 16-byte aligned, else cudaMemcpyAsync.
+proj_status_t copy_host(void *dst_dev, const void *src_dev, void *dst, const void *src, size_t bytes,
+                        cudaMemcpyKind kind, int sm_count, cudaStream_t s) {
+    if (bytes == 0) return PROJ_OK;
+    if (src_dev && dst_dev && aligned16(src_dev) && aligned16(dst_dev)) {
+        const int64_t n16 = static_cast<int64_t>(bytes / 16);
+        const int64_t want = (n16 + 255) / 256;
+        cudaLaunchConfig_t cfg{};
+        cudaLaunchAttribute attr[1];
+        cfg.gridDim = dim3(static_cast<unsigned>(want < 1 ? 1 : (want < 2 * sm_count ? want : 2 * sm_count)));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, dev::proj_copy_kernel, static_cast<const uint8_t *>(src_dev),
+                               static_cast<uint8_t *>(dst_dev), static_cast<int64_t>(bytes)) != cudaSuccess) {
+            cudaGetLastError();
+            return PROJ_ERR_CUDA;
+        }
+        return PROJ_OK;
+    }
+    return cudaMemcpyAsync(dst, src, bytes, kind, s) == cudaSuccess ? PROJ_OK : PROJ_ERR_CUDA;
+}
+
 proj_status_t run_host_impl(proj_handle_t h, const void *X_host, const void *W, bool packed,
                             const void *bias, void *Y_host, void *stream) {
     if (!h) return PROJ_ERR_INVALID_ARG;
@@ -587,13 +628,15 @@ proj_status_t run_host_impl(proj_handle_t h, const void *X_host, const void *W, 
         }
     }
     cudaStream_t s = as_stream(stream);
-    if (xb && cudaMemcpyAsync(h->stage_x, X_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return PROJ_ERR_CUDA;
-    proj_status_t st = run_impl(h, h->stage_x, W, packed, bias, nullptr, h->stage_y, stream);
+    // Device addresses of the host buffers, looked up on every call (a buffer
+    // may be freed and its address reused by memory of another kind).
+    const void *x_dev = X_host ? host_device_pointer(X_host) : nullptr;
+    void *y_dev = host_device_pointer(Y_host);
+    proj_status_t st = copy_host(h->stage_x, x_dev, h->stage_x, X_host, xb, cudaMemcpyHostToDevice, h->sm_count, s);
     if (st != PROJ_OK) return st;
-    if (cudaMemcpyAsync(Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return PROJ_ERR_CUDA;
-    return PROJ_OK;
+    st = run_impl(h, h->stage_x, W, packed, bias, nullptr, h->stage_y, stream);
+    if (st != PROJ_OK) return st;
+    return copy_host(y_dev, h->stage_y, Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, h->sm_count, s);
 }
 }  // namespace
 

@@ -133,6 +133,26 @@ __global__ void proj_pack_hilo_kernel(const float *W, uint16_t *P, int64_t N, in
     }
 }
 
+// Host <-> device copy of proj_run_host through memory the device can address
+// (pinned or registered host buffers): `bytes` from src to dst, 16 bytes a
+// thread while whole 16-byte chunks remain (both pointers 16-byte aligned),
+// then the tail byte by byte.  Launched with programmatic dependent launch
+// around the projection: it waits for the preceding kernel first (so it never
+// writes a buffer that kernel still reads) and only then lets the next one
+// start its set-up.
+__global__ void proj_copy_kernel(const uint8_t *src, uint8_t *dst, int64_t bytes) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const int64_t n16 = bytes / 16;
+    const uint4 *s16 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d16 = reinterpret_cast<uint4 *>(dst);
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        d16[i] = s16[i];
+    const int64_t tail = bytes - n16 * 16;
+    if (blockIdx.x == 0 && threadIdx.x < tail) dst[n16 * 16 + threadIdx.x] = src[n16 * 16 + threadIdx.x];
+}
+
 // K == 0: every sum is empty, so Y = act(bias or 0) + residual.
 __global__ void proj_fill_kernel(int64_t M, int64_t N, const uint16_t *bias, void *Y, int y_f32, int act,
                                  const void *residual) {

@@ -332,10 +332,12 @@ proj_status_t proj_run_host_packed(proj_handle_t h, const void *X_host, const vo
  * Same projection with HOST activations: copies X_host ([M,K] bf16) to a
  * device staging buffer, runs, and copies Y back to Y_host, all on `stream`.
  * W and bias stay device pointers (weights are resident, as after a
- * preparation step).  X_host / Y_host should be pinned for the copies to be
- * asynchronous; Y_host is valid once `stream` has been synchronised.  The
- * staging buffers are allocated by the first call on a handle (so that first
- * call is not capturable) and reused afterwards.
+ * preparation step).  Pinned or registered host buffers (16-byte aligned) are
+ * copied by small kernels chained to the projection by programmatic dependent
+ * launch; other host memory by cudaMemcpyAsync (asynchronous only when
+ * pinned).  Y_host is valid once `stream` has been synchronised.  The staging
+ * buffers are allocated by the first call on a handle (so that first call is
+ * not capturable) and reused afterwards.
  */
 proj_status_t proj_run_host(proj_handle_t h, const void *X_host, const void *W,
                             const void *bias, void *Y_host, void *stream);

@@ -384,3 +384,57 @@ def test_handles_with_different_rings_in_any_creation_order():
             w, inp, (proj, Y, _) = ws[i], inps[i], runs[i]
             r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
             gu.assert_within_tol(gu.y_to_f64(Y), r, w.name)
+
+
+@pytest.mark.parametrize("M,N,K,yd", [(16, 1024, 2048, "bf16"), (5, 1001, 520, "f32"), (3, 999, 256, "bf16")])
+def test_run_host_copy_paths(M, N, K, yd):
+    # Pinned host buffers go through the copy kernels (chained to the
+    # projection by programmatic dependent launch); pageable or unaligned
+    # ones through cudaMemcpyAsync.  Odd N leaves a Y tail that is not a
+    # whole 16-byte chunk.  Every path gives the device run's bits.
+    import torch
+    import dense_linear_projection_gb300 as dlp
+    w = synth.Workload("t", M, N, K, synth.W_NK, True, yd, 14)
+    inp = synth.make_inputs(w)
+    proj, Y, (X, W, b) = gu.run(w, inp)
+    torch.cuda.synchronize()
+    dt = torch.float32 if yd == "f32" else torch.bfloat16
+    iv = torch.int32 if yd == "f32" else torch.int16
+    xh = torch.from_numpy(inp["X"].view(np.int16)).view(torch.bfloat16)
+    s = torch.cuda.current_stream()
+    # Pinned X and Y; pageable X and Y; pinned but unaligned (offset by one element).
+    Xp, Yp = xh.pin_memory(), torch.empty((M, N), dtype=dt).pin_memory()
+    Xu_buf = torch.empty(M * K + 8, dtype=torch.bfloat16).pin_memory()
+    Yu_buf = torch.empty(M * N + 8, dtype=dt).pin_memory()
+    Xu, Yu = Xu_buf[1:1 + M * K].view(M, K), Yu_buf[1:1 + M * N].view(M, N)
+    Xu.copy_(xh)
+    cases = [("pinned", Xp, Yp), ("pageable", xh.clone(), torch.empty((M, N), dtype=dt)), ("unaligned", Xu, Yu)]
+    for name, Xh, Yh in cases:
+        Yh.zero_()
+        dlp.proj_run_host(proj.handle, Xh, W, b, Yh, s)
+        s.synchronize()
+        assert torch.equal(Yh.view(iv), Y.cpu().view(iv)), name
+    assert proj.status() == dlp.PROJ_OK
+
+
+def test_run_host_back_to_back_calls_keep_their_inputs():
+    # Eight host-buffer calls in a row on one stream, with no synchronisation
+    # between them: each call's X reaches the shared staging buffer only after
+    # the previous projection has read its own, and each Y leaves before the
+    # next projection overwrites the staging output.
+    import torch
+    import dense_linear_projection_gb300 as dlp
+    w = synth.Workload("t", 16, 2048, 4096, synth.W_NK, True, "bf16", 15)
+    inp = synth.make_inputs(w)
+    proj, _, (X, W, b) = gu.run(w, inp)
+    xs = [inp["X"], synth.normal_bf16(16, synth.STREAM_X, w.M * w.K, 1.0).reshape(w.M, w.K)]
+    Xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs]
+    Yh = [torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory() for _ in range(8)]
+    s = torch.cuda.current_stream()
+    for i in range(8):
+        dlp.proj_run_host(proj.handle, Xh[i % 2], W, b, Yh[i], s)
+    s.synchronize()
+    refs = [oracle.project(x, inp["W"], w.w_layout, inp["bias"]) for x in xs]
+    for i in range(8):
+        gu.assert_within_tol(gu.y_to_f64(Yh[i]), refs[i % 2], f"call {i}")
+    assert proj.status() == dlp.PROJ_OK
