@@ -41,8 +41,8 @@ int32_t token_tile_for(int64_t M) {
     return static_cast<int32_t>(bt < 16 ? 16 : bt);
 }
 
-int32_t stage_bytes_for(int32_t b_rows) {
-    return kBlockA * kBlockK * 2 + b_rows * kBlockK * 2;
+int32_t stage_bytes_for(int32_t a_rows, int32_t b_rows) {
+    return a_rows * kBlockK * 2 + b_rows * kBlockK * 2;
 }
 
 }  // namespace projgb
@@ -181,7 +181,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 }
             }
             const int32_t pb_rows = swap ? pbt : pbn;
-            const int32_t pstage = stage_bytes_for(pb_rows / 2);
+            const int32_t pstage = stage_bytes_for(kBlockA, pb_rows / 2);
             int32_t pstages = budget / pstage;
             if (pstages > kMaxStages) pstages = kMaxStages;
             const int64_t ptiles = ceil_div(M, pbt) * ceil_div(N, pbn);
@@ -215,7 +215,11 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     }
 
     const int32_t b_rows = swap ? bt : bn;
-    const int32_t stage = stage_bytes_for(b_rows);
+    // Half tiles stage only their 64 weight rows (the MMA's rows 64-127 read
+    // whatever follows them in shared memory, into accumulator rows nobody
+    // reads), so their stages are small and the ring deep.
+    const bool half = swap && bn < kBlockA;
+    const int32_t stage = stage_bytes_for(half ? bn : kBlockA, b_rows);
     int32_t stages = budget / stage;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return PROJ_ERR_UNSUPPORTED;
@@ -300,13 +304,14 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // the memory system busy; more only lengthens its queues (measured on
     // GB300: 8 stages of 18 KiB beat 12 for the 16-token decode shapes).  A
     // CTA with few k-blocks also pays the fill of a deep ring: at most a third
-    // of its k-blocks.  Data-parallel plans over several token tiles are
-    // tensor-bound and keep the whole ring.
+    // of its k-blocks (not for half tiles, whose small stages need the depth
+    // to keep as many weight bytes in flight).  Data-parallel plans over
+    // several token tiles are tensor-bound and keep the whole ring.
     const bool streaming = out->tiles_m == 1 || out->tiles_sk > 0;
     if (streaming) {
         int32_t want = kInflightTarget / stage;
         const int64_t units_per_cta = (out->tiles_dp * out->k_blocks + out->units_sk) / out->grid;
-        if (units_per_cta / 3 < want) want = static_cast<int32_t>(units_per_cta / 3);
+        if (!half && units_per_cta / 3 < want) want = static_cast<int32_t>(units_per_cta / 3);
         if (want < 2) want = 2;
         if (want < stages) stages = want;
     }

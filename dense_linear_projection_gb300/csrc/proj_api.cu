@@ -303,7 +303,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int st_force = std::atoi(e);
         if (st_force >= 2 && st_force < plan.stages && plan.kernel == PROJ_KERNEL_TC) {
             plan.stages = st_force;
-            plan.smem_bytes = st_force * stage_bytes_for(plan_cta_b_rows(plan)) +
+            plan.smem_bytes = st_force * stage_bytes_for(plan_a_rows(plan), plan_cta_b_rows(plan)) +
                               cluster_red_bytes(plan.cluster_split, plan_b_rows(plan)) + kSmemReserve;
         }
     }
@@ -588,7 +588,7 @@ proj_status_t copy_host(void *dst_dev, const void *src_dev, void *dst, const voi
     if (bytes == 0) return PROJ_OK;
     if (src_dev && dst_dev && aligned16(src_dev) && aligned16(dst_dev)) {
         const int64_t n16 = static_cast<int64_t>(bytes / 16);
-        const int64_t want = (n16 + 255) / 256;
+        const int64_t want = (n16 + 1023) / 1024;  // four chunks a thread
         cudaLaunchConfig_t cfg{};
         cudaLaunchAttribute attr[1];
         cfg.gridDim = dim3(static_cast<unsigned>(want < 1 ? 1 : (want < 2 * sm_count ? want : 2 * sm_count)));

@@ -146,9 +146,18 @@ __global__ void proj_copy_kernel(const uint8_t *src, uint8_t *dst, int64_t bytes
     const int64_t n16 = bytes / 16;
     const uint4 *s16 = reinterpret_cast<const uint4 *>(src);
     uint4 *d16 = reinterpret_cast<uint4 *>(dst);
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        d16[i] = s16[i];
+    // Four loads in flight per thread before their stores (the far side of
+    // the host link has a long round trip); each access stays coalesced.
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n16; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i + u * stride < n16) v[u] = s16[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (i + u * stride < n16) d16[i + u * stride] = v[u];
+    }
     const int64_t tail = bytes - n16 * 16;
     if (blockIdx.x == 0 && threadIdx.x < tail) dst[n16 * 16 + threadIdx.x] = src[n16 * 16 + threadIdx.x];
 }

@@ -18,7 +18,7 @@ constexpr int32_t kBlockA = 128;       // rows of the MMA's A operand (tcgen05 M
 constexpr int32_t kBlockK = 64;        // K per stage: 64 bf16 = one 128-byte swizzle row
 constexpr int32_t kMmaK = 16;          // K per tcgen05.mma (kind::f16)
 constexpr int32_t kMaxTokenTile = 256; // tcgen05 MMA N limit for cta_group::1
-constexpr int32_t kMaxStages = 12;
+constexpr int32_t kMaxStages = 16;
 constexpr int32_t kInflightTarget = 160 * 1024;  // stage bytes per SM when streaming W from HBM
 constexpr int32_t kMaxClusterSplit = 16;          // thread-block cluster size (16: non-portable)
 constexpr int32_t kClusterFillPct = 10;           // SMs a cluster split must keep busy (%)
@@ -88,9 +88,10 @@ struct PlanOptions {
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
                            proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t *dev,
                            const PlanOptions &opt, proj_plan_desc_t *out);
-// Shared-memory bytes of one pipeline stage: A (128 rows x 64 K) plus B
-// (b_rows x 64 K), bf16.  A CTA of a pair holds half of the B rows.
-int32_t stage_bytes_for(int32_t b_rows);
+// Shared-memory bytes of one pipeline stage: A (a_rows x 64 K: 128, or the 64
+// weight rows of a half tile) plus B (b_rows x 64 K), bf16.  A CTA of a pair
+// holds half of the B rows.
+int32_t stage_bytes_for(int32_t a_rows, int32_t b_rows);
 int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int w_layout,
                  int y_dtype, int has_bias, char *buf, size_t len);
 
@@ -115,8 +116,7 @@ struct KernelParams {
     int32_t cta_pair;      // 1: each tile on a cluster of 2 CTAs, one cta_group::2 MMA of 256 rows
     int32_t acc_bufs;      // accumulator buffers in tensor memory (2: epilogue overlaps the next tile)
     int32_t stages;
-    int32_t stage_bytes;   // shared memory of one stage (A region of 128 rows + B rows)
-    int32_t stage_tx;      // bytes one CTA's loads bring into a stage (A rows loaded + B rows)
+    int32_t stage_bytes;   // one stage: A rows + B rows, what one CTA's loads bring into it
     int32_t a_rows;        // A rows of a tile this CTA holds: 128, or 64 (half tiles: MMA rows 64-127 unused)
     int32_t red_bytes;     // cluster split: shared memory after the ring for peers' partial sums
     int32_t tmem_cols;
@@ -286,6 +286,11 @@ PROJ_HD int32_t plan_b_rows(const proj_plan_desc_t &plan) { return plan.swap_ab 
 PROJ_HD int32_t plan_cta_b_rows(const proj_plan_desc_t &plan) {
     return plan.cta_pair ? plan_b_rows(plan) / 2 : plan_b_rows(plan);
 }
+// A rows per CTA: the weight rows of a swapped tile (64 for half tiles, 128
+// of a pair's 256), else 128 token rows.
+PROJ_HD int32_t plan_a_rows(const proj_plan_desc_t &plan) {
+    return plan.swap_ab ? (plan.cta_pair ? plan.block_n / 2 : plan.block_n) : kBlockA;
+}
 
 inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.swap = plan.swap_ab;
@@ -305,11 +310,8 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.cluster_split = plan.cluster_split;
     if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;
     kp.stages = plan.stages;
-    kp.stage_bytes = stage_bytes_for(plan_cta_b_rows(plan));
-    // A rows per CTA: the weight rows of a swapped tile (64 for half tiles,
-    // 128 of a pair's 256), else 128 token rows.
-    kp.a_rows = plan.swap_ab ? (plan.cta_pair ? plan.block_n / 2 : plan.block_n) : kBlockA;
-    kp.stage_tx = (kp.a_rows + plan_cta_b_rows(plan)) * kBlockK * 2;
+    kp.a_rows = plan_a_rows(plan);
+    kp.stage_bytes = stage_bytes_for(kp.a_rows, plan_cta_b_rows(plan));
     kp.red_bytes = cluster_red_bytes(plan.cluster_split, kp.b_rows);
     kp.tmem_cols = plan.tmem_cols;
     kp.acc_bufs = plan.tmem_cols >= 2 * kp.b_rows ? 2 : 1;

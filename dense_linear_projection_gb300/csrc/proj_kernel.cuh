@@ -596,7 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const int32_t stages = p.stages;
-    const uint32_t a_bytes = kBlockA * kBlockK * 2;  // A region of a stage (16 KiB)
+    // A region of a stage: 128 rows (16 KiB), or the 64 weight rows of a
+    // half tile (8 KiB: the MMA's A rows 64-127 are then the bytes after
+    // them, shared memory the kernel owns, read into accumulator rows that
+    // are never used).
+    const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * kBlockK * 2;
     // Where W and X land in a stage: W is the A operand when swapped, else B.
     const uint32_t w_off = p.swap ? 0u : a_bytes;
     const uint32_t x_off = p.swap ? a_bytes : 0u;
@@ -675,9 +679,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = p.tiles_m == 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
             const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
             const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
-            // Bytes a stage's loads bring: less than the stage for half tiles
-            // (64 weight rows in the 128-row A region).
-            const uint32_t stage_tx = static_cast<uint32_t>(p.stage_tx);
             // CTA pairs: this CTA's halves of the tile's weight and token rows.
             const int32_t w_row_off = static_cast<int32_t>(pair_rank) * (p.block_n / 2);
             const int32_t x_row_off = static_cast<int32_t>(pair_rank) * (p.block_t / 2);
@@ -723,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tile_coords(p, s.tile, tm, tn);
                     for (int32_t kb = s.kb0; kb < s.kb1 && pre < pre_max; ++kb) {
                         const uint32_t full = smem_u32(&ctl->full[pre]);
-                        mbar_arrive_expect_tx(full, stage_tx);  // W + X bytes of the stage
+                        mbar_arrive_expect_tx(full, stage_bytes);  // W + X bytes of the stage
                         load_w(base_addr + static_cast<uint32_t>(pre) * stage_bytes + w_off, full, tn, kb);
                         ++pre;
                     }
@@ -762,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
                         }
                         // The leader expects both CTAs' bytes of the stage.
-                        if (leader) mbar_arrive_expect_tx(full, (kPair ? 2u : 1u) * stage_tx);
+                        if (leader) mbar_arrive_expect_tx(full, (kPair ? 2u : 1u) * stage_bytes);
                         dep_wait();
                         load_w(st_base + w_off, full, tn, kb);
                     }
