@@ -95,8 +95,13 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // tokens take the M side and the weight rows the N side, whose width (a
     // multiple of 16) is free: it is chosen so the tiles fill whole waves.
     const bool swap_fills = ceil_div(M, kMaxTokenTile) * ceil_div(N, kBlockA) >= sms;
-    const bool swap = force_block_n > 0 ? false
-                                        : (force_block_t > 0 || M < kBlockA || swap_fills);
+    // Token-major cluster split (option 2, at most 32 tokens): see the
+    // cluster rule below.
+    const bool tm_cluster = opt.tm_cluster == 2 && M <= 32 && force_block_t <= 0 && force_block_n <= 0 &&
+                            opt.max_cluster >= 2;
+    const bool swap = tm_cluster ? false
+                      : force_block_n > 0 ? false
+                                          : (force_block_t > 0 || M < kBlockA || swap_fills);
     int32_t bt, bn;
     if (swap) {
         bn = kBlockA;
@@ -117,7 +122,9 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         if (opt.half_tiles == 2 && bt <= 64) bn = kBlockA / 2;
     } else {
         bt = kBlockA;
-        if (force_block_n > 0) {
+        if (tm_cluster) {
+            bn = kMaxTokenTile;
+        } else if (force_block_n > 0) {
             bn = force_block_n;
         } else {
             // Per-SM time ~ waves x (block_n + a fixed share for the token
@@ -268,17 +275,33 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // 16.3 us for stream-K at its best grid.  S goes up to 16 (a non-portable
     // cluster size); the clusters must keep cluster_fill_pct (10) % of the SMs
     // busy.
+    //
+    // Token-major cluster split (at most 32 tokens): the same split over K,
+    // with the tokens as the MMA's A rows (zero beyond M) and 256 weight rows
+    // as its N side.  A CTA then streams 256 weight rows per MMA instruction
+    // instead of 128: measured on GB300 with 48 busy SMs, 70 GB/s per SM
+    // against 51 GB/s for 128 weight rows on either side.  Its partial sums
+    // are 32 token rows x 256 columns; rank c mod S adds 16-column chunk c.
+    auto red_for = [&](int32_t s_) {
+        return swap ? cluster_red_bytes(s_, b_rows) : cluster_red_bytes_tm(s_, bn);
+    };
     int32_t S = 0;
-    if (swap && opt.max_cluster >= 2 && 3 * tiles < sms && b_rows <= 64) {
+    if ((tm_cluster || (swap && b_rows <= 64)) && opt.max_cluster >= 2 && 3 * tiles < sms) {
         int64_t s_try = sms / tiles;
         if (s_try > opt.max_cluster) s_try = opt.max_cluster;
         if (s_try > out->k_blocks) s_try = out->k_blocks;
         if (s_try >= 2 && 100 * tiles * s_try >= int64_t(opt.cluster_fill_pct) * sms &&
-            budget - cluster_red_bytes(static_cast<int32_t>(s_try), b_rows) >= 2 * stage)
+            budget - red_for(static_cast<int32_t>(s_try)) >= 2 * stage)
             S = static_cast<int32_t>(s_try);
     }
+    if (tm_cluster && S < 2) {
+        // Not a cluster split after all: the ordinary plan.
+        PlanOptions plain = opt;
+        plain.tm_cluster = 0;
+        return plan_compute(M, N, K, w_layout, y_dtype, has_bias, dev, plain, out);
+    }
     // The peers' partial sums get their own shared memory after the ring.
-    const int32_t red_bytes = cluster_red_bytes(S, b_rows);
+    const int32_t red_bytes = red_for(S);
     if (stages * stage + red_bytes > budget) stages = (budget - red_bytes) / stage;
     const int64_t rem = tiles % grid;
     const int64_t waves = (tiles + grid - 1) / grid;
@@ -305,13 +328,14 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // GB300: 8 stages of 18 KiB beat 12 for the 16-token decode shapes).  A
     // CTA with few k-blocks also pays the fill of a deep ring: at most a third
     // of its k-blocks (not for half tiles, whose small stages need the depth
-    // to keep as many weight bytes in flight).  Data-parallel plans over
-    // several token tiles are tensor-bound and keep the whole ring.
+    // to keep as many weight bytes in flight, nor for token-major cluster
+    // splits, whose 48 KiB stages allow only three).  Data-parallel plans
+    // over several token tiles are tensor-bound and keep the whole ring.
     const bool streaming = out->tiles_m == 1 || out->tiles_sk > 0;
     if (streaming) {
         int32_t want = kInflightTarget / stage;
         const int64_t units_per_cta = (out->tiles_dp * out->k_blocks + out->units_sk) / out->grid;
-        if (!half && units_per_cta / 3 < want) want = static_cast<int32_t>(units_per_cta / 3);
+        if (!half && !tm_cluster && units_per_cta / 3 < want) want = static_cast<int32_t>(units_per_cta / 3);
         if (want < 2) want = 2;
         if (want < stages) stages = want;
     }

@@ -175,13 +175,12 @@ struct TcLaunch {
     }
 };
 
-// Plan for this device.  A cluster split is kept only if every tile's cluster
-// can be resident at once (GPCs hold whole clusters, so not every SM count
-// divides into clusters); otherwise the split size is lowered, down to the
+// A plan whose cluster split is kept only if every tile's cluster can be
+// resident at once (GPCs hold whole clusters, so not every SM count divides
+// into clusters); otherwise the split size is lowered, down to the
 // global-scratch split-K plans.  Needs the kernel's shared-memory limit set.
-proj_status_t plan_for_device(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
-                              proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t &dd,
-                              PlanOptions opt, proj_plan_desc_t *plan) {
+proj_status_t plan_fitted(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout, proj_dtype_t y_dtype,
+                          int has_bias, const proj_device_desc_t &dd, PlanOptions opt, proj_plan_desc_t *plan) {
     while (true) {
         proj_status_t st = plan_compute(M, N, K, w_layout, y_dtype, has_bias, &dd, opt, plan);
         if (st != PROJ_OK || plan->cluster_split < 2) return st;
@@ -194,6 +193,29 @@ proj_status_t plan_for_device(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_
         opt.max_cluster = plan->cluster_split - 1;
         if (opt.max_cluster < 2) opt.max_cluster = 0;
     }
+}
+
+// Plan for this device.  With PROJ_TM_CLUSTER=1, for at most 32 tokens, a
+// token-major cluster split (256 weight rows per MMA instruction) replaces a
+// swapped cluster split when, both fitted to the device, it keeps at least
+// 70 % as many SMs (each then streams about 1.4 times as fast).
+proj_status_t plan_for_device(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
+                              proj_dtype_t y_dtype, int has_bias, const proj_device_desc_t &dd,
+                              PlanOptions opt, proj_plan_desc_t *plan) {
+    const int32_t tm = opt.tm_cluster;
+    opt.tm_cluster = tm == 2 ? 2 : 0;
+    const proj_status_t st = plan_fitted(M, N, K, w_layout, y_dtype, has_bias, dd, opt, plan);
+    if (st != PROJ_OK || tm != 1 || opt.half_tiles == 2 || plan->kernel != PROJ_KERNEL_TC || !plan->swap_ab ||
+        plan->cluster_split < 2 || M > 32)
+        return st;
+    PlanOptions alt_opt = opt;
+    alt_opt.tm_cluster = 2;
+    proj_plan_desc_t alt;
+    if (plan_fitted(M, N, K, w_layout, y_dtype, has_bias, dd, alt_opt, &alt) == PROJ_OK &&
+        alt.kernel == PROJ_KERNEL_TC && !alt.swap_ab && alt.cluster_split >= 2 &&
+        10 * static_cast<int64_t>(alt.grid) >= 7 * static_cast<int64_t>(plan->grid))
+        *plan = alt;
+    return st;
 }
 
 // Y rows start on 16-byte boundaries: vector stores of 16 outputs are safe.
@@ -276,6 +298,10 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         if (c >= 0 && c <= 2) opt.cta_pair = c;
     }
     if (const char *e = std::getenv("PROJ_HALF_TILES")) opt.half_tiles = std::atoi(e) == 2 ? 2 : 0;
+    if (const char *e = std::getenv("PROJ_TM_CLUSTER")) {
+        const int c = std::atoi(e);
+        if (c >= 0 && c <= 2) opt.tm_cluster = c;
+    }
     // fp32 weights: the reduction runs over [H | L], twice the k-blocks of K.
     const int64_t kt = (K + kBlockK - 1) / kBlockK;
     const int64_t k_plan = hilo ? 2 * kt * kBlockK : K;
@@ -304,7 +330,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         if (st_force >= 2 && st_force < plan.stages && plan.kernel == PROJ_KERNEL_TC) {
             plan.stages = st_force;
             plan.smem_bytes = st_force * stage_bytes_for(plan_a_rows(plan), plan_cta_b_rows(plan)) +
-                              cluster_red_bytes(plan.cluster_split, plan_b_rows(plan)) + kSmemReserve;
+                              plan_red_bytes(plan) + kSmemReserve;
         }
     }
     if (const char *e = std::getenv("PROJ_FORCE_RASTER_GROUP")) {  // tuning only

@@ -83,6 +83,16 @@ struct PlanOptions {
     // 2048-row decode weight ran 15.9 us on 32 half tiles in clusters of 4
     // (128 SMs) against 12.6 us on 16 full tiles in clusters of 6 (96 SMs).
     int32_t half_tiles = 0;
+    // Token-major cluster split (PROJ_TM_CLUSTER) for at most 32 tokens: the
+    // tokens on the MMA's M side (128 rows, the rest zero) and 256 weight rows
+    // on its N side, which streams more weight bytes per MMA instruction than
+    // 128 weight rows on the M side.  0 never (the default); 1 where
+    // proj_create finds the swapped plan a cluster split too and this one
+    // keeps at least 70 % of its SMs; 2 wherever it applies.  Off by default:
+    // on GB300 the 2048-row decode weight streamed in 5.2 us instead of 7.1 us
+    // per CTA, but its 8 clusters of 12 CTAs started about 5 us later after
+    // the preceding call than 16 clusters of 6 (15.9 us per call vs 12.7).
+    int32_t tm_cluster = 0;
 };
 // The planner behind proj_plan_compute (which uses the default options).
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
@@ -279,6 +289,13 @@ PROJ_HD int32_t cluster_quarters_per_reducer(int32_t S) { return S <= 4 ? (4 + S
 PROJ_HD int32_t cluster_red_bytes(int32_t S, int32_t b_rows) {
     return S > 1 ? cluster_quarters_per_reducer(S) * (S - 1) * 32 * b_rows * 4 : 0;
 }
+// Token-major cluster split (at most 32 tokens, all in row quarter 0): rank
+// c mod S adds 16-column chunk c of the block_n columns, receiving S - 1
+// partial chunks of 32 rows x 16 fp32 (2 KiB) for each chunk it owns.
+PROJ_HD int32_t cluster_red_bytes_tm(int32_t S, int32_t block_n) {
+    const int32_t chunks = block_n / 16;
+    return S > 1 ? ((chunks + S - 1) / S) * (S - 1) * 2048 : 0;
+}
 
 // B rows of the MMA (its N), and the B rows one CTA holds per stage (half of
 // them in a CTA pair).
@@ -290,6 +307,11 @@ PROJ_HD int32_t plan_cta_b_rows(const proj_plan_desc_t &plan) {
 // of a pair's 256), else 128 token rows.
 PROJ_HD int32_t plan_a_rows(const proj_plan_desc_t &plan) {
     return plan.swap_ab ? (plan.cta_pair ? plan.block_n / 2 : plan.block_n) : kBlockA;
+}
+// Shared memory after the ring for a cluster split's incoming partial sums.
+PROJ_HD int32_t plan_red_bytes(const proj_plan_desc_t &plan) {
+    return plan.swap_ab ? cluster_red_bytes(plan.cluster_split, plan_b_rows(plan))
+                        : cluster_red_bytes_tm(plan.cluster_split, plan.block_n);
 }
 
 inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
@@ -312,7 +334,7 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.stages = plan.stages;
     kp.a_rows = plan_a_rows(plan);
     kp.stage_bytes = stage_bytes_for(kp.a_rows, plan_cta_b_rows(plan));
-    kp.red_bytes = cluster_red_bytes(plan.cluster_split, kp.b_rows);
+    kp.red_bytes = plan_red_bytes(plan);
     kp.tmem_cols = plan.tmem_cols;
     kp.acc_bufs = plan.tmem_cols >= 2 * kp.b_rows ? 2 : 1;
 }

@@ -1228,6 +1228,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_chunk(ch, v);
                 }
                 release_accumulator();
+            } else if (clustered && !p.swap) {
+                // Token-major cluster split (at most 32 tokens, so only row
+                // quarter 0 holds results).  The S ranks hold the tile's
+                // partial sums over consecutive K ranges.  Rank c mod S adds
+                // 16-column chunk c: every other rank stores its partial
+                // chunk (32 rows x 16 fp32, [float4][lane]) into the owner's
+                // shared memory, then every lane arrives on each other
+                // rank's barrier (releasing its stores).  The owner adds all
+                // ranks in rank (= K) order, so every run gives the same bits.
+                if (q == 0) {
+                    const uint32_t S = static_cast<uint32_t>(p.cluster_split);
+                    const uint32_t rank = static_cast<uint32_t>(cta) % S;  // = %cluster_ctarank
+                    const int32_t nch = p.block_n / 16;
+                    const uint32_t lane_off16 = static_cast<uint32_t>(lane) * 16u;
+                    // Slot (o, j): the owner's o-th chunk from contributor j.
+                    auto slot_addr = [&](uint32_t o, uint32_t j) {
+                        return red_addr + (o * (S - 1u) + j) * 2048u + lane_off16;
+                    };
+                    if (stamp_split) trace_stamp(p, kTraceSplitPartial);
+                    for (int32_t c = 0; c < nch; ++c) {
+                        const uint32_t owner = static_cast<uint32_t>(c) % S;
+                        if (owner == rank) continue;
+                        const uint32_t dst =
+                            map_to_rank(slot_addr(static_cast<uint32_t>(c) / S, rank < owner ? rank : rank - 1u), owner);
+                        float v[16];
+                        tmem_load16(tbase + c * 16, v);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            st_cluster_f4(dst + static_cast<uint32_t>(i) * 512u,
+                                          make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+                    }
+                    for (uint32_t r2 = 0; r2 < S; ++r2)
+                        if (r2 != rank) mbar_arrive_remote(map_to_rank(smem_u32(&ctl->ready[0]), r2));
+                    if (wait_phase<true>(smem_u32(&ctl->ready[0]), 0u, abort_flag, p.status, kErrWaitEpilogue,
+                                         p.wait_limit_ns)) {
+                        if (stamp_split) trace_stamp(p, kTraceSplitReady);
+                        for (int32_t c = static_cast<int32_t>(rank); c < nch; c += static_cast<int32_t>(S)) {
+                            if (c * 16 >= ccount) break;  // past N: nothing to store
+                            const uint32_t o = static_cast<uint32_t>(c) / S;
+                            float own[16], acc[16];
+                            tmem_load16(tbase + c * 16, own);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                            for (uint32_t rk = 0; rk < S; ++rk) {
+                                if (rk == rank) {
+#pragma unroll
+                                    for (int i = 0; i < 16; ++i) acc[i] += own[i];
+                                    continue;
+                                }
+                                const uint32_t src = slot_addr(o, rk < rank ? rk : rk - 1u);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float4 w4 = ld_shared_f4(src + static_cast<uint32_t>(i) * 512u);
+                                    acc[4 * i] += w4.x;
+                                    acc[4 * i + 1] += w4.y;
+                                    acc[4 * i + 2] += w4.z;
+                                    acc[4 * i + 3] += w4.w;
+                                }
+                            }
+                            store_chunk(c, acc);
+                        }
+                        if (stamp_split) trace_stamp(p, kTraceSplitStored);
+                    }
+                }
+                release_accumulator();
             } else if (clustered) {
                 // Cluster split: the S CTAs of this cluster hold the tile's
                 // partial sums over consecutive K ranges (rank order = K

@@ -234,6 +234,8 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
  *   PROJ_CLUSTER_FILL_PCT=f  SMs (%) a cluster split must keep busy
  *   PROJ_CTA_PAIR=0|2        CTA pairs off, or on wherever the tile allows them
  *   PROJ_HALF_TILES=2        swapped tiles of 64 weight rows (at most 64 tokens)
+ *   PROJ_TM_CLUSTER=1|2      token-major cluster splits for at most 32 tokens (1: where they
+ *                            keep 70 % of a swapped cluster split's SMs; 2: wherever they apply)
  *   PROJ_FORCE_STAGES=k      fewer pipeline stages than planned
  *   PROJ_FORCE_GRID=g        fewer CTAs for an all-split plan
  *   PROJ_FORCE_WHOLE_TILES=1 no split tiles

@@ -18,6 +18,13 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(autouse=True)
+def _swapped_clusters_only(monkeypatch):
+    # These cases are about the swapped cluster split; the token-major one
+    # (which proj_create may prefer for at most 32 tokens) has its own tests.
+    monkeypatch.setenv("PROJ_TM_CLUSTER", "0")
+
 # (M, N, K, layout, bias, y_dtype, S the planner picks on 152 SMs)
 CLUSTER_SHAPES = [
     (16, 2048, 8192, synth.W_NK, False, "f32", 9),   # 16 tiles x 9 (x 6 where 16 clusters of 9 do not fit)

@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
     (16, 2048, 8192, synth.W_NK, False, "f32"),   # 16 tiles split over clusters
     (16, 28672, 1024, synth.W_NK, True, "bf16"),  # 224 tiles: split-K through the scratch
     (3, 520, 1032, synth.W_KN, True, "bf16"),     # [K,N] weights, ragged edges
-    (256, 19456, 256, synth.W_NK, False, "bf16"), # 152 whole tiles, one wave: no split scratch
+    (256, 19456, 256, synth.W_NK, False, "bf16"), # 76 whole tiles on CTA pairs, one wave: no split scratch
 ])
 def test_noalloc_matches_proj_run_twice(M, N, K, layout, bias, yd):
     import torch
