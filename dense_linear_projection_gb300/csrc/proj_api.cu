@@ -562,7 +562,8 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
                         ? h->prefetch_stages
                         : 0;
     TcLaunch l(plan, s, h->overlap != PROJ_OVERLAP_NONE);
-    const bool fused = kp.act != 0 || kp.residual != nullptr;
+    // The fused instance also carries the token-major cluster reduction.
+    const bool fused = kp.act != 0 || kp.residual != nullptr || (plan.cluster_split > 1 && !plan.swap_ab);
     const CUtensorMap &map_w = packed ? h->map_wp : h->map_w;
     if (launch_tc(plan, l, fused, kp, map_w, h->map_x) != cudaSuccess) {
         cudaGetLastError();
@@ -897,7 +898,7 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
     kp.trace = nullptr;
     TcLaunch l(plan, s, false);
-    if (launch_tc(plan, l, false, kp, map_w, map_x) != cudaSuccess) {
+    if (launch_tc(plan, l, plan.cluster_split > 1 && !plan.swap_ab, kp, map_w, map_x) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }

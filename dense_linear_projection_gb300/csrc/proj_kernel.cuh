@@ -1228,9 +1228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_chunk(ch, v);
                 }
                 release_accumulator();
-            } else if (clustered && !p.swap) {
+            } else if (kFused && clustered && !p.swap) {
                 // Token-major cluster split (at most 32 tokens, so only row
-                // quarter 0 holds results).  The S ranks hold the tile's
+                // quarter 0 holds results; built into the fused instance
+                // only, which every such plan runs on, to keep the lean
+                // instance's epilogue code small).  The S ranks hold the tile's
                 // partial sums over consecutive K ranges.  Rank c mod S adds
                 // 16-column chunk c: every other rank stores its partial
                 // chunk (32 rows x 16 fp32, [float4][lane]) into the owner's
