@@ -6,9 +6,9 @@ Planner-chosen pairs (swapped 256-token tiles) and pairs forced on other
 tiles (PROJ_CTA_PAIR=2): token-major tiles (the QKV shape among them),
 narrower token tiles, several tiles per pair with both accumulator buffers in
 turn, ragged M, N and K, [K,N] weights loaded as stored and packed, fp32
-output, the fused epilogue and SwiGLU.  Each is compared with the fp64 oracle, must rerun bit for bit and
-must leave the device status clear (both CTAs of a pair see the same tensor
-memory).
+output, the fused epilogue and SwiGLU.  Each is compared with the fp64
+oracle, must rerun bit for bit and must leave the device status clear (both
+CTAs of a pair see the same tensor memory).
 """
 import numpy as np
 import pytest
