@@ -3,15 +3,52 @@
 GELU is taken from its definition x·Φ(x) (the pages fuse "GELU" into the FFN
 projection's epilogue without writing it out).  It is pinned against the
 standard normal CDF of an independent library routine (scipy.special.ndtr),
-the identity GELU(x) − GELU(−x) = x (from Φ(x) + Φ(−x) = 1), and its limits.
+against the Maclaurin series of erf summed here term by term, the identity
+GELU(x) − GELU(−x) = x (from Φ(x) + Φ(−x) = 1), and its limits.  SiLU is
+pinned against scipy's logistic function and against the tanh form of the
+logistic, σ(x) = (1 + tanh(x/2)) / 2.  scipy is required: a missing scipy
+fails these tests rather than skipping them.
 """
+import math
+
 import numpy as np
-import pytest
+import scipy.special as scipy_special
 
 import oracle
 import synth
 
-scipy_special = pytest.importorskip("scipy.special")
+
+def erf_series(z: float) -> float:
+    """erf(z) = 2/√π · Σ (−1)^n z^(2n+1) / (n! (2n+1)), summed until the terms
+    vanish (|z| ≤ 3 keeps the cancellation below 1e-13)."""
+    t, total, n = z, z, 0
+    while True:
+        n += 1
+        t *= -z * z / n
+        term = t / (2 * n + 1)
+        total += term
+        if abs(term) < 1e-18:
+            return 2.0 / math.sqrt(math.pi) * total
+
+
+def test_gelu_against_the_erf_series():
+    # For x < 0, 1 + erf(x/√2) cancels: about 1e-14 absolute error at most
+    # over this range, hence the absolute tolerance.
+    xs = np.linspace(-4.0, 4.0, 161)
+    want = np.array([0.5 * x * (1.0 + erf_series(x / math.sqrt(2.0))) for x in xs])
+    assert np.allclose(oracle.gelu(xs), want, rtol=1e-12, atol=1e-13)
+    # The series itself against two printed values: erf(1) = 0.8427007929497149,
+    # erf(0.5) = 0.5204998778130465.
+    assert abs(erf_series(1.0) - 0.8427007929497149) < 1e-15
+    assert abs(erf_series(0.5) - 0.5204998778130465) < 1e-15
+
+
+def test_silu_against_the_tanh_form():
+    # 1 + tanh(x/2) cancels for x << 0: the range stops at −8, where the
+    # relative error of the tanh form stays near 1e-13.
+    xs = np.linspace(-8.0, 30.0, 381)
+    want = np.array([x * 0.5 * (1.0 + math.tanh(x / 2.0)) for x in xs])
+    assert np.allclose(oracle.silu(xs), want, rtol=1e-11, atol=1e-15)
 
 
 def test_gelu_definition_against_normal_cdf():
