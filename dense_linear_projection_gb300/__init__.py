@@ -28,6 +28,7 @@ __all__ = [
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "TRACE_FIELDS",
     "PROJ_OVERLAP_NONE", "PROJ_OVERLAP_PROLOGUE", "PROJ_OVERLAP_WEIGHTS", "proj_run_noalloc",
+    "proj_noalloc_device_status", "proj_noalloc_selftest_wait_timeout",
     "proj_packed_weight_bytes", "proj_pack_weights", "proj_run_packed", "proj_run_host_packed",
     "proj_set_activation", "proj_run_fused", "PROJ_ACT_NONE", "PROJ_ACT_GELU", "PROJ_ACT_SWIGLU",
     "Projection",
@@ -46,7 +47,8 @@ EXPORTED_SYMBOLS = (
     "proj_get_plan", "proj_plan_info", "proj_destroy", "proj_status_string",
     "proj_selftest_wait_timeout", "proj_set_trace", "proj_set_overlap", "proj_run_noalloc",
     "proj_packed_weight_bytes", "proj_pack_weights", "proj_run_packed", "proj_run_host_packed",
-    "proj_set_activation", "proj_run_fused",
+    "proj_set_activation", "proj_run_fused", "proj_noalloc_device_status",
+    "proj_noalloc_selftest_wait_timeout",
 )
 
 
@@ -119,6 +121,8 @@ def lib() -> ctypes.CDLL:
     L.proj_set_trace.argtypes = [vp, vp, ctypes.c_size_t]
     L.proj_set_overlap.argtypes = [vp, i32]
     L.proj_run_noalloc.argtypes = [i64, i64, i64, i32, i32, vp, vp, vp, vp, vp]
+    L.proj_noalloc_device_status.argtypes = [vp]
+    L.proj_noalloc_selftest_wait_timeout.argtypes = [i64, vp]
     L.proj_packed_weight_bytes.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
     L.proj_pack_weights.argtypes = [vp, vp, vp, vp]
     L.proj_run_packed.argtypes = [vp, vp, vp, vp, vp, vp]
@@ -219,10 +223,24 @@ def proj_run_noalloc(M: int, N: int, K: int, w_layout: int, y_dtype: int, X, W, 
     """proj_run without a handle or any allocation (fixed 8 MiB device scratch).
 
     For callers that cannot allocate device memory.  The first call on a device
-    looks up the scratch address; calls that overlap on the GPU race.
+    looks up the scratch address; calls that overlap on the GPU race.  A device
+    wait that gave up is reported later, by proj_noalloc_device_status.
     """
     _check(lib().proj_run_noalloc(M, N, K, w_layout, y_dtype, _ptr(X), _ptr(W), _ptr(bias),
                                   _ptr(Y), _stream(stream)), "proj_run_noalloc")
+
+
+def proj_noalloc_device_status(stream=None) -> int:
+    """Raw status of the allocation-free path's status word (read and
+    cleared; synchronises the stream); does not raise."""
+    return int(lib().proj_noalloc_device_status(_stream(stream)))
+
+
+def proj_noalloc_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Queue a bounded wait that gives up and records a timeout in the
+    allocation-free path's status word."""
+    _check(lib().proj_noalloc_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "proj_noalloc_selftest_wait_timeout")
 
 
 def proj_packed_weight_bytes(h: int) -> int:

@@ -226,7 +226,16 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // whatever follows them in shared memory, into accumulator rows nobody
     // reads), so their stages are small and the ring deep.
     const bool half = swap && bn < kBlockA;
-    const int32_t stage = stage_bytes_for(half ? bn : kBlockA, b_rows);
+    // Two k-blocks a stage for the weight-streaming swapped plans (at most 64
+    // tokens): one TMA op brings both k-blocks of the weight tile and one the
+    // activations'.  On GB300 a CTA's TMA loads are paced per operation, not
+    // per byte: measured with the loads alone, one 16 KiB op and one 2 KiB op
+    // a stage streamed 61 GB/s of weights per SM, one 32 KiB and one 4 KiB
+    // op 122 GB/s, so about 64 SMs instead of 110 keep HBM busy.  The
+    // activations' 3-D tensor map needs K to be a multiple of 64.
+    const int32_t kpb = (swap && bt <= 64 && K % kBlockK == 0 && opt.kpb != 1) ? 2 : 1;
+    out->block_k = kpb * kBlockK;
+    const int32_t stage = kpb * stage_bytes_for(half ? bn : kBlockA, b_rows);
     int32_t stages = budget / stage;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return PROJ_ERR_UNSUPPORTED;
@@ -249,7 +258,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         if (g < 1) g = 1;
         out->raster_group = static_cast<int32_t>(out->tiles_m < g ? out->tiles_m : g);
     }
-    out->k_blocks = ceil_div(K, kBlockK);
+    out->k_blocks = ceil_div(K, out->block_k);
     const int64_t tiles = out->tiles_m * out->tiles_n;
     const int64_t units = tiles * out->k_blocks;
     const int64_t grid = units < sms ? units : sms;
@@ -286,7 +295,10 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         return swap ? cluster_red_bytes(s_, b_rows) : cluster_red_bytes_tm(s_, bn);
     };
     int32_t S = 0;
-    if ((tm_cluster || (swap && b_rows <= 64)) && opt.max_cluster >= 2 && 3 * tiles < sms) {
+    if (opt.force_cluster >= 2 && swap && b_rows <= 64 && int64_t(opt.force_cluster) * tiles <= sms &&
+        opt.force_cluster <= out->k_blocks && budget - red_for(opt.force_cluster) >= 2 * stage) {
+        S = opt.force_cluster;
+    } else if ((tm_cluster || (swap && b_rows <= 64)) && opt.max_cluster >= 2 && 3 * tiles < sms) {
         int64_t s_try = sms / tiles;
         if (s_try > opt.max_cluster) s_try = opt.max_cluster;
         if (s_try > out->k_blocks) s_try = out->k_blocks;
@@ -334,7 +346,8 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     const bool streaming = out->tiles_m == 1 || out->tiles_sk > 0;
     if (streaming) {
         int32_t want = kInflightTarget / stage;
-        const int64_t units_per_cta = (out->tiles_dp * out->k_blocks + out->units_sk) / out->grid;
+        // (Counted in 64-wide k-blocks: a stage of two counts twice.)
+        const int64_t units_per_cta = kpb * (out->tiles_dp * out->k_blocks + out->units_sk) / out->grid;
         if (!half && !tm_cluster && units_per_cta / 3 < want) want = static_cast<int32_t>(units_per_cta / 3);
         if (want < 2) want = 2;
         if (want < stages) stages = want;

@@ -41,6 +41,7 @@ struct proj_plan_s {
     const void *map_w_ptr = nullptr;
     const void *map_wp_ptr = nullptr;  // packed weights
     int32_t map_x_box = 0, map_w_box = 0;
+    int32_t map_x_kpb = 0, map_x_3d = 0;  // k-blocks per stage the X map was built for; 3-D or not
     CUtensorMap map_x;  // CUtensorMap carries its own 64-byte alignment
     CUtensorMap map_w;
     CUtensorMap map_wp;
@@ -64,6 +65,37 @@ constexpr int64_t kDefaultWaitLimitNs = 1000000000LL;  // 1 s
 
 cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
 
+// Host-side fault injection for tests (PROJ_FAULT, read once per process): a
+// comma-separated list of "alloc" (every device allocation of the library
+// fails as out of memory), "encode" (every tensor-map encoding fails) and
+// "launch" (every kernel launch fails before it is queued).  The failure is
+// made on the host: nothing faulty reaches the device.
+constexpr int kFaultAlloc = 1, kFaultEncode = 2, kFaultLaunch = 4;
+
+int fault_mask() {
+    static const int mask = [] {
+        int m = 0;
+        if (const char *e = std::getenv("PROJ_FAULT")) {
+            if (std::strstr(e, "alloc")) m |= kFaultAlloc;
+            if (std::strstr(e, "encode")) m |= kFaultEncode;
+            if (std::strstr(e, "launch")) m |= kFaultLaunch;
+        }
+        return m;
+    }();
+    return mask;
+}
+
+bool launch_faulted() { return (fault_mask() & kFaultLaunch) != 0; }
+
+// Every device allocation of the library goes through here.
+cudaError_t dev_malloc(void **p, size_t bytes) {
+    if (fault_mask() & kFaultAlloc) {
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+    }
+    return cudaMalloc(p, bytes);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static bool tried = false;
@@ -84,6 +116,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // out-of-range elements read as zero.
 bool encode_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_bytes,
                uint32_t box_inner, uint32_t box_outer) {
+    if (fault_mask() & kFaultEncode) return false;
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -93,6 +126,53 @@ bool encode_2d(CUtensorMap *map, const void *ptr, uint64_t inner, uint64_t outer
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor map: dims {64, d1, d2} with byte strides s1, s2 for the
+// outer two, box {64, b1, b2}, 128-byte swizzle, zero fill outside.
+bool encode_3d(CUtensorMap *map, const void *ptr, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
+               uint32_t b1, uint32_t b2) {
+    if (fault_mask() & kFaultEncode) return false;
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {64, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {64, b1, b2};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// X's tensor map for a plan: with two k-blocks a stage (K a multiple of 64),
+// a 3-D view {64 K, M rows, K/64 k-blocks} whose box brings a stage's
+// k-blocks in one op (*x_3d = 1); otherwise 2-D boxes of one k-block.
+bool encode_x(CUtensorMap *map, const void *X, int64_t M, int64_t K, const proj_plan_desc_t &plan, int32_t *x_3d) {
+    const int32_t kpb = plan_kpb(plan);
+    const uint32_t rows = static_cast<uint32_t>(plan.cta_pair ? plan.block_t / 2 : plan.block_t);
+    if (kpb > 1 && K % kBlockK == 0 &&
+        encode_3d(map, X, static_cast<uint64_t>(M), static_cast<uint64_t>(K / kBlockK), static_cast<uint64_t>(K) * 2,
+                  128, rows, static_cast<uint32_t>(kpb))) {
+        *x_3d = 1;
+        return true;
+    }
+    *x_3d = 0;
+    return encode_2d(map, X, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint64_t>(K) * 2,
+                     kBlockK, rows);
+}
+
+// The packed weights' tensor map: planes of block_n rows x 64 K, one per
+// (tile, k-block), tiles_n x (k_blocks x kpb) of them; box {64, the rows
+// this CTA holds, kpb planes}.  With one k-block a stage, the same memory as
+// a 2-D map of 64-wide rows.
+bool encode_packed(CUtensorMap *map, const void *Wp, const proj_plan_desc_t &plan) {
+    const uint32_t rows = static_cast<uint32_t>(plan.cta_pair ? plan.block_n / 2 : plan.block_n);
+    if (plan_kpb(plan) == 1)  // one k-block a stage: a 2-D map of 64-wide rows
+        return encode_2d(map, Wp, 64, static_cast<uint64_t>(plan.tiles_n * plan.k_blocks * plan.block_n), 128,
+                         kBlockK, rows);
+    return encode_3d(map, Wp, static_cast<uint64_t>(plan.block_n),
+                     static_cast<uint64_t>(plan.tiles_n * plan_packed_kblocks(plan)), 128,
+                     static_cast<uint64_t>(plan.block_n) * 128, rows, static_cast<uint32_t>(plan_kpb(plan)));
 }
 
 uint32_t make_idesc(int mma_m, int mma_n, bool a_mn_major, bool b_mn_major) {
@@ -191,6 +271,7 @@ proj_status_t plan_fitted(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layo
             return PROJ_OK;
         cudaGetLastError();
         opt.max_cluster = plan->cluster_split - 1;
+        opt.force_cluster = 0;  // a forced size that does not fit falls back to the rule
         if (opt.max_cluster < 2) opt.max_cluster = 0;
     }
 }
@@ -230,6 +311,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // without the fused epilogue.
 cudaError_t launch_tc(const proj_plan_desc_t &plan, const TcLaunch &l, bool fused, const KernelParams &kp,
                       const CUtensorMap &map_w, const CUtensorMap &map_x) {
+    if (launch_faulted()) return cudaErrorLaunchFailure;
     if (plan.cta_pair)
         return fused ? tc_launch_pair_fused(&l.cfg, kp, map_w, map_x) : tc_launch_pair(&l.cfg, kp, map_w, map_x);
     return fused ? tc_launch_fused(&l.cfg, kp, map_w, map_x) : tc_launch_lean(&l.cfg, kp, map_w, map_x);
@@ -302,9 +384,19 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int c = std::atoi(e);
         if (c >= 0 && c <= 2) opt.tm_cluster = c;
     }
+    if (const char *e = std::getenv("PROJ_FORCE_CLUSTER")) {
+        const int c = std::atoi(e);
+        if (c >= 2 && c <= kMaxClusterSplit) opt.force_cluster = c;
+    }
     // fp32 weights: the reduction runs over [H | L], twice the k-blocks of K.
+    // A stage must not straddle the halves (its X k-blocks are contiguous):
+    // with an odd number of k-blocks in K, one k-block a stage.
     const int64_t kt = (K + kBlockK - 1) / kBlockK;
     const int64_t k_plan = hilo ? 2 * kt * kBlockK : K;
+    if (hilo && kt % 2 != 0) opt.kpb = 1;
+    if (const char *e = std::getenv("PROJ_KPB")) {  // tuning only: 1 = one k-block a stage
+        if (std::atoi(e) == 1) opt.kpb = 1;
+    }
     proj_status_t st = plan_for_device(M, N, k_plan, w_layout, y_dtype, has_bias, dd, opt, &plan);
     if (st != PROJ_OK) return st;
     if (const char *e = std::getenv("PROJ_FORCE_GRID")) {  // tuning only: fewer CTAs, all-split plans
@@ -329,7 +421,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int st_force = std::atoi(e);
         if (st_force >= 2 && st_force < plan.stages && plan.kernel == PROJ_KERNEL_TC) {
             plan.stages = st_force;
-            plan.smem_bytes = st_force * stage_bytes_for(plan_a_rows(plan), plan_cta_b_rows(plan)) +
+            plan.smem_bytes = st_force * plan_kpb(plan) * stage_bytes_for(plan_a_rows(plan), plan_cta_b_rows(plan)) +
                               plan_red_bytes(plan) + kSmemReserve;
         }
     }
@@ -374,7 +466,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         int64_t scratch_bytes = plan.scratch_bytes;
         if (h->has_plan_stored && h->plan_stored.scratch_bytes > scratch_bytes)
             scratch_bytes = h->plan_stored.scratch_bytes;
-        if (cudaMalloc(&h->scratch, static_cast<size_t>(scratch_bytes)) != cudaSuccess) {
+        if (dev_malloc(&h->scratch, static_cast<size_t>(scratch_bytes)) != cudaSuccess) {
             cudaGetLastError();
             delete h;
             return PROJ_ERR_OUT_OF_MEMORY;
@@ -423,7 +515,7 @@ namespace {
 // Rows of the packed weight layout (see proj_pack_weights), or -1 if they do
 // not fit the 31-bit TMA coordinates.
 int64_t packed_rows(const proj_plan_desc_t &plan) {
-    const int64_t rows = plan.tiles_n * plan.k_blocks * plan.block_n;
+    const int64_t rows = plan.tiles_n * plan_packed_kblocks(plan) * plan.block_n;
     return rows < (int64_t(1) << 31) ? rows : -1;
 }
 
@@ -465,14 +557,15 @@ proj_status_t proj_pack_weights(proj_handle_t h, const void *W, void *W_packed, 
     const int64_t chunks = rows * 8;  // 16-byte chunks
     const int64_t want = (chunks + 255) / 256;
     const int blocks = static_cast<int>(want < int64_t(h->sm_count) * 16 ? want : int64_t(h->sm_count) * 16);
+    if (launch_faulted()) return PROJ_ERR_CUDA;
     if (h->hilo)
         dev::proj_pack_hilo_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
             static_cast<const float *>(W), static_cast<uint16_t *>(W_packed), h->N, h->K,
-            h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, h->kt, chunks);
+            h->w_layout == PROJ_W_KN, plan.block_n, plan_packed_kblocks(plan), h->kt, chunks);
     else
         dev::proj_pack_kernel<<<blocks, 256, 0, as_stream(stream)>>>(
             static_cast<const uint16_t *>(W), static_cast<uint16_t *>(W_packed), h->N, h->K,
-            h->w_layout == PROJ_W_KN, plan.block_n, plan.k_blocks, chunks,
+            h->w_layout == PROJ_W_KN, plan.block_n, plan_packed_kblocks(plan), chunks,
             h->act == PROJ_ACT_SWIGLU ? (plan.swap_ab ? 1 : 2) : 0);
     return check_launch();
 }
@@ -499,6 +592,7 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     const bool swiglu = h->act == PROJ_ACT_SWIGLU;
     if (plan.kernel == PROJ_KERNEL_FILL) {
         // K = 0: every sum is empty.  SwiGLU of zeros is zero (no bias).
+        if (launch_faulted()) return PROJ_ERR_CUDA;
         dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(
             h->M, swiglu ? h->N / 2 : h->N, static_cast<const uint16_t *>(bias), Y, h->y_dtype == PROJ_F32,
             swiglu ? 0 : h->act, residual);
@@ -509,19 +603,19 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
 
     if (!X || !W) return PROJ_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W)) return PROJ_ERR_MISALIGNED;
-    if (X != h->map_x_ptr || x_box_rows(plan) != h->map_x_box) {
-        if (!encode_2d(&h->map_x, X, h->K, h->M, h->K * 2, kBlockK, x_box_rows(plan))) {
+    if (X != h->map_x_ptr || x_box_rows(plan) != h->map_x_box || plan_kpb(plan) != h->map_x_kpb) {
+        if (!encode_x(&h->map_x, X, h->M, h->K, plan, &h->map_x_3d)) {
             h->map_x_ptr = nullptr;
             return PROJ_ERR_CUDA;
         }
         h->map_x_ptr = X;
         h->map_x_box = x_box_rows(plan);
+        h->map_x_kpb = plan_kpb(plan);
     }
     if (packed) {
         if (W != h->map_wp_ptr) {  // packed runs always use h->plan: one box size
-            const int64_t rows = packed_rows(plan);
-            if (rows < 0) return PROJ_ERR_UNSUPPORTED;
-            if (!encode_2d(&h->map_wp, W, 64, static_cast<uint64_t>(rows), 128, kBlockK, w_box_rows(plan))) {
+            if (packed_rows(plan) < 0) return PROJ_ERR_UNSUPPORTED;
+            if (!encode_packed(&h->map_wp, W, plan)) {
                 h->map_wp_ptr = nullptr;
                 return PROJ_ERR_CUDA;
             }
@@ -539,6 +633,7 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
         h->map_w_box = w_box_rows(plan);
     }
     KernelParams kp = stored ? h->params_stored : h->params;
+    kp.x_3d = h->map_x_3d;
     if (packed) {
         // Packed weights are K-major blocks whatever the stored layout.
         kp.w_packed = 1;
@@ -625,6 +720,7 @@ proj_status_t copy_host(void *dst_dev, const void *src_dev, void *dst, const voi
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        if (launch_faulted()) return PROJ_ERR_CUDA;
         if (cudaLaunchKernelEx(&cfg, dev::proj_copy_kernel, static_cast<const uint8_t *>(src_dev),
                                static_cast<uint8_t *>(dst_dev), static_cast<int64_t>(bytes)) != cudaSuccess) {
             cudaGetLastError();
@@ -643,11 +739,11 @@ proj_status_t run_host_impl(proj_handle_t h, const void *X_host, const void *W, 
     const size_t xb = static_cast<size_t>(h->M) * h->K * 2;
     const size_t yb = static_cast<size_t>(h->M) * h->N * (h->y_dtype == PROJ_F32 ? 4 : 2);
     if (!h->stage_y) {
-        if (xb && cudaMalloc(&h->stage_x, xb) != cudaSuccess) {
+        if (xb && dev_malloc(&h->stage_x, xb) != cudaSuccess) {
             cudaGetLastError();
             return PROJ_ERR_OUT_OF_MEMORY;
         }
-        if (cudaMalloc(&h->stage_y, yb) != cudaSuccess) {
+        if (dev_malloc(&h->stage_y, yb) != cudaSuccess) {
             cudaGetLastError();
             cudaFree(h->stage_x);
             h->stage_x = nullptr;
@@ -752,7 +848,7 @@ proj_status_t proj_destroy(proj_handle_t h) {
 proj_status_t proj_selftest_wait_timeout(int64_t limit_ns, void *stream) {
     if (limit_ns < 1000 || limit_ns > 1000000000LL) return PROJ_ERR_INVALID_ARG;
     int *word = nullptr;
-    if (cudaMalloc(&word, sizeof(int)) != cudaSuccess) {
+    if (dev_malloc(reinterpret_cast<void **>(&word), sizeof(int)) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_OUT_OF_MEMORY;
     }
@@ -761,8 +857,12 @@ proj_status_t proj_selftest_wait_timeout(int64_t limit_ns, void *stream) {
     int host_word = 0;
     if (cudaMemsetAsync(word, 0, sizeof(int), s) != cudaSuccess) st = PROJ_ERR_CUDA;
     if (st == PROJ_OK) {
-        dev::proj_selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns, word);
-        st = check_launch();
+        if (launch_faulted()) {
+            st = PROJ_ERR_CUDA;
+        } else {
+            dev::proj_selftest_wait_kernel<<<1, 32, 0, s>>>(limit_ns, word);
+            st = check_launch();
+        }
     }
     if (st == PROJ_OK && (cudaMemcpyAsync(&host_word, word, sizeof(int), cudaMemcpyDeviceToHost, s) !=
                               cudaSuccess ||
@@ -785,32 +885,99 @@ proj_status_t proj_selftest_wait_timeout(int64_t limit_ns, void *stream) {
 // same kernel as proj_run, taking its split-K scratch from the fixed-size
 // device array below instead of a handle.  Every GPU that loads this library
 // holds the array until the process exits.
+//
+// Layout of the array: a plan's partial sums from offset 0, its split-K
+// counters after them, and one status word in the last 256 bytes.  Each call
+// clears the counters it uses; the status word collects the error bits of
+// every call until proj_noalloc_device_status reads and clears it.
 // ----------------------------------------------------------------------------
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB: partials, counters, status
+constexpr size_t kNoAllocStatusOffset = kNoAllocScratchBytes - 256;
 constexpr int kNoAllocMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kNoAllocMaxDevices];  // device address of the array, per device
+// Per-device set-up: the array's device address (the host-side name of the
+// array is only a stand-in), the kernels' shared-memory limit and the
+// device's SM count, redone whenever the device's current context is a
+// different one (a context torn down by cudaDeviceReset takes the address
+// with it).  The plan of the last shape run on the device is kept too, so a
+// steady stream of calls of one shape plans once.
+struct NoAllocDevice {
+    bool ready = false;
+    unsigned long long ctx_id = 0;
+    void *scratch = nullptr;
+    int sms = 0, smem = 0;
+    bool has_plan = false;
+    int64_t M = 0, N = 0, K = 0;
+    int layout = 0, y_dtype = 0, bias = 0;
+    proj_plan_desc_t plan{};
+};
 
-// Set-up, once per device with that device current: the host-side name of the
-// array is only a stand-in, so the kernel gets the real device address.
-proj_status_t noalloc_scratch_for(int device, void **out) {
+std::mutex g_noalloc_mutex;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Unique id of the calling thread's current context (0 if there is none yet).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// The set-up of `device`, which must be current (done on its first use and
+// again after its context changed).  Call with g_noalloc_mutex held.
+proj_status_t noalloc_setup(int device, NoAllocDevice **out) {
     if (device < 0 || device >= kNoAllocMaxDevices) return PROJ_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[device]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
-            cudaGetLastError();
-            return PROJ_ERR_CUDA;
-        }
-        g_noalloc_ptr[device] = ptr;
+    NoAllocDevice &d = g_noalloc_dev[device];
+    const unsigned long long ctx = current_context_id();
+    if (d.ready && ctx != 0 && ctx == d.ctx_id) {
+        *out = &d;
+        return PROJ_OK;
     }
-    *out = g_noalloc_ptr[device];
+    d = NoAllocDevice{};
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return PROJ_ERR_CUDA;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
+        return PROJ_ERR_CUDA;
+    if (major != 10 || minor != 3) return PROJ_ERR_UNSUPPORTED;
+    if (!set_kernel_smem_limit(d.smem)) return PROJ_ERR_CUDA;
+    d.scratch = ptr;
+    d.ctx_id = current_context_id();  // the symbol lookup made the context current if it was not
+    d.ready = true;
+    *out = &d;
     return PROJ_OK;
+}
+
+// Error bits of the device status word as a status code.
+proj_status_t status_of_word(int word) {
+    if (word == 0) return PROJ_OK;
+    return (word & (kErrSmemTooSmall | kErrLaunchShape | kErrPairTmem)) ? PROJ_ERR_CUDA : PROJ_ERR_DEVICE_TIMEOUT;
 }
 
 }  // namespace
@@ -831,26 +998,39 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
 
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return PROJ_ERR_CUDA;
-    int major = 0, minor = 0, sms = 0, smem = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
-        return PROJ_ERR_CUDA;
-    if (major != 10 || minor != 3) return PROJ_ERR_UNSUPPORTED;
-
-    proj_device_desc_t dd{sms, smem};
-    if (!set_kernel_smem_limit(smem)) return PROJ_ERR_CUDA;
+    const int has_bias = bias != nullptr ? 1 : 0;
     proj_plan_desc_t plan;
-    proj_status_t st = plan_for_device(M, N, K, w_layout, y_dtype, bias != nullptr, dd, PlanOptions{}, &plan);
-    if (st != PROJ_OK) return st;
-    if (plan.kernel == PROJ_KERNEL_TC && w_layout == PROJ_W_KN && !loads_stored_kn(plan)) {
-        PlanOptions single;
-        single.cta_pair = 0;
-        st = plan_for_device(M, N, K, w_layout, y_dtype, bias != nullptr, dd, single, &plan);
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        NoAllocDevice *d = nullptr;
+        proj_status_t st = noalloc_setup(device, &d);
         if (st != PROJ_OK) return st;
+        if (!(d->has_plan && d->M == M && d->N == N && d->K == K && d->layout == w_layout &&
+              d->y_dtype == y_dtype && d->bias == has_bias)) {
+            d->has_plan = false;
+            proj_device_desc_t dd{d->sms, d->smem};
+            st = plan_for_device(M, N, K, w_layout, y_dtype, has_bias, dd, PlanOptions{}, &d->plan);
+            if (st != PROJ_OK) return st;
+            if (d->plan.kernel == PROJ_KERNEL_TC && w_layout == PROJ_W_KN && !loads_stored_kn(d->plan)) {
+                PlanOptions single;
+                single.cta_pair = 0;
+                st = plan_for_device(M, N, K, w_layout, y_dtype, has_bias, dd, single, &d->plan);
+                if (st != PROJ_OK) return st;
+            }
+            d->M = M;
+            d->N = N;
+            d->K = K;
+            d->layout = w_layout;
+            d->y_dtype = y_dtype;
+            d->bias = has_bias;
+            d->has_plan = true;
+        }
+        plan = d->plan;
+        scratch = d->scratch;
     }
     if (plan.kernel == PROJ_KERNEL_FILL) {
+        if (launch_faulted()) return PROJ_ERR_CUDA;
         dev::proj_fill_kernel<<<plan.grid, plan.threads, 0, s>>>(M, N, static_cast<const uint16_t *>(bias),
                                                                  Y, y_dtype == PROJ_F32, 0, nullptr);
         return check_launch();
@@ -860,21 +1040,21 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     if (!X || !W) return PROJ_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(W)) return PROJ_ERR_MISALIGNED;
 
-    void *scratch = nullptr;
-    st = noalloc_scratch_for(device, &scratch);
-    if (st != PROJ_OK) return st;
     const int64_t partial_bytes = partial_bytes_of(plan);
+    const int64_t counter_bytes = plan.scratch_bytes - 256 - partial_bytes;
     uint8_t *sc = static_cast<uint8_t *>(scratch);
-    // The array keeps the previous call's contents: counters and the status
-    // word must start at zero (partials are fully rewritten before use).
-    if (cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(plan.scratch_bytes - partial_bytes),
-                        s) != cudaSuccess) {
+    // The array keeps the previous call's contents: the counters must start
+    // at zero (partials are fully rewritten before use; the status word is
+    // left for proj_noalloc_device_status).
+    if (counter_bytes > 0 &&
+        cudaMemsetAsync(sc + partial_bytes, 0, static_cast<size_t>(counter_bytes), s) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }
 
     CUtensorMap map_x, map_w;
-    if (!encode_2d(&map_x, X, K, M, K * 2, kBlockK, x_box_rows(plan))) return PROJ_ERR_CUDA;
+    int32_t x_3d = 0;
+    if (!encode_x(&map_x, X, M, K, plan, &x_3d)) return PROJ_ERR_CUDA;
     const bool ok = w_layout == PROJ_W_NK ? encode_2d(&map_w, W, K, N, K * 2, kBlockK, w_box_rows(plan))
                                           : encode_2d(&map_w, W, N, K, N * 2, 64, kBlockK);
     if (!ok) return PROJ_ERR_CUDA;
@@ -895,12 +1075,49 @@ extern "C" proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_
     kp.y_vec = y_vec_of(Y, N, y_dtype);
     kp.partials = reinterpret_cast<float *>(sc);
     kp.counters = reinterpret_cast<uint32_t *>(sc + partial_bytes);
-    kp.status = reinterpret_cast<int *>(sc + plan.scratch_bytes - 256);
+    kp.status = reinterpret_cast<int *>(sc + kNoAllocStatusOffset);
     kp.trace = nullptr;
+    kp.x_3d = x_3d;
     TcLaunch l(plan, s, false);
     if (launch_tc(plan, l, plan.cluster_split > 1 && !plan.swap_ab, kp, map_w, map_x) != cudaSuccess) {
         cudaGetLastError();
         return PROJ_ERR_CUDA;
     }
     return PROJ_OK;
+}
+
+extern "C" proj_status_t proj_noalloc_device_status(void *stream) {
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return PROJ_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_noalloc_scratch, sizeof word, kNoAllocStatusOffset,
+                             cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return PROJ_ERR_CUDA;
+    }
+    if (word == 0) return PROJ_OK;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_noalloc_scratch, &zero, sizeof zero, kNoAllocStatusOffset,
+                           cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return PROJ_ERR_CUDA;
+    }
+    return status_of_word(word);
+}
+
+extern "C" proj_status_t proj_noalloc_selftest_wait_timeout(int64_t limit_ns, void *stream) {
+    if (limit_ns < 1000 || limit_ns > 1000000000LL) return PROJ_ERR_INVALID_ARG;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return PROJ_ERR_CUDA;
+    void *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+        NoAllocDevice *d = nullptr;
+        const proj_status_t st = noalloc_setup(device, &d);
+        if (st != PROJ_OK) return st;
+        scratch = d->scratch;
+    }
+    if (launch_faulted()) return PROJ_ERR_CUDA;
+    dev::proj_selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(
+        limit_ns, reinterpret_cast<int *>(static_cast<uint8_t *>(scratch) + kNoAllocStatusOffset));
+    return check_launch();
 }

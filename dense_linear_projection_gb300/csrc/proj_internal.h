@@ -93,6 +93,13 @@ struct PlanOptions {
     // per CTA, but its 8 clusters of 12 CTAs started about 5 us later after
     // the preceding call than 16 clusters of 6 (15.9 us per call vs 12.7).
     int32_t tm_cluster = 0;
+    // K per pipeline stage (PROJ_KPB): 0 lets the planner choose, 1 forces
+    // one 64-wide k-block a stage, 2 allows two (see the planner).
+    int32_t kpb = 0;
+    // Cluster split of exactly this size for swapped tiles of at most 64
+    // tokens whenever the clusters fit the SMs (PROJ_FORCE_CLUSTER; 0: the
+    // planner's rule).
+    int32_t force_cluster = 0;
 };
 // The planner behind proj_plan_compute (which uses the default options).
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
@@ -116,7 +123,9 @@ struct KernelParams {
     int32_t tiles_m;       // token-row tiles
     int32_t tiles_n;       // weight-row tiles
     int32_t raster_group;  // token tiles per raster group (tile order, see tile_coords)
-    int32_t k_blocks;
+    int32_t k_blocks;      // pipeline stages of K per tile: ceil(K / (64 · kpb))
+    int32_t kpb;           // 64-wide k-blocks per stage (1 or 2), loaded by one TMA op each for W and X
+    int32_t x_3d;          // X's tensor map is 3-D (64 K, rows, k-blocks): a stage's X in one op
     int32_t tiles_dp;      // whole tiles, dealt round-robin: CTA c gets c, c+G, ...
     int32_t grid;          // work owners the tiles are dealt to: CTAs, or pairs of CTAs
     int64_t units_sk;      // split-K units after the whole tiles
@@ -308,6 +317,12 @@ PROJ_HD int32_t plan_cta_b_rows(const proj_plan_desc_t &plan) {
 PROJ_HD int32_t plan_a_rows(const proj_plan_desc_t &plan) {
     return plan.swap_ab ? (plan.cta_pair ? plan.block_n / 2 : plan.block_n) : kBlockA;
 }
+// 64-wide k-blocks per stage, and the packed layout's k-blocks per weight
+// tile (whole stages: the blocks past K are zero).
+PROJ_HD int32_t plan_kpb(const proj_plan_desc_t &plan) {
+    return plan.block_k > kBlockK ? plan.block_k / kBlockK : 1;
+}
+PROJ_HD int64_t plan_packed_kblocks(const proj_plan_desc_t &plan) { return plan.k_blocks * plan_kpb(plan); }
 // Shared memory after the ring for a cluster split's incoming partial sums.
 PROJ_HD int32_t plan_red_bytes(const proj_plan_desc_t &plan) {
     return plan.swap_ab ? cluster_red_bytes(plan.cluster_split, plan_b_rows(plan))
@@ -323,6 +338,7 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
     kp.raster_group = plan.raster_group > 0 ? plan.raster_group : static_cast<int32_t>(plan.tiles_m);
     kp.k_blocks = static_cast<int32_t>(plan.k_blocks);
+    kp.kpb = plan.block_k > kBlockK ? plan.block_k / kBlockK : 1;
     kp.tiles_dp = static_cast<int32_t>(plan.tiles_dp);
     kp.cta_pair = plan.cta_pair;
     kp.grid = plan.cta_pair ? plan.grid / 2 : plan.grid;  // pairs own tiles, not CTAs
@@ -333,7 +349,7 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;
     kp.stages = plan.stages;
     kp.a_rows = plan_a_rows(plan);
-    kp.stage_bytes = stage_bytes_for(kp.a_rows, plan_cta_b_rows(plan));
+    kp.stage_bytes = kp.kpb * stage_bytes_for(kp.a_rows, plan_cta_b_rows(plan));
     kp.red_bytes = plan_red_bytes(plan);
     kp.tmem_cols = plan.tmem_cols;
     kp.acc_bufs = plan.tmem_cols >= 2 * kp.b_rows ? 2 : 1;

@@ -220,6 +220,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, uint3
         : "memory");
 }
 
+// 3-D tiled TMA load (x innermost): the box's z planes land one after another.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *map, uint32_t bar, int32_t x, int32_t y,
+                                            int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *map, uint32_t bar, int32_t x,
+                                                 int32_t y, int32_t z, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // CTA pairs: the same load, completing on an mbarrier that may sit in the
 // other CTA of the pair (`bar` is then a shared::cluster address from mapa).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *map, uint32_t bar, int32_t x,
@@ -601,9 +620,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // them, shared memory the kernel owns, read into accumulator rows that
     // are never used).
     const uint32_t a_bytes = static_cast<uint32_t>(p.a_rows) * kBlockK * 2;
+    // B region of one k-block (the B rows this CTA holds).
+    const uint32_t b_bytes = static_cast<uint32_t>(p.stage_bytes / p.kpb) - a_bytes;
+    // A stage holds kpb k-blocks: [A of each k-block][B of each k-block].
     // Where W and X land in a stage: W is the A operand when swapped, else B.
-    const uint32_t w_off = p.swap ? 0u : a_bytes;
-    const uint32_t x_off = p.swap ? a_bytes : 0u;
+    const uint32_t w_off = p.swap ? 0u : a_bytes * static_cast<uint32_t>(p.kpb);
+    const uint32_t x_off = p.swap ? a_bytes * static_cast<uint32_t>(p.kpb) : 0u;
+    const uint32_t w_blk = p.swap ? a_bytes : b_bytes;  // one k-block's W bytes
 
     if (threadIdx.x == 0) {
         trace_stamp(p, kTraceEntry);
@@ -695,20 +718,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 else
                     tma_load_2d(dst, map, bar, x, y, pol);
             };
-            // One k-block of a weight tile: a [block_n rows x 64 K] box for
-            // [N,K] weights; for [K,N] weights, block_n/64 boxes of 64 N-rows
-            // x 64 K, 8 KiB apart (the MN-major operand layout).
+            auto load3 = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x, int32_t y, int32_t z,
+                             uint64_t pol) {
+                if constexpr (kPair)
+                    tma_load_3d_pair(dst, map, bar, x, y, z, pol);
+                else
+                    tma_load_3d(dst, map, bar, x, y, z, pol);
+            };
+            // Stage kb of a weight tile: its kpb k-blocks of [block_n rows x
+            // 64 K]; for [K,N] weights, each k-block is block_n/64 boxes of
+            // 64 N-rows x 64 K, 8 KiB apart (the MN-major operand layout).
             auto load_w = [&](uint32_t dst, uint32_t full, int32_t tn, int32_t kb) {
+                const int32_t kb64 = kb * p.kpb;  // first 64-wide k-block of the stage
                 if (p.w_packed) {
-                    // Pre-packed: the stage is one contiguous block of block_n
-                    // rows x 128 bytes (a 2-D map of 64-wide rows).
-                    load(dst, &tmap_w, full, 0, (tn * p.k_blocks + kb) * p.block_n + w_row_off, pol_w);
+                    // Pre-packed: every (tile, k-block) is one contiguous block
+                    // of block_n rows x 128 bytes.  Two k-blocks a stage: planes
+                    // of a 3-D map, consecutive, one op; one: rows of a 2-D map
+                    // (a 2-D op is the quicker of the two for the TMA unit).
+                    if (p.kpb > 1)
+                        load3(dst, &tmap_w, full, 0, w_row_off, tn * p.k_blocks * p.kpb + kb64, pol_w);
+                    else
+                        load(dst, &tmap_w, full, 0, (tn * p.k_blocks + kb) * p.block_n + w_row_off, pol_w);
                 } else if (!p.w_kn) {
-                    load(dst, &tmap_w, full, kb * kBlockK, tn * p.block_n + w_row_off, pol_w);
+                    for (int32_t j = 0; j < p.kpb; ++j)
+                        load(dst + static_cast<uint32_t>(j) * w_blk, &tmap_w, full, (kb64 + j) * kBlockK,
+                             tn * p.block_n + w_row_off, pol_w);
                 } else {
-                    for (int32_t j = 0; j < w_rows / 64; ++j)
-                        load(dst + static_cast<uint32_t>(j) * 8192u, &tmap_w, full,
-                             tn * p.block_n + w_row_off + 64 * j, kb * kBlockK, pol_w);
+                    for (int32_t j = 0; j < p.kpb; ++j)
+                        for (int32_t i = 0; i < w_rows / 64; ++i)
+                            load(dst + static_cast<uint32_t>(j) * w_blk + static_cast<uint32_t>(i) * 8192u, &tmap_w,
+                                 full, tn * p.block_n + w_row_off + 64 * i, (kb64 + j) * kBlockK, pol_w);
                 }
             };
             // Optional weight prefetch: fill the ring with W before the
@@ -769,9 +808,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     dep_wait();
                     // fp32 router weights run as [H | L] along K: the second
-                    // half multiplies the same X k-blocks again.
-                    const int32_t xkb = (p.x_kb_mod > 0 && kb >= p.x_kb_mod) ? kb - p.x_kb_mod : kb;
-                    load(st_base + x_off, &tmap_x, full, xkb * kBlockK, tm * p.block_t + x_row_off, pol_x);
+                    // half multiplies the same X k-blocks again (a stage never
+                    // straddles the halves: kpb divides their k-blocks).
+                    const int32_t kb64 = kb * p.kpb;
+                    const int32_t xkb = (p.x_kb_mod > 0 && kb64 >= p.x_kb_mod) ? kb64 - p.x_kb_mod : kb64;
+                    if (p.x_3d) {
+                        // The stage's k-blocks of X: planes of a 3-D map, one op.
+                        load3(st_base + x_off, &tmap_x, full, 0, tm * p.block_t + x_row_off, xkb, pol_x);
+                    } else {
+                        const uint32_t x_blk = p.swap ? b_bytes : a_bytes;  // one k-block's X bytes
+                        for (int32_t j = 0; j < p.kpb; ++j)
+                            load(st_base + x_off + static_cast<uint32_t>(j) * x_blk, &tmap_x, full,
+                                 (xkb + j) * kBlockK, tm * p.block_t + x_row_off, pol_x);
+                    }
                     if (issued == 0 && pre == 0) trace_stamp(p, kTraceFirstLoad);
                     ++issued;
                     if (++stage == stages) {
@@ -812,21 +861,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after_sync();
                     if (seg_idx == 0 && kb == s.kb0) trace_stamp(p, kTraceFirstData);
-                    const uint32_t a_addr = base_addr + stage * static_cast<uint32_t>(p.stage_bytes);
-                    const uint32_t b_addr = a_addr + a_bytes;
+                    const uint32_t st_addr = base_addr + stage * static_cast<uint32_t>(p.stage_bytes);
+                    for (int32_t j = 0; j < p.kpb; ++j) {
+                        const uint32_t a_addr = st_addr + static_cast<uint32_t>(j) * a_bytes;
+                        const uint32_t b_addr =
+                            st_addr + a_bytes * static_cast<uint32_t>(p.kpb) + static_cast<uint32_t>(j) * b_bytes;
 #pragma unroll
-                    for (int kk = 0; kk < kBlockK / kMmaK; ++kk) {
-                        // K-major: the next 16 K values start 32 bytes further
-                        // along the 128-byte swizzled row.  MN-major (W stored
-                        // [K,N]): 16 more K rows, 16 × 128 bytes further; its
-                        // 64-wide MN blocks are 8 KiB apart.
-                        const uint64_t a_desc =
-                            a_mn ? smem_desc_sw128(a_addr + kk * (kMmaK * 128), 8192, 1024)
-                                 : smem_desc_sw128(a_addr + kk * (kMmaK * 2), 16, 1024);
-                        const uint64_t b_desc =
-                            b_mn ? smem_desc_sw128(b_addr + kk * (kMmaK * 128), 8192, 1024)
-                                 : smem_desc_sw128(b_addr + kk * (kMmaK * 2), 16, 1024);
-                        tc_mma<kPair>(d_tmem, a_desc, b_desc, p.idesc, (kb > s.kb0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kBlockK / kMmaK; ++kk) {
+                            // K-major: the next 16 K values start 32 bytes further
+                            // along the 128-byte swizzled row.  MN-major (W stored
+                            // [K,N]): 16 more K rows, 16 × 128 bytes further; its
+                            // 64-wide MN blocks are 8 KiB apart.
+                            const uint64_t a_desc =
+                                a_mn ? smem_desc_sw128(a_addr + kk * (kMmaK * 128), 8192, 1024)
+                                     : smem_desc_sw128(a_addr + kk * (kMmaK * 2), 16, 1024);
+                            const uint64_t b_desc =
+                                b_mn ? smem_desc_sw128(b_addr + kk * (kMmaK * 128), 8192, 1024)
+                                     : smem_desc_sw128(b_addr + kk * (kMmaK * 2), 16, 1024);
+                            tc_mma<kPair>(d_tmem, a_desc, b_desc, p.idesc,
+                                          (kb > s.kb0 || j > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     // The stage is free (in both CTAs of a pair) once these MMAs finish.
                     if constexpr (kPair)

@@ -432,12 +432,41 @@ proj_status_t proj_plan_info(proj_handle_t h, char *buf, size_t len);
  *     PROJ_ERR_UNSUPPORTED.
  *   - Every call shares the array: calls that overlap on the GPU (other
  *     streams, other threads) race and give wrong results.  Each call clears
- *     the array's counters and status word on `stream` before its kernel.
- * Returns the same status codes as proj_create/proj_run.
+ *     the split-K counters it uses on `stream` before its kernel.
+ *   - The first call on a device (and the first after the device's context
+ *     changed) also sets the kernels' shared-memory limit; the plan of the
+ *     last shape run on each device is kept, so repeated calls of one shape
+ *     plan once.
+ * Returns the argument and launch status codes of proj_create/proj_run.  A
+ * bounded device wait that gave up inside the kernel is not known when the
+ * call returns: the kernel records it in the array's status word, which
+ * collects the error bits of every call until proj_noalloc_device_status
+ * reads and clears it.
  */
 proj_status_t proj_run_noalloc(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,
                                proj_dtype_t y_dtype, const void *X, const void *W,
                                const void *bias, void *Y, void *stream);
+
+/*
+ * Device status of proj_run_noalloc, the allocation-free counterpart of
+ * proj_device_status: synchronises `stream`, reads the fixed array's status
+ * word and clears it.  PROJ_OK if no call since the last read recorded an
+ * error; PROJ_ERR_DEVICE_TIMEOUT if a bounded wait gave up (the output of
+ * that call is incomplete); PROJ_ERR_CUDA for a launch whose shared memory
+ * or cluster shape did not match its plan, or if the read itself failed.
+ * Allocates nothing.  The worklog has no counterpart of this call.
+ */
+proj_status_t proj_noalloc_device_status(void *stream);
+
+/*
+ * proj_selftest_wait_timeout for the allocation-free path: one CTA waits on a
+ * barrier nothing arrives on, gives up after `limit_ns` (1 µs .. 1 s) and
+ * records the timeout in the fixed array's status word, where
+ * proj_noalloc_device_status then reports PROJ_ERR_DEVICE_TIMEOUT.
+ * Asynchronous on `stream`; allocates nothing; PROJ_ERR_INVALID_ARG for a
+ * limit out of range.  No fault, trap or hang is involved.
+ */
+proj_status_t proj_noalloc_selftest_wait_timeout(int64_t limit_ns, void *stream);
 
 /* Free the handle and its scratch (synchronises the device).  NULL is a no-op. */
 proj_status_t proj_destroy(proj_handle_t h);

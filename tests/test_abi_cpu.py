@@ -77,7 +77,11 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
         assert p["block_n"] == 128 and p["block_t"] % 16 == 0
     else:
         assert p["block_t"] == 128 and p["block_n"] % 16 == 0 and 64 <= p["block_n"] <= 256
-    assert KT == -(-K // 64)
+    # Two 64-wide k-blocks a stage for the weight-streaming swapped plans (at
+    # most 64 tokens, K a multiple of 64), one otherwise.
+    kpb = 2 if (p["swap_ab"] and not pair and p["block_t"] <= 64 and K % 64 == 0) else 1
+    assert p["block_k"] == 64 * kpb
+    assert KT == -(-K // p["block_k"])
     assert 1 <= G <= GB300["sm_count"]
     assert p["tiles_dp"] + p["tiles_sk"] == tiles
     S = p["cluster_split"]
@@ -113,7 +117,7 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
         quarters = -(-4 // S) if S <= 4 else 1
         red = quarters * (S - 1) * 32 * b_rows * 4
     # A CTA of a pair stages half of the B rows.
-    assert p["smem_bytes"] == p["stages"] * (128 + (b_rows // 2 if pair else b_rows)) * 128 + red + 25600
+    assert p["smem_bytes"] == p["stages"] * kpb * (128 + (b_rows // 2 if pair else b_rows)) * 128 + red + 25600
     cover = np.zeros((tiles, KT), dtype=np.int32)
     by_tile = collections.defaultdict(list)
     coords = {}
@@ -193,9 +197,10 @@ def test_cluster_split_plans():
     # Fewer than 10 % of the SMs busy: 1 tile with 4 or 8 k-blocks on 152 SMs.
     assert plan(16, 128, 256)["cluster_split"] == 0
     assert plan(16, 128, 512)["cluster_split"] == 0
-    # S is capped by the k-blocks there are to share (5 SMs, 1 tile, 4 k-blocks).
-    p = plan(16, 128, 256, sm_count=5, smem_optin_bytes=232448)
-    assert p["k_blocks"] == 4 and p["cluster_split"] == 4 and p["grid"] == 4
+    # S is capped by the stages of K there are to share (5 SMs, 1 tile, K = 512
+    # in 4 stages of two k-blocks).
+    p = plan(16, 128, 512, sm_count=5, smem_optin_bytes=232448)
+    assert p["k_blocks"] == 4 and p["block_k"] == 128 and p["cluster_split"] == 4 and p["grid"] == 4
     # Several token tiles (100 tokens in two 64-row tiles) are clustered too.
     p = plan(100, 1024, 8192)
     assert (p["block_t"], p["tiles_m"], p["cluster_split"], p["grid"]) == (64, 2, 9, 144)
@@ -269,7 +274,9 @@ def test_token_tile_choice():
 def test_scratch_and_stages():
     p = plan(16, 28672, 8192)
     assert p["tiles_sk"] > 0 and p["cluster_split"] == 0
-    stage = 128 * 64 * 2 + p["block_t"] * 64 * 2  # swapped: B holds the token rows
+    # swapped: B holds the token rows; two k-blocks a stage
+    stage = (p["block_k"] // 64) * (128 * 64 * 2 + p["block_t"] * 64 * 2)
+    assert p["block_k"] == 128
     assert p["smem_bytes"] == p["stages"] * stage + 25600
     assert p["scratch_bytes"] >= 2 * p["grid"] * p["block_t"] * 128 * 4 + 4 * 4 * p["tiles_sk"]
     assert p["tmem_cols"] >= 2 * p["block_t"] and p["tmem_cols"] in (32, 64, 128, 256, 512)

@@ -76,14 +76,15 @@ def test_pack_layout_matches_definition(M, N, K, layout):
     proj = dlp.Projection(M, N, K, layout, dlp.PROJ_BF16)
     p = proj.plan
     nbytes = dlp.proj_packed_weight_bytes(proj.handle)
-    assert nbytes == p["tiles_n"] * p["k_blocks"] * p["block_n"] * 128
+    kblk = p["k_blocks"] * (p["block_k"] // 64)  # 64-wide k-blocks per weight tile, whole stages
+    assert nbytes == p["tiles_n"] * kblk * p["block_n"] * 128
     W = gu.to_dev(inp["W"])
     # Pre-fill the destination so that unwritten or non-zero padding shows.
     P = torch.full((nbytes // 2,), -1, dtype=torch.int16, device="cuda").view(torch.bfloat16)
     dlp.proj_pack_weights(proj.handle, W, P, torch.cuda.current_stream())
     torch.cuda.synchronize()
     got = P.view(torch.int16).cpu().numpy().view(np.uint16)
-    want = expected_packed(inp["W"], layout, N, K, p["block_n"], p["k_blocks"], p["tiles_n"])
+    want = expected_packed(inp["W"], layout, N, K, p["block_n"], kblk, p["tiles_n"])
     assert np.array_equal(got, want)
 
 
