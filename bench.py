@@ -46,6 +46,8 @@ import subprocess
 import sys
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -53,6 +55,9 @@ if ROOT not in sys.path:
 METRIC = "projection µs & weight HBM GB/s (M=16,K=8192) / TFLOP/s at M≥512 vs roofline"
 DEFAULT_WORKLOAD = "decode_bias"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 datasheet figures (nominal, not measured): HBM3e bandwidth and dense
+# bf16 tensor throughput.  Reported beside the measured-peak fractions.
+DATASHEET = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 CSRC_DIR = os.path.join(ROOT, "dense_linear_projection_gb300", "csrc")
 
@@ -111,6 +116,16 @@ def profile_traffic(workload: str):
         return int(fields["traffic_bytes_per_launch"]), os.path.relpath(path, ROOT)
     except (KeyError, ValueError):
         return None, os.path.relpath(path, ROOT)
+
+
+def hold_stream(stream, seconds: float = 50e-6) -> None:
+    """Queue a short spin kernel on ``stream``: while it runs, the host queues
+    the start event and the timed graph behind it, so the timed region holds
+    the device time of the steps alone, not the host's launch latency (the
+    blocking-kernel technique of GPU benchmark harnesses)."""
+    import torch
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(seconds * 2.0e9))
 
 
 def dist_env():
@@ -287,6 +302,173 @@ def swiglu_output_check(w, inp, y_gpu, residual, features: int = 64) -> dict:
     return {"cells": int(u.size), "out_of_tolerance": bad}
 
 
+# ---------------------------------------------------------------- every config
+def oracle_report(w, inp, y64: np.ndarray, rows) -> dict:
+    """Accuracy of the GPU output against the fp64 oracle on the given token
+    rows (all columns): the elementwise rule of the parity tests, relative L2
+    over those rows, and the row rule of section "The actual error rule,
+    including what L2 means" (each row's error norm over max(row norm, a tenth
+    of the mean row norm)).  Also returns the all-thread oracle time of the
+    sample."""
+    import oracle
+    Xs = np.ascontiguousarray(inp["X"][rows])
+    t0 = time.perf_counter()
+    r = oracle.project(Xs, inp["W"], w.w_layout, inp["bias"])
+    t_all = time.perf_counter() - t0
+    u = y64[rows]
+    bad = int(np.count_nonzero(~(np.abs(u - r) <= 1e-3 + 5e-3 * np.abs(r))))
+    diff = np.linalg.norm(u - r, axis=1)
+    rn = np.linalg.norm(r, axis=1)
+    denom = np.maximum(rn, 0.1 * rn.mean())
+    return {"rows_checked": int(len(rows)), "cells": int(u.size), "out_of_tolerance": bad,
+            "max_abs_err": float(np.abs(u - r).max()),
+            "rel_l2": float(np.linalg.norm(u - r) / np.linalg.norm(r)),
+            "row_rule_max": float((diff / denom).max())}, t_all
+
+
+def oracle_single_thread_ms(w, inp, target_s: float = 0.4) -> tuple:
+    """Single-thread oracle time of one whole call, extrapolated from a block
+    of output columns (all token rows, or the first 64 of many)."""
+    import oracle
+    X, W, b = inp["X"], inp["W"], inp["bias"]
+    m = min(w.M, 64)
+    Xs = np.ascontiguousarray(X[:m])
+
+    def cols(nc):
+        Wc = np.ascontiguousarray(W[:nc] if w.w_layout == 0 else W[:, :nc])
+        return Wc, (None if b is None else b[:nc])
+
+    prev = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        Wc, bc = cols(min(w.N, 8))
+        t0 = time.perf_counter()
+        oracle.project(Xs, Wc, w.w_layout, bc)
+        per_col = max(time.perf_counter() - t0, 1e-6) / Wc.shape[0 if w.w_layout == 0 else 1]
+        nc = int(max(8, min(w.N, target_s / per_col)))
+        Wc, bc = cols(nc)
+        t0 = time.perf_counter()
+        oracle.project(Xs, Wc, w.w_layout, bc)
+        dt = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(prev)
+    full = dt * (w.N / nc) * (w.M / m)
+    return full * 1e3, f"{m} of {w.M} token rows x {nc} of {w.N} columns, scaled to the whole call"
+
+
+def measure_workloads(args, device, peaks: dict) -> dict:
+    """Every configuration the metric names, each timed like the headline:
+    packed weights rotating through copies larger than twice the L2, the
+    --steps steps replayed from one CUDA graph (warmed once), device time of
+    the steps alone.  Per config: µs per call, weight GB/s, TFLOP/s, the
+    roofline fraction (measured and datasheet peaks), the oracle's time on
+    the host cores (all threads and one thread) and its accuracy report."""
+    import torch
+    import dense_linear_projection_gb300 as dlp
+    import oracle
+    import synth
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    stream = torch.cuda.Stream(device)
+    out = {}
+    cores = oracle.max_threads()
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+    def one(key, w, inp):
+        X = dev_bf16(inp["X"])
+        W0 = dev_bf16(inp["W"])
+        bias = dev_bf16(inp["bias"]) if w.has_bias else None
+        n_copies = max(2, math.ceil(2 * l2 / w.weight_bytes) + 1)
+        proj = dlp.Projection(w.M, w.N, w.K, w.w_layout,
+                              dlp.PROJ_F32 if w.y_dtype == "f32" else dlp.PROJ_BF16, w.has_bias,
+                              overlap=dlp.PROJ_OVERLAP_PROLOGUE)
+        Wp = [proj.pack(W0)] + [proj.pack(W0.clone()) for _ in range(n_copies - 1)]
+        del W0
+        Y = torch.empty((w.M, w.N), dtype=torch.float32 if w.y_dtype == "f32" else torch.bfloat16,
+                        device=device)
+        torch.cuda.synchronize()  # inputs and packing (current stream) before the runs on `stream`
+        steps = max(args.steps, 2 * n_copies)
+        with torch.cuda.stream(stream):
+            proj(X, Wp[0], bias, out=Y, stream=stream, packed=True)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(steps):
+                proj(X, Wp[i % n_copies], bias, out=Y, stream=stream, packed=True)
+        with torch.cuda.stream(stream):
+            g.replay()  # warm-up: the same graph (its first launch also uploads it)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        hold_stream(stream)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        st = proj.status(stream)
+        if st != dlp.PROJ_OK:
+            raise RuntimeError(f"{key}: device status {dlp.proj_status_string(st)}")
+        t = e0.elapsed_time(e1) / 1e3 / steps
+        y64 = Y.float().cpu().numpy().astype(np.float64)
+        plan = proj.plan
+        proj.close()
+        del Wp, g
+        torch.cuda.empty_cache()
+        bytes_alg, flops = w.algorithmic_bytes, w.flops
+        hbm_t = bytes_alg / (peaks["hbm_gbs"] * 1e9)
+        ten_t = flops / (peaks["bf16_tflops"] * 1e12)
+        if hbm_t >= ten_t:
+            achieved = bytes_alg / t / 1e9
+            roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"],
+                    "datasheet": {"peak": DATASHEET["hbm_gbs"], "frac": achieved / DATASHEET["hbm_gbs"]}}
+        else:
+            achieved = flops / t / 1e12
+            roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"],
+                    "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                    "datasheet": {"peak": DATASHEET["bf16_tflops"],
+                                  "frac": achieved / DATASHEET["bf16_tflops"]}}
+        roof["peak_source"] = "of measured" if peaks["source"] == "measured" else "of fallback"
+        roof["bytes_per_launch"] = bytes_alg
+        roof["flops_per_launch"] = flops
+        # Accuracy against the oracle: every token row up to 256, else 128
+        # rows spread over the output (first, last and evenly spaced).
+        rows = (np.arange(w.M) if w.M <= 256
+                else np.unique(np.linspace(0, w.M - 1, 128).astype(np.int64)))
+        acc, t_all = oracle_report(w, inp, y64, rows)
+        ms_1t, sample_1t = oracle_single_thread_ms(w, inp)
+        out[key] = {
+            "M": w.M, "N": w.N, "K": w.K, "w_layout": "NK" if w.w_layout == 0 else "KN",
+            "bias": w.has_bias, "y_dtype": w.y_dtype, "seed": w.seed, "steps": steps,
+            "us_per_call": t * 1e6, "weight_gbs": w.weight_bytes / t / 1e9,
+            "tflops": flops / t / 1e12, "roofline": roof,
+            "plan": {k: plan[k] for k in ("block_t", "block_n", "grid", "stages", "cluster_split",
+                                          "cta_pair", "tiles_dp", "tiles_sk")},
+            "oracle": {"cores": cores,
+                       "ms_all_threads": t_all * 1e3 * (w.M / len(rows)),
+                       "all_threads_sample": (f"all {w.M} token rows" if len(rows) == w.M else
+                                              f"{len(rows)} of {w.M} token rows, scaled to the whole call"),
+                       "ms_single_thread": ms_1t, "single_thread_sample": sample_1t},
+            "accuracy_vs_oracle": acc,
+        }
+
+    for name in args.workload_list:
+        if name == "ffn_up_sweep":
+            base = synth.workload(name, max(synth.FFN_SWEEP_M))
+            full = synth.make_inputs(base)  # X rows of smaller M are a prefix (same seed)
+            for M in synth.FFN_SWEEP_M:
+                w = base.with_m(M)
+                one(f"ffn_up_sweep_m{M}", w, dict(full, X=np.ascontiguousarray(full["X"][:M])))
+            del full
+        else:
+            w = synth.workload(name)
+            one(name, w, synth.make_inputs(w))
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm
 def run_gpu_arm(args) -> dict:
     import numpy as np
@@ -373,7 +555,10 @@ def run_gpu_arm(args) -> dict:
 
     sampler = ClockSampler(visible_gpu_id(local)).start()
     with torch.cuda.stream(stream):
-        run_steps(chunk * math.ceil(args.warmup / chunk))  # at least `warmup` steps
+        # Warm-up replays the very graphs the timed region replays (a graph's
+        # first launch also uploads it), at least `warmup` steps in all.
+        for _ in range(max(1, math.ceil(args.warmup / args.steps))):
+            run_steps(args.steps)
         # Untimed soak so the clock sampler sees the GPU under load even when
         # the timed region itself is only milliseconds long.
         t_soak = time.perf_counter()
@@ -384,6 +569,7 @@ def run_gpu_arm(args) -> dict:
         dist.barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    hold_stream(stream)
     with torch.cuda.stream(stream):
         ev0.record(stream)
         run_steps(args.steps)
@@ -408,6 +594,7 @@ def run_gpu_arm(args) -> dict:
         with torch.cuda.stream(stream):
             for _ in range(args.repeats):
                 a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                hold_stream(stream)
                 a.record(stream)
                 for _ in range(r_steps // chunk):
                     g_chunk.replay()
@@ -427,6 +614,7 @@ def run_gpu_arm(args) -> dict:
             for i in range(args.cold_calls):
                 flush.fill_(float(i))
                 a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                hold_stream(stream)
                 a.record(stream)
                 step(Wrun[i % n_copies], stream)
                 b_.record(stream)
@@ -434,7 +622,7 @@ def run_gpu_arm(args) -> dict:
                 times.append(a.elapsed_time(b_) * 1e3)
         del flush
         cold = {"calls": args.cold_calls, "median_us": statistics.median(times),
-                "what": "one proj_run after writing 2x L2, events around the call alone"}
+                "what": "one proj_run after writing 2x L2, events around the call alone (device time)"}
 
     # ---- Informational: the same projection through cuBLAS (torch), never the target.
     library = None
@@ -464,6 +652,7 @@ def run_gpu_arm(args) -> dict:
             for _ in range(max(1, math.ceil(args.warmup / chunk))):
                 gl.replay()
             a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            hold_stream(stream)
             a.record(stream)
             for _ in range(l_steps // chunk):
                 gl.replay()
@@ -493,6 +682,8 @@ def run_gpu_arm(args) -> dict:
         roof = {"bound": "tensor", "achieved": w.flops / t_step / 1e12, "peak": peak_tf,
                 "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    ds = DATASHEET["hbm_gbs"] if roof["bound"] == "hbm" else DATASHEET["bf16_tflops"]
+    roof["datasheet"] = {"peak": ds, "frac": roof["achieved"] / ds}
     roof["traffic"] = traffic
     roof["peak_source"] = ("of measured" if peaks["source"] == "measured" else "of fallback")
     roof["bytes_per_launch"] = alg_bytes
@@ -545,7 +736,45 @@ def run_gpu_arm(args) -> dict:
                                                             R.double().cpu().numpy())
         cpu.pop("seconds", None)
 
+    # ---- The allocation-free entry point against proj_run on the same weights
+    # as stored (it takes no packed weights): eager calls, so the host-side
+    # cost of each call shows (host µs per call) beside the device time.
+    noalloc = None
+    if rank == 0 and world == 1 and not args.no_noalloc and not fp32_w and not fused:
+        y_code = dlp.PROJ_F32 if w.y_dtype == "f32" else dlp.PROJ_BF16
+        calls = 64
+
+        def eager(fn):
+            for i in range(8):
+                fn(i)
+            torch.cuda.synchronize()
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            h0 = time.perf_counter()
+            for i in range(calls):
+                fn(i)
+            host = time.perf_counter() - h0
+            b_.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b_) * 1e3 / calls, host * 1e6 / calls
+
+        run_us, run_host = eager(lambda i: dlp.proj_run(proj.handle, X, Ws[i % n_copies], bias, Y, stream))
+        na_us, na_host = eager(lambda i: dlp.proj_run_noalloc(w.M, w.N, w.K, w.w_layout, y_code, X,
+                                                              Ws[i % n_copies], bias, Y, stream))
+        st_na = dlp.proj_noalloc_device_status(stream)
+        if st_na != dlp.PROJ_OK:
+            raise RuntimeError(f"allocation-free path status: {dlp.proj_status_string(st_na)}")
+        noalloc = {"calls": calls, "proj_run_us_per_call": run_us, "proj_run_host_us_per_call": run_host,
+                   "noalloc_us_per_call": na_us, "noalloc_host_us_per_call": na_host,
+                   "what": "eager back-to-back calls on the weights as stored (no graph), events around "
+                           "the loop; host µs = enqueue time per call"}
+
     plan = proj.plan
+    proj.close()
+    workloads = None
+    if rank == 0 and world == 1 and args.workload_list:
+        torch.cuda.empty_cache()
+        workloads = measure_workloads(args, device, peaks)
     line = {
         "metric": METRIC,
         "value": agg["per_second"] / 1e9,
@@ -585,8 +814,9 @@ def run_gpu_arm(args) -> dict:
         "clocks": clocks,
         "plan": {k: plan[k] for k in ("kernel", "block_t", "stages", "grid", "tiles_dp",
                                       "tiles_sk", "units_sk")},
+        "noalloc": noalloc,
+        "workloads": workloads,
     }
-    proj.close()
     if world > 1:
         dist.destroy_process_group()
     return line if rank == 0 else None
@@ -671,6 +901,8 @@ def parse_args(argv=None):
                     help="shorter timed regions for the median/p10/p90 spread (0: none)")
     ap.add_argument("--cold-calls", type=int, default=10,
                     help="single calls timed after an L2 flush (0: none)")
+    ap.add_argument("--no-noalloc", action="store_true",
+                    help="skip the allocation-free entry point's per-call timing")
     ap.add_argument("--no-library", dest="library", action="store_false",
                     help="skip the informational cuBLAS timing")
     ap.add_argument("--no-packed", dest="packed", action="store_false",
@@ -680,7 +912,11 @@ def parse_args(argv=None):
                          "reads W as [gate rows; up rows] and writes N/2 columns")
     ap.add_argument("--residual", action="store_true",
                     help="fused residual add: Y = act(X·Wᵀ + b) + R, R an [M,N] input")
+    ap.add_argument("--workloads", default="decode_f32out,decode_bias,ffn_up_sweep,qkv_kn_bias,prefill",
+                    help="comma-separated configs also timed into the line's 'workloads' object "
+                         "(single GPU only; empty: none)")
     args = ap.parse_args(argv)
+    args.workload_list = [x for x in args.workloads.split(",") if x]
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.steps < 1:
