@@ -188,7 +188,9 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 }
             }
             const int32_t pb_rows = swap ? pbt : pbn;
-            const int32_t pstage = stage_bytes_for(kBlockA, pb_rows / 2);
+            // Two k-blocks a stage for pairs only when asked (PROJ_KPB=2).
+            const int32_t pkpb = (opt.kpb == 2 && K % kBlockK == 0) ? 2 : 1;
+            const int32_t pstage = pkpb * stage_bytes_for(kBlockA, pb_rows / 2);
             int32_t pstages = budget / pstage;
             if (pstages > kMaxStages) pstages = kMaxStages;
             const int64_t ptiles = ceil_div(M, pbt) * ceil_div(N, pbn);
@@ -207,7 +209,8 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 int64_t g = 2048 / pbt;
                 if (g < 1) g = 1;
                 out->raster_group = static_cast<int32_t>(out->tiles_m < g ? out->tiles_m : g);
-                out->k_blocks = ceil_div(K, kBlockK);
+                out->block_k = pkpb * kBlockK;
+                out->k_blocks = ceil_div(K, out->block_k);
                 const int64_t tiles = out->tiles_m * out->tiles_n;
                 out->grid = static_cast<int32_t>(2 * (tiles < pairs_max ? tiles : pairs_max));
                 out->tiles_dp = tiles;
@@ -233,7 +236,8 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // a stage streamed 61 GB/s of weights per SM, one 32 KiB and one 4 KiB
     // op 122 GB/s, so about 64 SMs instead of 110 keep HBM busy.  The
     // activations' 3-D tensor map needs K to be a multiple of 64.
-    const int32_t kpb = (swap && bt <= 64 && K % kBlockK == 0 && opt.kpb != 1) ? 2 : 1;
+    // (PROJ_KPB=2 also allows two for the other plans, as an experiment.)
+    const int32_t kpb = (((swap && bt <= 64 && opt.kpb != 1) || opt.kpb == 2) && K % kBlockK == 0) ? 2 : 1;
     out->block_k = kpb * kBlockK;
     const int32_t stage = kpb * stage_bytes_for(half ? bn : kBlockA, b_rows);
     int32_t stages = budget / stage;
@@ -272,18 +276,25 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // (weight-streaming) plans, 80 % for the tensor-bound token-major plans,
     // whose split partial tiles are large.
     //
-    // Cluster split: far fewer (swapped, narrow) tiles than SMs, each split
-    // along K over the S CTAs of one thread-block cluster whose partial sums
-    // meet in distributed shared memory (no global scratch, no atomics).
-    // Stream-K over every SM wins while a split tile has about three
-    // contributors or fewer (3·tiles >= SMs); below that its fixups cost more
-    // than the idle SMs of a cluster split.  Measured on GB300 with packed
-    // weights, K = 8192, 16 tokens: 64 tiles, stream-K 25.2 us vs clusters of
-    // 2 26.2 us; 16 tiles, clusters of 6 on 96 SMs 12.6 us vs stream-K 13.4 us;
-    // the 2 tiles of a 256-row router weight, clusters of 8 on 16 SMs 14.6 us vs
-    // 16.3 us for stream-K at its best grid.  S goes up to 16 (a non-portable
-    // cluster size); the clusters must keep cluster_fill_pct (10) % of the SMs
-    // busy.
+    // Cluster split: fewer (swapped, narrow) tiles than SMs, each split along
+    // K over the S CTAs of one thread-block cluster whose partial sums meet
+    // in distributed shared memory (no global scratch, no atomics).
+    //   * Two k-blocks a stage: whenever S = SMs / tiles >= 2.  A CTA then
+    //     streams up to twice the HBM share of one SM, so the S·tiles CTAs
+    //     (at least half of the SMs) keep HBM busy, and the reduction in
+    //     shared memory is cheaper than stream-K's through global memory.
+    //     Measured on GB300 with packed weights, 16 tokens, K = 8192: 64
+    //     tiles in clusters of 2 on 128 SMs 24.8 us, stream-K on 152 SMs
+    //     26.2 us (26.1-26.5 on 128-144 SMs).
+    //   * One k-block a stage: only while 3·tiles < SMs, when stream-K would
+    //     give a split tile more than about three contributors.  With one
+    //     k-block a stage a CTA streams at most about 50 GB/s, so idle SMs
+    //     cost bandwidth: 64 tiles, stream-K 25.2 us vs clusters of 2
+    //     26.2 us; 16 tiles, clusters of 6 on 96 SMs 12.6 us vs stream-K
+    //     13.4 us; the 2 tiles of a 256-row router weight, clusters of 8 on
+    //     16 SMs 14.6 us vs 16.3 us for stream-K at its best grid.
+    // S goes up to 16 (a non-portable cluster size); the clusters must keep
+    // cluster_fill_pct (10) % of the SMs busy.
     //
     // Token-major cluster split (at most 32 tokens): the same split over K,
     // with the tokens as the MMA's A rows (zero beyond M) and 256 weight rows
@@ -298,7 +309,8 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     if (opt.force_cluster >= 2 && swap && b_rows <= 64 && int64_t(opt.force_cluster) * tiles <= sms &&
         opt.force_cluster <= out->k_blocks && budget - red_for(opt.force_cluster) >= 2 * stage) {
         S = opt.force_cluster;
-    } else if ((tm_cluster || (swap && b_rows <= 64)) && opt.max_cluster >= 2 && 3 * tiles < sms) {
+    } else if ((tm_cluster || (swap && b_rows <= 64)) && opt.max_cluster >= 2 &&
+               (kpb == 2 ? 2 * tiles <= sms : 3 * tiles < sms)) {
         int64_t s_try = sms / tiles;
         if (s_try > opt.max_cluster) s_try = opt.max_cluster;
         if (s_try > out->k_blocks) s_try = out->k_blocks;
@@ -345,7 +357,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // over several token tiles are tensor-bound and keep the whole ring.
     const bool streaming = out->tiles_m == 1 || out->tiles_sk > 0;
     if (streaming) {
-        int32_t want = kInflightTarget / stage;
+        int32_t want = opt.inflight_bytes / stage;
         // (Counted in 64-wide k-blocks: a stage of two counts twice.)
         const int64_t units_per_cta = kpb * (out->tiles_dp * out->k_blocks + out->units_sk) / out->grid;
         if (!half && !tm_cluster && units_per_cta / 3 < want) want = static_cast<int32_t>(units_per_cta / 3);

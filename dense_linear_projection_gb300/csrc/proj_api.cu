@@ -384,6 +384,10 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int c = std::atoi(e);
         if (c >= 0 && c <= 2) opt.tm_cluster = c;
     }
+    if (const char *e = std::getenv("PROJ_INFLIGHT_KB")) {
+        const int kb = std::atoi(e);
+        if (kb >= 16 && kb <= 228) opt.inflight_bytes = kb * 1024;
+    }
     if (const char *e = std::getenv("PROJ_FORCE_CLUSTER")) {
         const int c = std::atoi(e);
         if (c >= 2 && c <= kMaxClusterSplit) opt.force_cluster = c;
@@ -394,8 +398,9 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     const int64_t kt = (K + kBlockK - 1) / kBlockK;
     const int64_t k_plan = hilo ? 2 * kt * kBlockK : K;
     if (hilo && kt % 2 != 0) opt.kpb = 1;
-    if (const char *e = std::getenv("PROJ_KPB")) {  // tuning only: 1 = one k-block a stage
-        if (std::atoi(e) == 1) opt.kpb = 1;
+    if (const char *e = std::getenv("PROJ_KPB")) {  // tuning only: 1 = one k-block a stage, 2 = two wherever K allows
+        const int c = std::atoi(e);
+        if ((c == 1 || c == 2) && !(hilo && kt % 2 != 0)) opt.kpb = c;
     }
     proj_status_t st = plan_for_device(M, N, k_plan, w_layout, y_dtype, has_bias, dd, opt, &plan);
     if (st != PROJ_OK) return st;

@@ -100,6 +100,9 @@ struct PlanOptions {
     // tokens whenever the clusters fit the SMs (PROJ_FORCE_CLUSTER; 0: the
     // planner's rule).
     int32_t force_cluster = 0;
+    // Stage bytes per SM a weight-streaming plan keeps in flight
+    // (PROJ_INFLIGHT_KB).
+    int32_t inflight_bytes = kInflightTarget;
 };
 // The planner behind proj_plan_compute (which uses the default options).
 proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layout,

@@ -241,6 +241,10 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
  *   PROJ_FORCE_WHOLE_TILES=1 no split tiles
  *   PROJ_FORCE_RASTER_GROUP=r token tiles per raster group
  *   PROJ_PREFETCH_STAGES=k   weight stages streamed early in PROJ_OVERLAP_WEIGHTS
+ *   PROJ_KPB=1|2             one 64-wide k-block a pipeline stage, or two wherever K allows
+ *                            (default: two for the weight-streaming swapped plans)
+ *   PROJ_INFLIGHT_KB=n       stage bytes a weight-streaming plan keeps in flight per SM
+ *   PROJ_FORCE_CLUSTER=s     cluster split of s CTAs per tile where the clusters fit the SMs
  */
 proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
                           proj_wlayout_t w_layout, proj_dtype_t x_dtype,

@@ -90,7 +90,10 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
         # least 10 % of the SMs busy, fewer than a third as many tiles as SMs,
         # narrow swapped tiles, partials in shared memory.
         assert 2 <= S <= 16 and S <= KT and p["swap_ab"] == 1 and p["block_t"] <= 64
-        assert p["tiles_dp"] == 0 and G == tiles * S and 10 * G >= sms and 3 * tiles < sms
+        # Two k-blocks a stage: S = SMs / tiles >= 2; one: fewer than a third
+        # as many tiles as SMs.
+        assert p["tiles_dp"] == 0 and G == tiles * S and 10 * G >= sms
+        assert (2 * tiles <= sms) if kpb == 2 else (3 * tiles < sms)
         assert p["scratch_bytes"] == 256
     if p["tiles_sk"]:
         assert p["tiles_dp"] % G == 0
@@ -179,16 +182,25 @@ def test_cluster_split_plans():
     # of 16, the largest size.
     p = plan(16, 256, 2 * 8192)
     assert (p["cluster_split"], p["grid"]) == (16, 32)
-    # 64 tiles of the 8192-row decode weight: stream-K over every SM (a split
-    # tile has about 2.4 contributors), as for the 28672-row FFN weight.
-    for N in (8192, 28672):
-        p = plan(16, N, 8192)
-        assert p["cluster_split"] == 0 and p["grid"] == 152
-    # Clusters only below a third of the SMs in tiles: 50 tiles (3·50 < 152)
-    # take clusters of 3 on 150 SMs; 51 tiles stream-K; 45 tiles clusters of 3.
+    # 64 tiles of the 8192-row decode weight (two k-blocks a stage): clusters
+    # of 2 on 128 SMs; the 224 tiles of the 28672-row FFN weight: stream-K
+    # over every SM.
+    p = plan(16, 8192, 8192)
+    assert (p["cluster_split"], p["grid"], p["block_k"]) == (2, 128, 128)
+    p = plan(16, 28672, 8192)
+    assert p["cluster_split"] == 0 and p["grid"] == 152
+    # Two k-blocks a stage: clusters while 2·tiles <= SMs (76 tiles: clusters
+    # of 2; 77 tiles: stream-K; 50 tiles: clusters of 3).
+    assert plan(16, 76 * 128, 8192)["cluster_split"] == 2
+    assert plan(16, 77 * 128, 8192)["cluster_split"] == 0
     assert plan(16, 50 * 128, 8192)["cluster_split"] == 3
-    assert plan(16, 51 * 128, 8192)["cluster_split"] == 0
-    assert plan(16, 45 * 128, 8192)["cluster_split"] == 3
+    # One k-block a stage (K not a multiple of 64): clusters only below a
+    # third of the SMs in tiles: 50 tiles (3·50 < 152) take clusters of 3 on
+    # 150 SMs; 51 tiles stream-K; 45 tiles clusters of 3.
+    assert plan(16, 50 * 128, 8200)["cluster_split"] == 3
+    assert plan(16, 51 * 128, 8200)["cluster_split"] == 0
+    assert plan(16, 45 * 128, 8200)["cluster_split"] == 3
+    assert plan(16, 51 * 128, 8200)["block_k"] == 64
     # Small devices (12 SMs, 3 tiles: clusters of 4; 8 SMs and 2 tiles:
     # clusters of 4; 5 SMs, 1 tile: clusters of 5).
     assert plan(16, 3 * 128, 8192, sm_count=12, smem_optin_bytes=232448)["cluster_split"] == 4

@@ -103,13 +103,17 @@ def test_every_cluster_size(S, M, N, K, layout, bias, yd, half, monkeypatch):
 
 
 def test_handle_keeps_only_clusters_that_fit():
-    # The 8192-row decode projection (64 tiles) runs stream-K on every SM; the
-    # 2048-row one (16 tiles) keeps a cluster split whose clusters all fit at
-    # once.  Whatever split size a handle ends with, its clusters fit together.
+    # The 8192-row decode projection (64 tiles) runs in 64 clusters of 2 (all
+    # resident at once on GB300); the 28672-row FFN weight (224 tiles) runs
+    # stream-K on every SM; the 2048-row one (16 tiles) keeps a cluster split
+    # whose clusters all fit at once.  Whatever split size a handle ends
+    # with, its clusters fit together.
     import torch
     import dense_linear_projection_gb300 as dlp
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     proj = dlp.Projection(16, 8192, 8192, dlp.PROJ_W_NK, dlp.PROJ_BF16, has_bias=True)
+    assert proj.plan["cluster_split"] == 2 and proj.plan["grid"] == 128
+    proj = dlp.Projection(16, 28672, 8192, dlp.PROJ_W_NK, dlp.PROJ_BF16)
     assert proj.plan["cluster_split"] == 0 and proj.plan["grid"] == sms
     p = dlp.Projection(16, 2048, 8192, dlp.PROJ_W_NK, dlp.PROJ_F32).plan
     assert p["cluster_split"] >= 2 and p["grid"] == 16 * p["cluster_split"]

@@ -29,7 +29,7 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("M,N,K,layout,bias,yd", [
-    (16, 8192, 8192, synth.W_NK, True, "bf16"),   # decode shape: stream-K over every SM
+    (16, 8192, 8192, synth.W_NK, True, "bf16"),   # decode shape: clusters of 2
     (16, 2048, 8192, synth.W_NK, False, "f32"),   # 16 tiles split over clusters
     (16, 28672, 1024, synth.W_NK, True, "bf16"),  # 224 tiles: split-K through the scratch
     (3, 520, 1032, synth.W_KN, True, "bf16"),     # [K,N] weights, ragged edges
