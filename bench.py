@@ -383,7 +383,8 @@ def measure_workloads(args, device, peaks: dict) -> dict:
         n_copies = max(2, math.ceil(2 * l2 / w.weight_bytes) + 1)
         proj = dlp.Projection(w.M, w.N, w.K, w.w_layout,
                               dlp.PROJ_F32 if w.y_dtype == "f32" else dlp.PROJ_BF16, w.has_bias,
-                              overlap=dlp.PROJ_OVERLAP_PROLOGUE)
+                              overlap={"none": dlp.PROJ_OVERLAP_NONE, "prologue": dlp.PROJ_OVERLAP_PROLOGUE,
+                                       "weights": dlp.PROJ_OVERLAP_WEIGHTS}[args.overlap])
         Wp = [proj.pack(W0)] + [proj.pack(W0.clone()) for _ in range(n_copies - 1)]
         del W0
         Y = torch.empty((w.M, w.N), dtype=torch.float32 if w.y_dtype == "f32" else torch.bfloat16,
@@ -505,10 +506,11 @@ def run_gpu_arm(args) -> dict:
         raise SystemExit("swiglu runs packed, without bias, on bf16 weights with an even N")
     n_out = w.N // 2 if swiglu else w.N
     Y = torch.empty((w.M, n_out), dtype=y_dt, device=device)
-    # Each step's kernel may start (set-up only) while the previous step
-    # finishes; it touches global memory only after that step completes
-    # (mode "prologue").  Mode "weights" also streams W early, which measured no
-    # faster with packed weights.
+    # Each step's kernel may start its set-up while the previous step
+    # finishes (programmatic dependent launch).  Mode "weights" (the default)
+    # also streams its first weight stages early, which the library does for
+    # plans that occupy every SM; everything else waits for the previous
+    # step to complete.  W is never written by the preceding kernel here.
     overlap = {"none": dlp.PROJ_OVERLAP_NONE, "prologue": dlp.PROJ_OVERLAP_PROLOGUE,
                "weights": dlp.PROJ_OVERLAP_WEIGHTS}[args.overlap]
     proj = dlp.Projection(w.M, w.N, w.K, w.w_layout,
@@ -893,7 +895,7 @@ def parse_args(argv=None):
                     help="seconds of untimed load before timing (clock sampling)")
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
-    ap.add_argument("--overlap", choices=["none", "prologue", "weights"], default="prologue",
+    ap.add_argument("--overlap", choices=["none", "prologue", "weights"], default="weights",
                     help="overlap of consecutive steps (programmatic dependent launch)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -154,10 +154,11 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // a multiple of 32 between 64 and 256.  Chosen for the tensor-bound
     // swapped plans of 256-token tiles that keep at least half of the SMs
     // busy (measured on GB300, 4096 x 8192 x 8192: 359 us on pairs with one
-    // accumulator vs 370 us on single CTAs).  Token-major pairs measured no
-    // faster on the 256 x 12288 x 4096 QKV shape (27.9 vs 27.7 us, whose
-    // time is its weight stream): they are taken only with option 2, which
-    // takes pairs wherever the tile allows them.
+    // accumulator vs 370 us on single CTAs).  Token-major pairs (more than
+    // 128 tokens) are taken with two k-blocks a stage; with one they
+    // measured no faster on the 256 x 12288 x 4096 QKV shape (27.9 vs
+    // 27.7 us), so then only with option 2, which takes pairs wherever the
+    // tile allows them.
     {
         const bool forced = opt.cta_pair == 2;
         const int64_t pairs_max = sms / 2;
@@ -165,7 +166,11 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         if (!forced)
             pair_swapped = pair_swapped && bt == kMaxTokenTile && 2 * bt <= kPairTmemMax &&
                            2 * ceil_div(M, bt) * ceil_div(N, 2 * kBlockA) >= pairs_max;
-        const bool pair_tm = forced && !swap && M > kBlockA && (force_block_n <= 0 || force_block_n % 32 == 0);
+        // Two k-blocks a stage (K a multiple of 64, not turned off): also
+        // token-major pairs by default (see below).
+        const bool kpb2_ok = K % kBlockK == 0 && opt.kpb != 1;
+        const bool pair_tm = (forced || (opt.cta_pair == 1 && kpb2_ok)) && !swap && M > kBlockA &&
+                             (force_block_n <= 0 || force_block_n % 32 == 0);
         if (opt.cta_pair >= 1 && sms >= 2 && (pair_swapped || pair_tm)) {
             int32_t pbt = bt, pbn = bn;
             if (swap) {
@@ -188,8 +193,16 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 }
             }
             const int32_t pb_rows = swap ? pbt : pbn;
-            // Two k-blocks a stage for pairs only when asked (PROJ_KPB=2).
-            const int32_t pkpb = (opt.kpb == 2 && K % kBlockK == 0) ? 2 : 1;
+            // Two k-blocks a stage whenever K allows: each CTA's operands for
+            // a stage come in two TMA ops of 32 KiB instead of two of
+            // 16 KiB, and the per-op pacing of the loads (see the swapped
+            // streaming plans below) had held the tensor pipe back.  Measured
+            // on GB300, packed: 4096 x 8192 x 8192 on swapped pairs 298.5 us
+            // (1842 TFLOP/s) against 350.4 us with one k-block a stage; the
+            // 256 x 12288 x 4096 QKV shape on token-major pairs 27.2 us
+            // against 31.3 us on single CTAs (34.3 us single CTAs with two
+            // k-blocks, whose 80 KiB stages leave room for two).
+            const int32_t pkpb = kpb2_ok ? 2 : 1;
             const int32_t pstage = pkpb * stage_bytes_for(kBlockA, pb_rows / 2);
             int32_t pstages = budget / pstage;
             if (pstages > kMaxStages) pstages = kMaxStages;

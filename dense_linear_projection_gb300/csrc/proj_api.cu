@@ -48,6 +48,7 @@ struct proj_plan_s {
     unsigned long long *trace = nullptr;  // caller's phase-trace buffer, if any
     int overlap = PROJ_OVERLAP_PROLOGUE;    // programmatic dependent launch mode
     int prefetch_stages = kMaxStages;       // PROJ_OVERLAP_WEIGHTS: W stages before the wait
+    bool prefetch_any = false;              // PROJ_PREFETCH_ANY=1: also plans that leave SMs idle
     int sm_count = 0;
     int act = 0;  // fused activation (proj_set_activation)
     // fp32 router weights: planned and run as [H | L] along K (2·kt k-blocks);
@@ -449,6 +450,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     h->y_dtype = y_dtype;
     h->has_bias = has_bias;
     h->plan = plan;
+    if (const char *e = std::getenv("PROJ_PREFETCH_ANY")) h->prefetch_any = std::atoi(e) == 1;  // tuning only
     if (const char *e = std::getenv("PROJ_PREFETCH_STAGES")) {  // tuning only
         const int n = std::atoi(e);
         if (n >= 0 && n <= kMaxStages) h->prefetch_stages = n;
@@ -658,7 +660,8 @@ proj_status_t run_impl(proj_handle_t h, const void *X, const void *W, bool packe
     // idle they would start at once and compete with its weight stream
     // (measured slower on GB300 for the cluster-split and 128-tile plans).
     // (Not with CTA pairs, whose stages are armed by the leader for both.)
-    kp.w_prefetch = h->overlap == PROJ_OVERLAP_WEIGHTS && plan.grid >= h->sm_count && !plan.cta_pair
+    kp.w_prefetch = h->overlap == PROJ_OVERLAP_WEIGHTS && (plan.grid >= h->sm_count || h->prefetch_any) &&
+                            !plan.cta_pair
                         ? h->prefetch_stages
                         : 0;
     TcLaunch l(plan, s, h->overlap != PROJ_OVERLAP_NONE);

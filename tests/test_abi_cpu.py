@@ -78,8 +78,8 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     else:
         assert p["block_t"] == 128 and p["block_n"] % 16 == 0 and 64 <= p["block_n"] <= 256
     # Two 64-wide k-blocks a stage for the weight-streaming swapped plans (at
-    # most 64 tokens, K a multiple of 64), one otherwise.
-    kpb = 2 if (p["swap_ab"] and not pair and p["block_t"] <= 64 and K % 64 == 0) else 1
+    # most 64 tokens) and for CTA pairs, K a multiple of 64; one otherwise.
+    kpb = 2 if (K % 64 == 0 and (pair or (p["swap_ab"] and p["block_t"] <= 64))) else 1
     assert p["block_k"] == 64 * kpb
     assert KT == -(-K // p["block_k"])
     assert 1 <= G <= GB300["sm_count"]
@@ -280,7 +280,8 @@ def test_token_tile_choice():
     assert plan(17, 8192, 8192)["block_t"] == 32
     assert plan(64, 28672, 8192)["block_t"] == 64
     assert plan(4096, 8192, 8192)["block_t"] == 256
-    assert plan(256, 12288, 4096, 1)["block_t"] == 128  # token-major: 128-row token tiles
+    assert plan(256, 12288, 4096, 1)["block_t"] == 256  # token-major pairs: 256 tokens per pair
+    assert plan(256, 12288, 4100, 1)["block_t"] == 128  # one k-block a stage: single CTAs, 128 tokens
 
 
 def test_scratch_and_stages():
@@ -317,10 +318,17 @@ def test_orientation_and_weight_tile_choice():
     for M in (1, 16, 64, 127):
         assert plan(M, 8192, 8192)["swap_ab"] == 1
     # From 128 tokens: tokens on the M side, weight tile sized to fill waves.
+    # The QKV shape (K a multiple of 64, two k-blocks a stage): token-major CTA
+    # pairs of 256 tokens x 192 weight rows, one whole wave of 64 pair tiles.
     qkv = plan(256, 12288, 4096, 1)
-    assert qkv["swap_ab"] == 0 and qkv["block_t"] == 128 and qkv["cta_pair"] == 0
-    assert qkv["block_n"] == 192 and qkv["tiles_m"] * qkv["tiles_n"] == 128
-    assert qkv["tiles_sk"] == 0  # one whole wave (84 % of the SMs) beats splitting
+    assert qkv["swap_ab"] == 0 and qkv["block_t"] == 256 and qkv["cta_pair"] == 1
+    assert qkv["block_n"] == 192 and qkv["tiles_m"] * qkv["tiles_n"] == 64 and qkv["grid"] == 128
+    assert qkv["block_k"] == 128 and qkv["tiles_sk"] == 0
+    # One k-block a stage (K not a multiple of 64): single CTAs of 128 tokens.
+    qkv1 = plan(256, 12288, 4104, 1)
+    assert qkv1["swap_ab"] == 0 and qkv1["block_t"] == 128 and qkv1["cta_pair"] == 0
+    assert qkv1["block_n"] == 192 and qkv1["tiles_m"] * qkv1["tiles_n"] == 128
+    assert qkv1["tiles_sk"] == 0  # one whole wave (84 % of the SMs) beats splitting
     # Many tiles either way (prefill): the swapped 256-token x 128-row tiles.
     # Many tiles either way (prefill): swapped 256-token tiles, on CTA pairs of
     # 2 x 128 weight rows.
@@ -341,12 +349,18 @@ def test_cta_pair_choice():
     assert plan(16, 8192, 8192)["cta_pair"] == 0           # decode: stream-K
     assert plan(100, 1024, 8192)["cta_pair"] == 0          # two 64-token tiles: cluster split
     assert plan(64, 28672, 8192)["cta_pair"] == 0          # weight streaming
-    assert plan(256, 12288, 4096, 1)["cta_pair"] == 0      # token-major: single CTAs
-    assert plan(1024, 4096, 4096)["cta_pair"] == 0         # token-major
+    assert plan(256, 12288, 4096, 1)["cta_pair"] == 1      # token-major, two k-blocks a stage: pairs
+    assert plan(256, 12288, 4104, 1)["cta_pair"] == 0      # token-major, one k-block: single CTAs
+    assert plan(1024, 4096, 4096)["cta_pair"] == 1         # token-major, 64 pair tiles
     p = plan(512, 20480, 256)
     assert (p["cta_pair"], p["swap_ab"], p["block_t"], p["block_n"]) == (1, 1, 256, 256)
     assert p["tiles_m"] * p["tiles_n"] == 160 and p["grid"] == 152
-    # Stages: 16 KiB of A (128 weight rows) plus half of the 256 token rows.
-    assert p["stages"] == 6 and p["smem_bytes"] == 6 * (16384 + 128 * 128) + 25600
-    # A small swapped problem: too few pair tiles for half of the SMs.
-    assert plan(256, 4096, 1024)["cta_pair"] == 0
+    # Stages: two k-blocks of 16 KiB of A (128 weight rows) plus half of the
+    # 256 token rows.
+    assert p["block_k"] == 128
+    assert p["stages"] == 3 and p["smem_bytes"] == 3 * 2 * (16384 + 128 * 128) + 25600
+    # A small problem: with two k-blocks a stage, token-major pairs of 64
+    # weight rows (64 pair tiles on 128 SMs); with one, single CTAs.
+    p = plan(256, 4096, 1024)
+    assert (p["cta_pair"], p["swap_ab"], p["block_t"], p["block_n"], p["grid"]) == (1, 0, 256, 64, 128)
+    assert plan(256, 4096, 1032)["cta_pair"] == 0
