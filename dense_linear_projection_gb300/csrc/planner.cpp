@@ -151,7 +151,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // holds 16 KiB + b_rows/2 rows instead of 16 KiB + b_rows, and each CTA
     // pulls half the weight (token-major) or token (swapped) rows from L2
     // per FLOP.  Whole tiles only, dealt to pairs; the MMA's N side (b_rows)
-    // a multiple of 32 between 64 and 256.  Chosen for the tensor-bound
+    // between 64 and 256, a multiple of 32 (swapped) or 16 (token-major).  Chosen for the tensor-bound
     // swapped plans of 256-token tiles that keep at least half of the SMs
     // busy (measured on GB300, 4096 x 8192 x 8192: 359 us on pairs with one
     // accumulator vs 370 us on single CTAs).  Token-major pairs (more than
@@ -170,7 +170,7 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         // token-major pairs by default (see below).
         const bool kpb2_ok = K % kBlockK == 0 && opt.kpb != 1;
         const bool pair_tm = (forced || (opt.cta_pair == 1 && kpb2_ok)) && !swap && M > kBlockA &&
-                             (force_block_n <= 0 || force_block_n % 32 == 0);
+                             (force_block_n <= 0 || force_block_n % 16 == 0);
         if (opt.cta_pair >= 1 && sms >= 2 && (pair_swapped || pair_tm)) {
             int32_t pbt = bt, pbn = bn;
             if (swap) {
@@ -179,10 +179,12 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 pbt = 2 * kBlockA;
                 if (force_block_n <= 0) {
                     // As for single CTAs: per-pair time ~ waves x (block_n +
-                    // a fixed share); the widest block_n wins ties.
+                    // a fixed share); the widest block_n wins ties.  Steps of
+                    // 16 (each CTA holds half, a multiple of 8 rows): the QKV
+                    // shape's 12288 rows fill 70 of 76 pairs at 176.
                     const int64_t tiles_m = ceil_div(M, pbt);
                     int64_t best_cost = -1;
-                    for (int32_t cand = kMaxTokenTile; cand >= 64; cand -= 32) {
+                    for (int32_t cand = kMaxTokenTile; cand >= 64; cand -= 16) {
                         const int64_t waves = ceil_div(tiles_m * ceil_div(N, cand), pairs_max);
                         const int64_t cost = waves * (cand + 32);
                         if (best_cost < 0 || cost < best_cost) {

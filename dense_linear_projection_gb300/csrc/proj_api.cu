@@ -421,6 +421,7 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
             plan.tiles_dp += plan.tiles_sk;
             plan.tiles_sk = 0;
             plan.units_sk = 0;
+            if (plan.tiles_dp < plan.grid) plan.grid = static_cast<int32_t>(plan.tiles_dp);  // no idle CTAs
         }
     }
     if (const char *e = std::getenv("PROJ_FORCE_STAGES")) {  // tuning only

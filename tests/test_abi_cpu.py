@@ -67,10 +67,10 @@ def check_decomposition(p, M, N, K, sms=GB300["sm_count"]):
     pair = p["cta_pair"]
     if pair:
         # CTA pairs: 256 rows on the MMA's M side (two CTAs of 128), the N
-        # side a multiple of 32 in [64, 256] split in halves; whole tiles
-        # dealt to pairs, two CTAs each.
+        # side in [64, 256] split in halves, a multiple of 32 (swapped) or 16
+        # (token-major); whole tiles dealt to pairs, two CTAs each.
         a, b = ("block_n", "block_t") if p["swap_ab"] else ("block_t", "block_n")
-        assert p[a] == 256 and p[b] % 32 == 0 and 64 <= p[b] <= 256
+        assert p[a] == 256 and p[b] % (32 if p["swap_ab"] else 16) == 0 and 64 <= p[b] <= 256
         assert p["cluster_split"] == 0 and p["tiles_sk"] == 0 and p["scratch_bytes"] == 256
         assert G % 2 == 0 and G == 2 * min(tiles, sms // 2)
     elif p["swap_ab"]:
@@ -319,10 +319,10 @@ def test_orientation_and_weight_tile_choice():
         assert plan(M, 8192, 8192)["swap_ab"] == 1
     # From 128 tokens: tokens on the M side, weight tile sized to fill waves.
     # The QKV shape (K a multiple of 64, two k-blocks a stage): token-major CTA
-    # pairs of 256 tokens x 192 weight rows, one whole wave of 64 pair tiles.
+    # pairs of 256 tokens x 176 weight rows, one whole wave of 70 pair tiles.
     qkv = plan(256, 12288, 4096, 1)
     assert qkv["swap_ab"] == 0 and qkv["block_t"] == 256 and qkv["cta_pair"] == 1
-    assert qkv["block_n"] == 192 and qkv["tiles_m"] * qkv["tiles_n"] == 64 and qkv["grid"] == 128
+    assert qkv["block_n"] == 176 and qkv["tiles_m"] * qkv["tiles_n"] == 70 and qkv["grid"] == 140
     assert qkv["block_k"] == 128 and qkv["tiles_sk"] == 0
     # One k-block a stage (K not a multiple of 64): single CTAs of 128 tokens.
     qkv1 = plan(256, 12288, 4104, 1)
@@ -336,12 +336,12 @@ def test_orientation_and_weight_tile_choice():
     assert (pre["swap_ab"], pre["block_t"], pre["block_n"], pre["tiles_sk"]) == (1, 256, 256, 0)
     assert pre["cta_pair"] == 1 and pre["tmem_cols"] == 512 and pre["grid"] == 152
     # [K,N] weights load in 64-row boxes: the weight tile of a single-CTA plan
-    # is a multiple of 64.  A pair's tile is a multiple of 32 (the handle runs
+    # is a multiple of 64.  A pair's tile is a multiple of 16 (the handle runs
     # weights as stored on a single-CTA plan when the halves are not whole
     # boxes; packed weights have no such limit).
     for N in (1000, 3000, 9000):  # few enough weight rows that swapped tiles leave SMs idle
         p = plan(300, N, 1024, 1)
-        assert p["swap_ab"] == 0 and p["block_n"] % (32 if p["cta_pair"] else 64) == 0
+        assert p["swap_ab"] == 0 and p["block_n"] % (16 if p["cta_pair"] else 64) == 0
 
 
 def test_cta_pair_choice():
