@@ -722,7 +722,7 @@ def run_gpu_arm(args) -> dict:
                "h2d_bytes_per_step": 2 * w.M * w.K, "d2h_bytes_per_step": ybytes,
                "us_per_step": e_agg["seconds"] / args.steps * 1e6,
                "path": ("proj_run_host_packed" if args.packed else "proj_run_host")
-                       + " per step (X H2D, kernel, Y D2H; W resident)"}
+                       + " per step (X H2D by a copy kernel; Y written to pinned host by the epilogue; W resident)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -766,6 +766,9 @@ proj_status_t run_host_impl(proj_handle_t h, const void *X_host, const void *W, 
     void *y_dev = host_device_pointer(Y_host);
     proj_status_t st = copy_host(h->stage_x, x_dev, h->stage_x, X_host, xb, cudaMemcpyHostToDevice, h->sm_count, s);
     if (st != PROJ_OK) return st;
+    // A device-addressable, 16-byte aligned Y is written by the projection's
+    // own epilogue, through its device address (no staging, no copy kernel).
+    if (y_dev && aligned16(y_dev)) return run_impl(h, h->stage_x, W, packed, bias, nullptr, y_dev, stream);
     st = run_impl(h, h->stage_x, W, packed, bias, nullptr, h->stage_y, stream);
     if (st != PROJ_OK) return st;
     return copy_host(y_dev, h->stage_y, Y_host, h->stage_y, yb, cudaMemcpyDeviceToHost, h->sm_count, s);

@@ -338,10 +338,13 @@ proj_status_t proj_run_host_packed(proj_handle_t h, const void *X_host, const vo
  * Same projection with HOST activations: copies X_host ([M,K] bf16) to a
  * device staging buffer, runs, and copies Y back to Y_host, all on `stream`.
  * W and bias stay device pointers (weights are resident, as after a
- * preparation step).  Pinned or registered host buffers (16-byte aligned) are
- * copied by small kernels chained to the projection by programmatic dependent
- * launch; other host memory by cudaMemcpyAsync (asynchronous only when
- * pinned).  Y_host is valid once `stream` has been synchronised.  The staging
+ * preparation step).  A pinned or registered X_host (16-byte aligned) is
+ * copied by a small kernel chained to the projection by programmatic
+ * dependent launch; a pinned or registered Y_host (16-byte aligned) is written
+ * by the projection's epilogue itself, through its device address, with no
+ * staging copy.  Other host memory goes through cudaMemcpyAsync and the
+ * staging buffers (asynchronous only when pinned).  Y_host is valid once
+ * `stream` has been synchronised.  The staging
  * buffers are allocated by the first call on a handle (so that first call is
  * not capturable) and reused afterwards.
  */

@@ -388,10 +388,13 @@ def test_handles_with_different_rings_in_any_creation_order():
 
 @pytest.mark.parametrize("M,N,K,yd", [(16, 1024, 2048, "bf16"), (5, 1001, 520, "f32"), (3, 999, 256, "bf16")])
 def test_run_host_copy_paths(M, N, K, yd):
-    # Pinned host buffers go through the copy kernels (chained to the
-    # projection by programmatic dependent launch); pageable or unaligned
-    # ones through cudaMemcpyAsync.  Odd N leaves a Y tail that is not a
-    # whole 16-byte chunk.  Every path gives the device run's bits.
+    # A pinned X goes through the copy kernel (chained to the projection by
+    # programmatic dependent launch) and a pinned Y is written by the
+    # projection's epilogue through its device address; pageable or
+    # unaligned buffers go through cudaMemcpyAsync and the staging buffers.
+    # Mixed cases take one route for X and the other for Y.  Odd N leaves a
+    # Y tail that is not a whole 16-byte chunk.  Every path gives the device
+    # run's bits.
     import torch
     import dense_linear_projection_gb300 as dlp
     w = synth.Workload("t", M, N, K, synth.W_NK, True, yd, 14)
@@ -408,7 +411,8 @@ def test_run_host_copy_paths(M, N, K, yd):
     Yu_buf = torch.empty(M * N + 8, dtype=dt).pin_memory()
     Xu, Yu = Xu_buf[1:1 + M * K].view(M, K), Yu_buf[1:1 + M * N].view(M, N)
     Xu.copy_(xh)
-    cases = [("pinned", Xp, Yp), ("pageable", xh.clone(), torch.empty((M, N), dtype=dt)), ("unaligned", Xu, Yu)]
+    cases = [("pinned", Xp, Yp), ("pageable", xh.clone(), torch.empty((M, N), dtype=dt)), ("unaligned", Xu, Yu),
+             ("pinned Y only", xh.clone(), Yp), ("pinned X only", Xp, torch.empty((M, N), dtype=dt))]
     for name, Xh, Yh in cases:
         Yh.zero_()
         dlp.proj_run_host(proj.handle, Xh, W, b, Yh, s)
@@ -420,8 +424,8 @@ def test_run_host_copy_paths(M, N, K, yd):
 def test_run_host_back_to_back_calls_keep_their_inputs():
     # Eight host-buffer calls in a row on one stream, with no synchronisation
     # between them: each call's X reaches the shared staging buffer only after
-    # the previous projection has read its own, and each Y leaves before the
-    # next projection overwrites the staging output.
+    # the previous projection has read its own, and each call's Y lands in
+    # its own pinned buffer.
     import torch
     import dense_linear_projection_gb300 as dlp
     w = synth.Workload("t", 16, 2048, 4096, synth.W_NK, True, "bf16", 15)
