@@ -628,28 +628,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t x_off = p.swap ? a_bytes * static_cast<uint32_t>(p.kpb) : 0u;
     const uint32_t w_blk = p.swap ? a_bytes : b_bytes;  // one k-block's W bytes
 
-    if (threadIdx.x == 0) {
-        trace_stamp(p, kTraceEntry);
-        for (int s = 0; s < stages; ++s) {
-            mbar_init(smem_u32(&ctl->full[s]), 1);
-            mbar_init(smem_u32(&ctl->empty[s]), 1);
+    if (threadIdx.x == 0) trace_stamp(p, kTraceEntry);
+    if (warp == 2) {
+        // Barrier set-up, a few barriers per lane of an epilogue warp (idle
+        // until the first accumulator), while the producer lane works out its
+        // first segment below.
+        for (int st = lane; st < stages; st += 32) {
+            mbar_init(smem_u32(&ctl->full[st]), 1);
+            mbar_init(smem_u32(&ctl->empty[st]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+        if (lane < 2) {
+            mbar_init(smem_u32(&ctl->acc_full[lane]), 1);
             // Pairs: the leader's accumulator is free once both CTAs' epilogue
             // warps have read their halves.
-            mbar_init(smem_u32(&ctl->acc_empty[b]), (kPair ? 2 : 1) * kEpilogueThreads / 32);
+            mbar_init(smem_u32(&ctl->acc_empty[lane]), (kPair ? 2 : 1) * kEpilogueThreads / 32);
+        } else if (lane == 2) {
+            mbar_init(smem_u32(&ctl->drain), 1);
+            ctl->abort_flag = 0;
+        } else if (lane >= 4 && lane < 8 && p.cluster_split > 1) {
+            mbar_init(smem_u32(&ctl->ready[lane - 4]), static_cast<uint32_t>(32 * (p.cluster_split - 1)));
         }
-        mbar_init(smem_u32(&ctl->drain), 1);
-        if (p.cluster_split > 1)
-            for (int qq = 0; qq < 4; ++qq)
-                mbar_init(smem_u32(&ctl->ready[qq]), static_cast<uint32_t>(32 * (p.cluster_split - 1)));
-        ctl->abort_flag = 0;
         fence_barrier_init();
     }
+    // The producer's cache policies and first segment.  This single-lane
+    // integer work (the work iterator alone takes about 0.5 µs) runs during
+    // set-up instead of between set-up and the first load, where it had
+    // delayed the CTAs that start only as the preceding kernel's leave.
+    uint64_t pol_w = 0, pol_x = 0;
+    WorkIter prod_it;
+    Segment prod_s;
+    bool prod_more = false;
+    int32_t prod_tm = 0, prod_tn = 0;
     if (warp == 0 && lane == 0) {
         tma_prefetch_map(&tmap_w);
         tma_prefetch_map(&tmap_x);
+        // W is evict-first even where several token tiles reuse a weight
+        // panel: the raster order runs those tiles in the same wave, in step
+        // along K, so a panel's k-block is shared while it is in L2 anyway,
+        // and evicting it first keeps more of the raster group's token panels
+        // for the next wave.  (4096 x 8192 x 8192 on GB300: 460-540 MB of
+        // DRAM traffic a launch against 545-550 MB with evict-normal, same
+        // time.)
+        pol_w = l2_policy_evict_first();
+        pol_x = l2_policy_evict_last();  // X is reread by every CTA
+        prod_it.init(p, cta);
+        prod_more = prod_it.next(p, prod_s);
+        if (prod_more) tile_coords(p, prod_s.tile, prod_tm, prod_tn);
     }
     if (warp == 1) {
         tmem_alloc<kPair>(smem_u32(&ctl->tmem_base), static_cast<uint32_t>(p.tmem_cols));
@@ -697,15 +721,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            // W is evict-first even where several token tiles reuse a weight
-            // panel: the raster order runs those tiles in the same wave, in
-            // step along K, so a panel's k-block is shared while it is in L2
-            // anyway, and evicting it first keeps more of the raster group's
-            // token panels for the next wave.  (4096 x 8192 x 8192 on GB300:
-            // 460-540 MB of DRAM traffic a launch against 545-550 MB with
-            // evict-normal, same time.)
-            const uint64_t pol_w = l2_policy_evict_first();
-            const uint64_t pol_x = l2_policy_evict_last();   // X is reread by every CTA
             const uint32_t stage_bytes = static_cast<uint32_t>(p.stage_bytes);
             // CTA pairs: this CTA's halves of the tile's weight and token rows.
             const int32_t w_row_off = static_cast<int32_t>(pair_rank) * (p.block_n / 2);
@@ -760,17 +775,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             int64_t pre = 0;
             if (!kPair && p.w_prefetch > 0) {
                 const int32_t pre_max = min(p.w_prefetch, stages);
-                WorkIter it;
-                it.init(p, cta);
-                Segment s;
-                while (pre < pre_max && it.next(p, s)) {
-                    int32_t tm, tn;
-                    tile_coords(p, s.tile, tm, tn);
+                WorkIter it = prod_it;  // from the first segment onwards
+                Segment s = prod_s;
+                int32_t tn = prod_tn;
+                bool more = prod_more;
+                while (pre < pre_max && more) {
                     for (int32_t kb = s.kb0; kb < s.kb1 && pre < pre_max; ++kb) {
                         const uint32_t full = smem_u32(&ctl->full[pre]);
                         mbar_arrive_expect_tx(full, stage_bytes);  // W + X bytes of the stage
                         load_w(base_addr + static_cast<uint32_t>(pre) * stage_bytes + w_off, full, tn, kb);
                         ++pre;
+                    }
+                    if (pre < pre_max) {
+                        more = it.next(p, s);
+                        int32_t tm_unused;
+                        if (more) tile_coords(p, s.tile, tm_unused, tn);
                     }
                 }
                 if (pre > 0) trace_stamp(p, kTraceFirstLoad);
@@ -790,13 +809,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             int32_t stage = 0;
             uint32_t phase = 0;
-            WorkIter it;
-            it.init(p, cta);
-            Segment s;
+            WorkIter &it = prod_it;
+            Segment &s = prod_s;
+            int32_t tm = prod_tm, tn = prod_tn;
+            bool more = prod_more;
             bool ok = true;
-            while (ok && it.next(p, s)) {
-                int32_t tm, tn;
-                tile_coords(p, s.tile, tm, tn);
+            while (ok && more) {
                 for (int32_t kb = s.kb0; kb < s.kb1; ++kb) {
                     const uint32_t full = full_bar(stage);
                     const uint32_t st_base = base_addr + stage * stage_bytes;
@@ -833,6 +851,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         phase ^= 1u;
                     }
                 }
+                if (!ok) break;
+                more = it.next(p, s);
+                if (more) tile_coords(p, s.tile, tm, tn);
             }
             if (issued < pre) issued = pre;  // stages armed by the prefetch (abort drain)
             trace_stamp(p, kTraceLastLoad);
