@@ -66,7 +66,8 @@ class PlanDesc(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in (
         "kernel", "block_n", "block_t", "block_k", "stages", "grid", "threads", "smem_bytes",
         "tmem_cols", "raster_group", "swap_ab", "cluster_split", "cta_pair")] + [(name, ctypes.c_int64) for name in (
-        "tiles_m", "tiles_n", "k_blocks", "tiles_dp", "tiles_sk", "units_sk", "scratch_bytes")]
+        "tiles_m", "tiles_n", "k_blocks", "tiles_dp", "tiles_sk", "units_sk", "scratch_bytes")] + [
+        ("cluster_groups", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -339,6 +339,13 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
         plain.tm_cluster = 0;
         return plan_compute(M, N, K, w_layout, y_dtype, has_bias, dev, plain, out);
     }
+    // Several clusters per tile (forced with option cluster_groups): the G
+    // clusters of S CTAs split the tile's K range into G·S parts; their
+    // sums meet in the scratch.  Swapped splits only.
+    int32_t G = 1;
+    if (S >= 2 && swap && !tm_cluster && opt.cluster_groups >= 2 &&
+        int64_t(opt.cluster_groups) * S * tiles <= sms && int64_t(opt.cluster_groups) * S <= out->k_blocks)
+        G = opt.cluster_groups;
     // The peers' partial sums get their own shared memory after the ring.
     const int32_t red_bytes = red_for(S);
     if (stages * stage + red_bytes > budget) stages = (budget - red_bytes) / stage;
@@ -347,7 +354,8 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     const int64_t fill_pct = swap ? 95 : 80;
     if (S >= 2) {
         out->cluster_split = S;
-        out->grid = static_cast<int32_t>(tiles * S);
+        out->cluster_groups = G;
+        out->grid = static_cast<int32_t>(tiles * S * G);
         out->tiles_sk = tiles;
     } else if (rem == 0 || 100 * tiles >= fill_pct * waves * grid) {
         out->tiles_sk = 0;
@@ -385,9 +393,12 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
     // Scratch: one partial tile per (CTA, first|last split segment), one
     // completion counter per (split tile, 32-row quarter), and the device
     // status word.
+    // (Clusters of a split over several clusters per tile: one partial tile
+    // per (tile, cluster).)
     int64_t partial_bytes = 0;
     if (out->tiles_sk > 0 && S < 2) partial_bytes = 2 * grid * int64_t(kBlockA) * b_rows * 4;
-    const int64_t counter_bytes = S < 2 ? ((out->tiles_sk * 4 * 4 + 255) / 256) * 256 : 0;
+    if (S >= 2 && G >= 2) partial_bytes = out->tiles_sk * G * int64_t(kBlockA) * b_rows * 4;
+    const int64_t counter_bytes = (S < 2 || G >= 2) ? ((out->tiles_sk * 4 * 4 + 255) / 256) * 256 : 0;
     out->scratch_bytes = partial_bytes + counter_bytes + 256;
     (void)has_bias;
     return PROJ_OK;
@@ -447,15 +458,19 @@ extern "C" proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan,
     const int32_t ts = static_cast<int32_t>(split_tile);
     const int32_t kt = static_cast<int32_t>(plan->k_blocks);
     if (plan->cluster_split > 1) {
-        // Cluster split: ranks 0..S-1 of the tile's cluster, added in rank
-        // order in distributed shared memory (no global slot).
+        // Cluster split: parts 0..P-1 of the tile (P = G·S), in K order.
+        // Each cluster adds its S ranks in rank order in distributed shared
+        // memory (slot -1 with one cluster per tile); with G clusters per
+        // tile, cluster g's sum goes to scratch slot ts·G + g, and the G sums
+        // are added in group order.
         const int32_t S = plan->cluster_split;
-        for (int32_t r = 0; r < S; ++r)
+        const int32_t G = plan->cluster_groups > 1 ? plan->cluster_groups : 1;
+        for (int32_t r = 0; r < G * S; ++r)
             if (r < cap) {
-                ctas[r] = ts * S + r;
-                slots[r] = -1;
+                ctas[r] = ts * G * S + r;
+                slots[r] = G > 1 ? ts * G + r / S : -1;
             }
-        *count = S;
+        *count = G * S;
         return PROJ_OK;
     }
     int32_t first, last;
@@ -484,12 +499,12 @@ int plan_to_json(const proj_plan_desc_t &p, int64_t M, int64_t N, int64_t K, int
         "{\"kernel\": \"%s\", \"M\": %lld, \"N\": %lld, \"K\": %lld, \"w_layout\": \"%s\", "
         "\"y_dtype\": \"%s\", \"bias\": %s, \"block_n\": %d, \"block_t\": %d, \"block_k\": %d, "
         "\"stages\": %d, \"grid\": %d, \"threads\": %d, \"smem_bytes\": %d, "
-        "\"tmem_cols\": %d, \"raster_group\": %d, \"swap_ab\": %d, \"cluster_split\": %d, \"cta_pair\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
+        "\"tmem_cols\": %d, \"raster_group\": %d, \"swap_ab\": %d, \"cluster_split\": %d, \"cluster_groups\": %d, \"cta_pair\": %d, \"tiles_m\": %lld, \"tiles_n\": %lld, \"k_blocks\": %lld, "
         "\"tiles_dp\": %lld, \"tiles_sk\": %lld, \"units_sk\": %lld, \"scratch_bytes\": %lld}",
         kname, (long long)M, (long long)N, (long long)K, w_layout == PROJ_W_NK ? "NK" : "KN",
         y_dtype == PROJ_F32 ? "f32" : "bf16", has_bias ? "true" : "false", p.block_n,
         p.block_t, p.block_k, p.stages, p.grid, p.threads, p.smem_bytes, p.tmem_cols, p.raster_group,
-        p.swap_ab, p.cluster_split, p.cta_pair,
+        p.swap_ab, p.cluster_split, p.cluster_groups, p.cta_pair,
         (long long)p.tiles_m, (long long)p.tiles_n, (long long)p.k_blocks,
         (long long)p.tiles_dp, (long long)p.tiles_sk, (long long)p.units_sk,
         (long long)p.scratch_bytes);

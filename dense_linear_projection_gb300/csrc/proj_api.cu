@@ -211,6 +211,8 @@ bool loads_stored_kn(const proj_plan_desc_t &plan) { return w_box_rows(plan) % 6
 // the status word).  Cluster-split plans reduce in shared memory: none.
 int64_t partial_bytes_of(const proj_plan_desc_t &plan) {
     const int64_t b_rows = plan.swap_ab ? plan.block_t : plan.block_n;
+    if (plan.tiles_sk > 0 && plan.cluster_split >= 2 && plan.cluster_groups >= 2)
+        return plan.tiles_sk * plan.cluster_groups * kBlockA * b_rows * 4;  // one per (tile, cluster)
     return plan.tiles_sk > 0 && plan.cluster_split < 2 ? int64_t(2) * plan.grid * kBlockA * b_rows * 4 : 0;
 }
 
@@ -267,10 +269,14 @@ proj_status_t plan_fitted(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_layo
         if (st != PROJ_OK || plan->cluster_split < 2) return st;
         TcLaunch l(*plan, nullptr, false);
         int clusters = 0;
-        if (tc_max_active_clusters(&clusters, &l.cfg) == cudaSuccess &&
-            static_cast<int64_t>(clusters) >= plan->tiles_sk)
+        const int64_t need = plan->tiles_sk * (plan->cluster_groups > 1 ? plan->cluster_groups : 1);
+        if (tc_max_active_clusters(&clusters, &l.cfg) == cudaSuccess && static_cast<int64_t>(clusters) >= need)
             return PROJ_OK;
         cudaGetLastError();
+        if (plan->cluster_groups > 1) {  // first one cluster per tile
+            opt.cluster_groups = 1;
+            continue;
+        }
         opt.max_cluster = plan->cluster_split - 1;
         opt.force_cluster = 0;  // a forced size that does not fit falls back to the rule
         if (opt.max_cluster < 2) opt.max_cluster = 0;
@@ -392,6 +398,10 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
     if (const char *e = std::getenv("PROJ_FORCE_CLUSTER")) {
         const int c = std::atoi(e);
         if (c >= 2 && c <= kMaxClusterSplit) opt.force_cluster = c;
+    }
+    if (const char *e = std::getenv("PROJ_CLUSTER_GROUPS")) {  // tuning only
+        const int g = std::atoi(e);
+        if (g >= 1 && g <= 16) opt.cluster_groups = g;
     }
     // fp32 weights: the reduction runs over [H | L], twice the k-blocks of K.
     // A stage must not straddle the halves (its X k-blocks are contiguous):

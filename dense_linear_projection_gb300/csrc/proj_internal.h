@@ -100,6 +100,10 @@ struct PlanOptions {
     // tokens whenever the clusters fit the SMs (PROJ_FORCE_CLUSTER; 0: the
     // planner's rule).
     int32_t force_cluster = 0;
+    // Clusters per tile of a swapped cluster split (PROJ_CLUSTER_GROUPS): 0
+    // lets the planner choose, 1 forces one, G >= 2 forces G where the G·S
+    // CTAs of every tile fit the SMs.
+    int32_t cluster_groups = 0;
     // Stage bytes per SM a weight-streaming plan keeps in flight
     // (PROJ_INFLIGHT_KB).
     int32_t inflight_bytes = kInflightTarget;
@@ -149,6 +153,7 @@ struct KernelParams {
     int32_t y_f32;         // store fp32 (else bf16)
     int32_t y_vec;         // Y rows start 16-byte aligned (N·size % 16 == 0, aligned base)
     int64_t wait_limit_ns; // bounded device waits give up after this long
+    int32_t cluster_groups; // cluster split: clusters per tile (their sums meet in scratch), else 1
     int32_t w_prefetch;    // stages of W streamed before the preceding kernel completes (0: none)
     int32_t act;           // fused activation: 0 none, 1 GELU (on projection + bias), 2 SwiGLU
     int32_t ldy;           // Y row stride in elements: N, or N / 2 for SwiGLU (gate and up rows stacked)
@@ -236,15 +241,16 @@ struct WorkIter {
     PROJ_HD void init(const KernelParams &p, int32_t c) {
         cta = c;
         if (p.cluster_split > 1) {
-            // One segment: rank c % S of tile c / S, an integer share of K.
-            // (32-bit divisions: a 64-bit one here, on its first run in each
-            // CTA, had put 0.7 µs between set-up and the first weight load.)
-            const int32_t S = p.cluster_split;
-            const int32_t r = c % S;
+            // One segment: part c % P of tile c / P, an integer share of K,
+            // with P = G·S parts per tile (G clusters of S CTAs; cluster
+            // c / S is group (c / S) % G of its tile, rank c % S of it).
+            const int32_t P = p.cluster_split * (p.cluster_groups > 1 ? p.cluster_groups : 1);
+            const int32_t part = c % P;
+            const int32_t tile = c / P;
             dp_next = -1;
-            u = static_cast<int64_t>(c / S) * p.k_blocks + div_nonneg(static_cast<int64_t>(r) * p.k_blocks, S);
-            u_end = static_cast<int64_t>(c / S) * p.k_blocks + div_nonneg(static_cast<int64_t>(r + 1) * p.k_blocks, S);
-            first_sk_tile = c / S;
+            u = static_cast<int64_t>(tile) * p.k_blocks + div_nonneg(static_cast<int64_t>(part) * p.k_blocks, P);
+            u_end = static_cast<int64_t>(tile) * p.k_blocks + div_nonneg(static_cast<int64_t>(part + 1) * p.k_blocks, P);
+            first_sk_tile = tile;
             return;
         }
         dp_next = c;
@@ -351,6 +357,7 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.sk_pair = plan.grid > 0 && plan.units_sk / plan.grid >= plan.k_blocks;
     kp.sk_dense = plan.units_sk >= plan.grid;
     kp.cluster_split = plan.cluster_split;
+    kp.cluster_groups = plan.cluster_split > 1 && plan.cluster_groups > 1 ? plan.cluster_groups : 1;
     if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;
     kp.stages = plan.stages;
     kp.a_rows = plan_a_rows(plan);

@@ -1422,6 +1422,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          kErrWaitEpilogue, p.wait_limit_ns)) {
                         if (stamp_split) trace_stamp(p, kTraceSplitReady);
                         if (warp == 2 && lane == 0) ++reductions;
+                        // Several clusters per tile: this cluster's sum of the
+                        // quarter goes to its scratch slot [tile·G + group]
+                        // (laid out like a split tile's partial) instead of Y.
+                        const int32_t G = p.cluster_groups;
+                        const int32_t grp = (cta / static_cast<int32_t>(S)) % G;
+                        float *mine = G > 1 ? p.partials + (static_cast<size_t>(s.tile * G + grp) * kBlockA + r) * p.b_rows
+                                            : nullptr;
                         for (int32_t ch = 0; ch < nchunks; ++ch) {
                             float own[16], acc[16];
                             tmem_load16(tbase + ch * 16, own);
@@ -1444,7 +1451,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     acc[4 * i + 3] += o.w;
                                 }
                             }
-                            store_chunk(ch, acc);
+                            if (G > 1) {
+                                float4 *dst = reinterpret_cast<float4 *>(mine + ch * 16);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
+                            } else {
+                                store_chunk(ch, acc);
+                            }
+                        }
+                        if (G > 1) {
+                            // One acquire-release add per (tile, quarter) and
+                            // cluster: it releases this warp's sums (ordered
+                            // before it by the __syncwarp) and, for the cluster
+                            // that completes last, acquires the others'.  That
+                            // one adds the G sums in group order, starting
+                            // from group 0's, so the bits do not depend on
+                            // which cluster completes last.
+                            __syncwarp();
+                            int last = 0;
+                            uint32_t *ctr = p.counters + static_cast<size_t>(s.tile) * 4 + q;
+                            if (lane == 0) {
+                                const uint32_t old = atom_add_acq_rel_gpu(ctr, 1u);
+                                last = (old == static_cast<uint32_t>(G - 1)) ? 1 : 0;
+                                if (last) store_relaxed_gpu(ctr, 0u);  // fresh for the next run
+                            }
+                            last = __shfl_sync(0xFFFFFFFFu, last, 0);
+                            __syncwarp();
+                            if (last) {
+                                const float *g0 = p.partials + (static_cast<size_t>(s.tile * G) * kBlockA + r) * p.b_rows;
+                                const size_t gstride = static_cast<size_t>(kBlockA) * p.b_rows;
+                                for (int32_t ch = 0; ch < nchunks; ++ch) {
+                                    float sum[16];
+                                    float4 o[4];
+                                    load_partial16(g0, ch, o);
+#pragma unroll
+                                    for (int i = 0; i < 4; ++i) {
+                                        sum[4 * i] = o[i].x;
+                                        sum[4 * i + 1] = o[i].y;
+                                        sum[4 * i + 2] = o[i].z;
+                                        sum[4 * i + 3] = o[i].w;
+                                    }
+                                    for (int32_t gg = 1; gg < G; ++gg) {
+                                        load_partial16(g0 + static_cast<size_t>(gg) * gstride, ch, o);
+#pragma unroll
+                                        for (int i = 0; i < 4; ++i) {
+                                            sum[4 * i] += o[i].x;
+                                            sum[4 * i + 1] += o[i].y;
+                                            sum[4 * i + 2] += o[i].z;
+                                            sum[4 * i + 3] += o[i].w;
+                                        }
+                                    }
+                                    store_chunk(ch, sum);
+                                }
+                            }
                         }
                         if (stamp_split) trace_stamp(p, kTraceSplitStored);
                     }

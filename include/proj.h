@@ -158,6 +158,13 @@ typedef struct proj_plan_desc {
     int64_t tiles_sk;        /* tiles split along K across CTAs */
     int64_t units_sk;        /* tiles_sk * k_blocks */
     int64_t scratch_bytes;   /* device scratch the handle owns */
+    int32_t cluster_groups;  /* with cluster_split S >= 2: 0 or 1, one cluster per tile; G >= 2,
+                                each tile's K range is split over G clusters of S CTAs (grid =
+                                tiles_sk * G * S; CTA c: tile c / (G·S), part p = c % (G·S),
+                                k-blocks [⌊p·k_blocks/(G·S)⌋, ⌊(p+1)·k_blocks/(G·S)⌋)).  Each
+                                cluster adds its ranks' partial sums in rank order; the G
+                                cluster sums meet in the handle's scratch and the cluster that
+                                completes last adds them in group order */
 } proj_plan_desc_t;
 
 /*
@@ -200,8 +207,10 @@ proj_status_t proj_plan_segments(const proj_plan_desc_t *plan, int32_t cta, proj
  * (0 ≤ split_tile < tiles_sk; tile index tiles_dp + split_tile) are added:
  * contributing CTAs in ascending order with their partial-sum slots.  Writes
  * min(cap, total) pairs and the total to *count.  For a cluster split the
- * CTAs are the tile's cluster ranks, split_tile·S .. split_tile·S + S − 1,
- * each with slot −1.
+ * CTAs are the tile's parts, split_tile·P .. split_tile·P + P − 1 (P = G·S,
+ * G = max(1, cluster_groups)), each with slot −1 when G = 1, else with its
+ * cluster's scratch slot split_tile·G + (part / S): each cluster adds its
+ * ranks in rank order, then the G cluster sums are added in group order.
  */
 proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t split_tile,
                                         int32_t *ctas, int32_t *slots, int64_t cap,
@@ -245,6 +254,7 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
  *                            (default: two for the weight-streaming swapped plans)
  *   PROJ_INFLIGHT_KB=n       stage bytes a weight-streaming plan keeps in flight per SM
  *   PROJ_FORCE_CLUSTER=s     cluster split of s CTAs per tile where the clusters fit the SMs
+ *   PROJ_CLUSTER_GROUPS=g    g clusters per tile for a swapped cluster split (1: one)
  */
 proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
                           proj_wlayout_t w_layout, proj_dtype_t x_dtype,

@@ -172,6 +172,33 @@ def test_plans_of_the_workloads(M, N, K, layout):
     check_decomposition(p, M, N, K)
 
 
+def test_cluster_group_decomposition():
+    # Several clusters per tile: the 16 tiles of the 2048-row decode weight
+    # as 2 clusters of 4 each (128 CTAs).  CTA c takes part c % 8 of tile
+    # c // 8, K split into 8 integer shares; every (tile, k-block) is covered
+    # once; the reduction order lists the 8 parts in K order with their
+    # cluster's scratch slot (tile·2 + part // 4).
+    p = dict(plan(16, 2048, 8192))
+    KT = p["k_blocks"]
+    S, G = 4, 2
+    p.update(cluster_split=S, cluster_groups=G, grid=16 * S * G)
+    cover = np.zeros((16, KT), dtype=np.int32)
+    for c in range(p["grid"]):
+        segs = dlp.proj_plan_segments(p, c)
+        assert len(segs) == 1
+        tile, tm, tn, kb0, kb1, slot, split = segs[0]
+        part = c % (S * G)
+        assert (tile, kb0, kb1, slot, split) == (c // (S * G), part * KT // (S * G), (part + 1) * KT // (S * G), -1, 1)
+        cover[tile, kb0:kb1] += 1
+    assert (cover == 1).all()
+    for ts in (0, 7, 15):
+        assert dlp.proj_plan_reduction_order(p, ts) == [(ts * 8 + r, ts * 2 + r // 4) for r in range(8)]
+    # G = 1 (and 0) keep the one-cluster-per-tile order.
+    p.update(cluster_groups=1, grid=16 * S)
+    assert dlp.proj_plan_reduction_order(p, 3) == [(3 * 4 + r, -1) for r in range(4)]
+    assert plan(16, 2048, 8192)["cluster_groups"] == 1
+
+
 def test_cluster_split_plans():
     # 16 tiles of the 2048-row decode weight: clusters of 9 (144 CTAs; a
     # device lowers S until all 16 clusters fit at once).

@@ -102,6 +102,54 @@ def test_every_cluster_size(S, M, N, K, layout, bias, yd, half, monkeypatch):
     assert torch.equal(again.view(iv), Y.view(iv))
 
 
+@pytest.mark.parametrize("S,G,M,N,K,layout,bias,yd", [
+    (4, 2, 16, 2048, 8192, synth.W_NK, False, "f32"),   # 16 tiles x 2 clusters of 4 (128 CTAs)
+    (3, 3, 16, 2048, 8192, synth.W_NK, True, "bf16"),   # 16 tiles x 3 clusters of 3 (144 CTAs)
+    (2, 3, 9, 2500, 1032, synth.W_NK, True, "bf16"),    # ragged N, 17 k-blocks in 6 parts
+    (2, 2, 16, 3304, 1032, synth.W_KN, True, "f32"),    # [K,N] weights, 26 tiles
+    (4, 2, 100, 1024, 8192, synth.W_NK, True, "bf16"),  # two 64-token tiles
+], ids=lambda v: str(v))
+def test_cluster_groups_parity(S, G, M, N, K, layout, bias, yd, monkeypatch):
+    # Each tile's K range over G clusters of S CTAs: every cluster adds its
+    # ranks in shared memory, the G cluster sums meet in the scratch, and the
+    # cluster that completes last adds them in group order.  Oracle parity
+    # and bit-identical reruns (the arrival order of the clusters varies).
+    import torch
+    import dense_linear_projection_gb300 as dlp
+    monkeypatch.setenv("PROJ_FORCE_CLUSTER", str(S))
+    monkeypatch.setenv("PROJ_CLUSTER_GROUPS", str(G))
+    w = synth.Workload("t", M, N, K, layout, bias, yd, seed=90 + S * G)
+    inp = synth.make_inputs(w)
+    proj, Y, (X, W, b) = gu.run(w, inp)
+    pl = proj.plan
+    # A device that cannot hold every cluster at once falls back to one per tile.
+    assert pl["cluster_split"] == S and pl["cluster_groups"] in (1, G)
+    if pl["cluster_groups"] == G:
+        assert pl["grid"] == pl["tiles_sk"] * S * G
+    iv = torch.int16 if yd == "bf16" else torch.int32
+    runs = [proj(X, W, b).clone() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert proj.status() == dlp.PROJ_OK
+    r = oracle.project(inp["X"], inp["W"], w.w_layout, inp["bias"])
+    gu.assert_within_tol(gu.y_to_f64(Y), r, f"S={S} G={pl['cluster_groups']}")
+    for again in runs:
+        assert torch.equal(again.view(iv), Y.view(iv))
+
+
+def test_cluster_groups_on_the_decode_shape():
+    # The 2048-row decode weight in 2 clusters of 4 per tile fits GB300's
+    # SMs at once (32 clusters), so the grouped plan is the one that runs.
+    import os
+    import torch
+    import dense_linear_projection_gb300 as dlp
+    os.environ["PROJ_FORCE_CLUSTER"], os.environ["PROJ_CLUSTER_GROUPS"] = "4", "2"
+    try:
+        proj = dlp.Projection(16, 2048, 8192, dlp.PROJ_W_NK, dlp.PROJ_F32)
+    finally:
+        del os.environ["PROJ_FORCE_CLUSTER"], os.environ["PROJ_CLUSTER_GROUPS"]
+    assert (proj.plan["cluster_split"], proj.plan["cluster_groups"], proj.plan["grid"]) == (4, 2, 128)
+
+
 def test_handle_keeps_only_clusters_that_fit():
     # The 8192-row decode projection (64 tiles) runs in 64 clusters of 2 (all
     # resident at once on GB300); the 28672-row FFN weight (224 tiles) runs
