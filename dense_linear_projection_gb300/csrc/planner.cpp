@@ -177,7 +177,9 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 pbn = 2 * kBlockA;
             } else {
                 pbt = 2 * kBlockA;
-                if (force_block_n <= 0) {
+                if (force_block_n <= 0 && opt.pair_sk) {
+                    pbn = kMaxTokenTile;  // stream-K evens out the pairs' work
+                } else if (force_block_n <= 0) {
                     // As for single CTAs: per-pair time ~ waves x (block_n +
                     // a fixed share); the widest block_n wins ties.  Steps of
                     // 16 (each CTA holds half, a multiple of 8 rows): the QKV
@@ -227,13 +229,23 @@ proj_status_t plan_compute(int64_t M, int64_t N, int64_t K, proj_wlayout_t w_lay
                 out->block_k = pkpb * kBlockK;
                 out->k_blocks = ceil_div(K, out->block_k);
                 const int64_t tiles = out->tiles_m * out->tiles_n;
-                out->grid = static_cast<int32_t>(2 * (tiles < pairs_max ? tiles : pairs_max));
-                out->tiles_dp = tiles;
-                out->tiles_sk = 0;
-                out->units_sk = 0;
+                // Stream-K over pairs (option pair_sk, token-major): the last
+                // partial wave and one full wave before it are shared along K
+                // by all pairs, as for single CTAs.  A split tile's partial
+                // slots hold the pair's 256 rows; each CTA counts its own row
+                // quarters (8 counters a tile).
+                int64_t sk = 0;
+                if (opt.pair_sk && !swap && tiles % pairs_max != 0)
+                    sk = tiles < pairs_max ? tiles : tiles % pairs_max + pairs_max;
+                out->grid = static_cast<int32_t>(2 * (tiles < pairs_max && sk == 0 ? tiles : pairs_max));
+                out->tiles_dp = tiles - sk;
+                out->tiles_sk = sk;
+                out->units_sk = sk * out->k_blocks;
                 out->stages = pstages;
                 out->smem_bytes = pstages * pstage + kSmemReserve;
                 out->scratch_bytes = 256;  // the status word
+                if (sk > 0)
+                    out->scratch_bytes += int64_t(2) * out->grid * kBlockA * pb_rows * 4 + ((sk * 8 * 4 + 255) / 256) * 256;
                 return PROJ_OK;
             }
         }
@@ -473,14 +485,16 @@ extern "C" proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan,
         *count = G * S;
         return PROJ_OK;
     }
+    // Stream-K: CTAs (pairs, for a CTA-pair plan) in ascending order.
+    const int32_t g = plan->cta_pair ? plan->grid / 2 : plan->grid;
     int32_t first, last;
-    split_tile_ctas(ts, kt, plan->units_sk, plan->grid, first, last);
+    split_tile_ctas(ts, kt, plan->units_sk, g, first, last);
     int64_t n = 0;
     for (int32_t c = first; c <= last; ++c) {
-        if (!cta_has_units(c, plan->units_sk, plan->grid)) continue;
+        if (!cta_has_units(c, plan->units_sk, g)) continue;
         if (n < cap) {
             ctas[n] = c;
-            slots[n] = split_slot(c, ts, plan->units_sk, plan->grid, kt);
+            slots[n] = split_slot(c, ts, plan->units_sk, g, kt);
         }
         ++n;
     }

@@ -399,6 +399,9 @@ proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
         const int c = std::atoi(e);
         if (c >= 2 && c <= kMaxClusterSplit) opt.force_cluster = c;
     }
+    if (const char *e = std::getenv("PROJ_PAIR_SK")) {  // tuning only
+        if (std::atoi(e) == 1) opt.pair_sk = 1;
+    }
     if (const char *e = std::getenv("PROJ_CLUSTER_GROUPS")) {  // tuning only
         const int g = std::atoi(e);
         if (g >= 1 && g <= 16) opt.cluster_groups = g;

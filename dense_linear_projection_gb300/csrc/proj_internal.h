@@ -100,6 +100,11 @@ struct PlanOptions {
     // tokens whenever the clusters fit the SMs (PROJ_FORCE_CLUSTER; 0: the
     // planner's rule).
     int32_t force_cluster = 0;
+    // Stream-K over CTA pairs (PROJ_PAIR_SK=1): token-major pair tiles of
+    // 256 weight columns whose K ranges are shared by all pairs (the
+    // data-parallel + two-tile stream-K hybrid), instead of whole tiles of
+    // the width that best fills the pairs.  Off by default.
+    int32_t pair_sk = 0;
     // Clusters per tile of a swapped cluster split (PROJ_CLUSTER_GROUPS): 0
     // lets the planner choose, 1 forces one, G >= 2 forces G where the G·S
     // CTAs of every tile fit the SMs.
@@ -354,8 +359,8 @@ inline void params_from_plan(const proj_plan_desc_t &plan, KernelParams &kp) {
     kp.cta_pair = plan.cta_pair;
     kp.grid = plan.cta_pair ? plan.grid / 2 : plan.grid;  // pairs own tiles, not CTAs
     kp.units_sk = plan.units_sk;
-    kp.sk_pair = plan.grid > 0 && plan.units_sk / plan.grid >= plan.k_blocks;
-    kp.sk_dense = plan.units_sk >= plan.grid;
+    kp.sk_pair = kp.grid > 0 && plan.units_sk / kp.grid >= plan.k_blocks;
+    kp.sk_dense = plan.units_sk >= kp.grid;
     kp.cluster_split = plan.cluster_split;
     kp.cluster_groups = plan.cluster_split > 1 && plan.cluster_groups > 1 ? plan.cluster_groups : 1;
     if (kp.cluster_split > 1) kp.sk_pair = kp.sk_dense = 0;

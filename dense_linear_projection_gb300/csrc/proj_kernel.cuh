@@ -1313,7 +1313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     store_chunk(ch, v);
                 }
                 release_accumulator();
-            } else if (kFused && clustered && !p.swap) {
+            } else if (kFused && p.cluster_split > 1 && !p.swap) {
                 // Token-major cluster split (at most 32 tokens, so only row
                 // quarter 0 holds results; built into the fused instance
                 // only, which every such plan runs on, to keep the lean
@@ -1380,7 +1380,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 release_accumulator();
-            } else if (clustered) {
+            } else if (p.cluster_split > 1) {
+                // (Not `clustered`: a CTA pair is a cluster too, but its split
+                // tiles go through the scratch below.)
                 // Cluster split: the S CTAs of this cluster hold the tile's
                 // partial sums over consecutive K ranges (rank order = K
                 // order).  Quarter q is reduced by rank q mod S (S <= 4) or q
@@ -1513,8 +1515,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // Split tile.  This lane's row of fp32 partial sums goes to
                 // scratch, laid out [slot][128 rows][b_rows] (16 columns =
-                // 64 contiguous bytes per lane per chunk).
-                float *own = p.partials + (static_cast<size_t>(s.slot) * kBlockA + r) * p.b_rows;
+                // 64 contiguous bytes per lane per chunk).  A CTA pair's slot
+                // holds its 256 rows, each CTA writing and reading its own
+                // 128; each CTA counts its own row quarters.
+                auto partial_row = [&](int32_t slot) {
+                    return p.partials + (static_cast<size_t>(slot) * (kPair ? 2 : 1) * kBlockA +
+                                         (kPair ? pair_rank * kBlockA : 0u) + r) * p.b_rows;
+                };
+                float *own = partial_row(s.slot);
                 for (int32_t ch = 0; ch < nchunks; ++ch) {
                     float v[16];
                     tmem_load16(tbase + ch * 16, v);
@@ -1544,7 +1552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Publish (release) and count arrivals per 32-row quarter.
                 __syncwarp();
                 int last = 0;
-                uint32_t *ctr = p.counters + static_cast<size_t>(ts) * 4 + q;
+                uint32_t *ctr = p.counters + static_cast<size_t>(ts) * (kPair ? 8 : 4) + (kPair ? pair_rank * 4u : 0u) + q;
                 if (lane == 0) {
                     // One acquire-release add: releases this warp's partials
                     // (ordered before it by the __syncwarp above) and, for the
@@ -1564,7 +1572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // commutative, so the bits do not depend on who is last.
                     const int32_t other_slot =
                         s.kb0 == 0 ? 2 * (cta + 1) : 2 * (cta - 1) + 1;
-                    const float *other = p.partials + (static_cast<size_t>(other_slot) * kBlockA + r) * p.b_rows;
+                    const float *other = partial_row(other_slot);
                     for (int32_t ch0 = 0; ch0 < nchunks; ch0 += 4) {
                         float4 o[4][4];
 #pragma unroll
@@ -1607,7 +1615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         const int32_t slot =
                                             p.sk_dense ? (cc == c_first ? first_slot : 2 * cc)
                                                        : split_slot(cc, ts, U, p.grid, p.k_blocks);
-                                        load_partial16(p.partials + (static_cast<size_t>(slot) * kBlockA + r) * p.b_rows,
+                                        load_partial16(partial_row(slot),
                                                        ch, o[k]);
                                     }
                                 }

@@ -205,7 +205,8 @@ proj_status_t proj_plan_segments(const proj_plan_desc_t *plan, int32_t cta, proj
 /*
  * The order in which the partial sums of split tile `split_tile`
  * (0 ≤ split_tile < tiles_sk; tile index tiles_dp + split_tile) are added:
- * contributing CTAs in ascending order with their partial-sum slots.  Writes
+ * contributing CTAs (pair indices for a CTA-pair plan) in ascending order
+ * with their partial-sum slots.  Writes
  * min(cap, total) pairs and the total to *count.  For a cluster split the
  * CTAs are the tile's parts, split_tile·P .. split_tile·P + P − 1 (P = G·S,
  * G = max(1, cluster_groups)), each with slot −1 when G = 1, else with its
@@ -255,6 +256,7 @@ proj_status_t proj_plan_reduction_order(const proj_plan_desc_t *plan, int64_t sp
  *   PROJ_INFLIGHT_KB=n       stage bytes a weight-streaming plan keeps in flight per SM
  *   PROJ_FORCE_CLUSTER=s     cluster split of s CTAs per tile where the clusters fit the SMs
  *   PROJ_CLUSTER_GROUPS=g    g clusters per tile for a swapped cluster split (1: one)
+ *   PROJ_PAIR_SK=1           stream-K over CTA pairs for token-major pair tiles of 256 columns
  */
 proj_status_t proj_create(proj_handle_t *out, int64_t M, int64_t N, int64_t K,
                           proj_wlayout_t w_layout, proj_dtype_t x_dtype,
