@@ -665,10 +665,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // W is evict-first even where several token tiles reuse a weight
         // panel: the raster order runs those tiles in the same wave, in step
         // along K, so a panel's k-block is shared while it is in L2 anyway,
-        // and evicting it first keeps more of the raster group's token panels
-        // for the next wave.  (4096 x 8192 x 8192 on GB300: 460-540 MB of
-        // DRAM traffic a launch against 545-550 MB with evict-normal, same
-        // time.)
+        // and evicting it first leaves more of the L2 to the raster group's
+        // token panels.  (4096 x 8192 x 8192 on GB300: the same time as
+        // evict-normal; DRAM traffic varied more between GPUs than between
+        // the two hints.)
         pol_w = l2_policy_evict_first();
         pol_x = l2_policy_evict_last();  // X is reread by every CTA
         prod_it.init(p, cta);
