@@ -525,10 +525,16 @@ __device__ __forceinline__ void store_relaxed_gpu(uint32_t *ptr, uint32_t v) {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
-// The 16 columns [ch·16, ch·16+16) of one partial-sum row: four 16-byte loads
-// through L2 (partials are written by other SMs).
+// Partial sums in scratch are chunk-major: a slot of 128 rows x b_rows fp32
+// holds, for each 16-column chunk, the 128 rows' 16 values one after another
+// (64 bytes a row).  A warp's 32 rows of one chunk are then 2 KiB contiguous
+// however wide the tile; for a 16-column tile this is plain row order.
+constexpr int32_t kPartialChunkStride = kBlockA * 16;  // floats from one chunk to the next
+
+// Chunk ch of one partial-sum row (`row` points at the row's first chunk):
+// four 16-byte loads through L2 (partials are written by other SMs).
 __device__ __forceinline__ void load_partial16(const float *row, int32_t ch, float4 (&o)[4]) {
-    const float4 *src = reinterpret_cast<const float4 *>(row + ch * 16);
+    const float4 *src = reinterpret_cast<const float4 *>(row + ch * kPartialChunkStride);
 #pragma unroll
     for (int i = 0; i < 4; ++i) o[i] = __ldcg(src + i);
 }
@@ -1429,7 +1435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // (laid out like a split tile's partial) instead of Y.
                         const int32_t G = p.cluster_groups;
                         const int32_t grp = (cta / static_cast<int32_t>(S)) % G;
-                        float *mine = G > 1 ? p.partials + (static_cast<size_t>(s.tile * G + grp) * kBlockA + r) * p.b_rows
+                        float *mine = G > 1 ? p.partials + static_cast<size_t>(s.tile * G + grp) * kBlockA * p.b_rows + r * 16
                                             : nullptr;
                         for (int32_t ch = 0; ch < nchunks; ++ch) {
                             float own[16], acc[16];
@@ -1454,7 +1460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             }
                             if (G > 1) {
-                                float4 *dst = reinterpret_cast<float4 *>(mine + ch * 16);
+                                float4 *dst = reinterpret_cast<float4 *>(mine + ch * kPartialChunkStride);
 #pragma unroll
                                 for (int i = 0; i < 4; ++i)
                                     dst[i] = make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]);
@@ -1481,7 +1487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             last = __shfl_sync(0xFFFFFFFFu, last, 0);
                             __syncwarp();
                             if (last) {
-                                const float *g0 = p.partials + (static_cast<size_t>(s.tile * G) * kBlockA + r) * p.b_rows;
+                                const float *g0 = p.partials + static_cast<size_t>(s.tile * G) * kBlockA * p.b_rows + r * 16;
                                 const size_t gstride = static_cast<size_t>(kBlockA) * p.b_rows;
                                 for (int32_t ch = 0; ch < nchunks; ++ch) {
                                     float sum[16];
@@ -1514,19 +1520,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // Split tile.  This lane's row of fp32 partial sums goes to
-                // scratch, laid out [slot][128 rows][b_rows] (16 columns =
-                // 64 contiguous bytes per lane per chunk).  A CTA pair's slot
-                // holds its 256 rows, each CTA writing and reading its own
-                // 128; each CTA counts its own row quarters.
+                // scratch: slot [128 rows x b_rows], chunk-major (see
+                // kPartialChunkStride).  A CTA pair's slot holds its 256 rows
+                // as two such halves, each CTA writing and reading its own;
+                // each CTA counts its own row quarters.
                 auto partial_row = [&](int32_t slot) {
-                    return p.partials + (static_cast<size_t>(slot) * (kPair ? 2 : 1) * kBlockA +
-                                         (kPair ? pair_rank * kBlockA : 0u) + r) * p.b_rows;
+                    return p.partials +
+                           (static_cast<size_t>(slot) * (kPair ? 2 : 1) + (kPair ? pair_rank : 0u)) * kBlockA * p.b_rows +
+                           r * 16;
                 };
                 float *own = partial_row(s.slot);
                 for (int32_t ch = 0; ch < nchunks; ++ch) {
                     float v[16];
                     tmem_load16(tbase + ch * 16, v);
-                    float4 *dst = reinterpret_cast<float4 *>(own + ch * 16);
+                    float4 *dst = reinterpret_cast<float4 *>(own + ch * kPartialChunkStride);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
                         dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
