@@ -199,6 +199,34 @@ def test_cluster_group_decomposition():
     assert plan(16, 2048, 8192)["cluster_groups"] == 1
 
 
+def test_pair_stream_k_decomposition():
+    # Stream-K over CTA pairs (option PROJ_PAIR_SK): the QKV shape as 48
+    # token-major pair tiles of 256 columns shared along K by all 76 pairs.
+    # Both CTAs of a pair run the same segments; every (tile, k-block) is
+    # covered once per pair; the reduction order lists pair indices in K order
+    # with unique slots (2·pair for a pair's first split segment, 2·pair + 1
+    # for its last).
+    p = dict(dlp.proj_plan_compute(256, 12288, 4096, 1))
+    KT = p["k_blocks"]
+    p.update(block_n=256, tiles_n=48, grid=152, tiles_dp=0, tiles_sk=48, units_sk=48 * KT)
+    cover = np.zeros((48, KT), dtype=np.int32)
+    for c in range(0, 152, 2):
+        segs = dlp.proj_plan_segments(p, c)
+        assert segs == dlp.proj_plan_segments(p, c + 1)
+        for (tile, tm, tn, kb0, kb1, slot, split) in segs:
+            cover[tile, kb0:kb1] += 1
+            assert split == 1 and slot in (2 * (c // 2), 2 * (c // 2) + 1)
+    assert (cover == 1).all()
+    for ts in range(48):
+        order = dlp.proj_plan_reduction_order(p, ts)
+        pairs = [c for c, _ in order]
+        assert pairs == sorted(pairs) and 2 <= len(order) <= 3
+        assert len({sl for _, sl in order}) == len(order)
+        segs = sorted((kb0, c // 2) for c in range(0, 152, 2)
+                      for (tile, _, _, kb0, _, _, _) in dlp.proj_plan_segments(p, c) if tile == ts)
+        assert pairs == [q for _, q in segs]
+
+
 def test_cluster_split_plans():
     # 16 tiles of the 2048-row decode weight: clusters of 9 (144 CTAs; a
     # device lowers S until all 16 clusters fit at once).
